@@ -1,0 +1,89 @@
+"""Decode attention over the compressed cache (oracle; test infrastructure only).
+
+Sources:
+  * XQuant page ("XQuant KV Cache Rematerialization"), step 4 "Implement On-the-Fly
+    K, V Recomputation": scores = Q K^T / sqrt(head_dim), softmax over the keys,
+    context = weights V.  That plain definition is what is computed here.
+  * FoveatedKV page, section "The VR headset thing": every token of every tier
+    contributes to one softmax, so its denominator stays correct.
+
+Steps, in this order, all in float64:
+  1. read every stored row of the sequence's kv head from each tier and dequantise
+     it (codebook: fp16 norm * C[idx] / sqrt(d); fp16; fp8 E4M3; (nibble-8) * scale);
+  2. undo the rotation, x = s * H x~ / sqrt(d), to get keys and values in the
+     original domain;
+  3. for every query head of the group (query head h reads kv head h // (Hq/Hkv)),
+     plain softmax(q K^T / sqrt(d)) V over all tokens of all tiers.
+
+Readings taken: decode attends to the whole cache (no causal or window mask: the
+query is the newest token); the output is float32; a sequence with no cached
+token gives a zero output.  The oracle does not use the rotated-domain scores, a
+lookup table, split-K or an online softmax; that those give the same result is
+what the GPU tests check.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Sequence
+
+import numpy as np
+
+from . import cache
+
+
+@dataclasses.dataclass
+class TierState:
+    """One precision tier: K and V sides, block tables and per-sequence lengths."""
+
+    k: cache.Side
+    v: cache.Side
+    block_table: np.ndarray  # int32 [B, max_pages]
+    lens: np.ndarray  # [B]
+    page_size: int
+
+
+def dequantised_kv(tiers: Sequence[TierState], b: int, g: int):
+    """Keys and values (float64 [L_total, d], original domain) of sequence b, kv head g,
+    concatenated over the tiers."""
+    ks, vs = [], []
+    for t in tiers:
+        n = int(t.lens[b])
+        if n == 0:
+            continue
+        ks.append(cache.read(t.k, t.block_table[b], n, g, t.page_size))
+        vs.append(cache.read(t.v, t.block_table[b], n, g, t.page_size))
+    if not ks:
+        return None, None
+    return np.concatenate(ks, axis=0), np.concatenate(vs, axis=0)
+
+
+def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray) -> np.ndarray:
+    """softmax(q K^T / sqrt(d)) V for one query vector q [d] (float64)."""
+    d = q.shape[-1]
+    scores = keys @ np.asarray(q, dtype=np.float64) / math.sqrt(d)
+    w = np.exp(scores - np.max(scores))  # the shift cancels in the normalisation
+    w = w / np.sum(w)
+    return w @ values
+
+
+def decode_attention(q16: np.ndarray, tiers: Sequence[TierState],
+                     heads: Sequence[tuple] | None = None) -> np.ndarray:
+    """Decode attention for queries q16 [B, Hq, d] (fp16).  Returns float32 [B, Hq, d].
+    heads: optional list of (b, h_q) to compute; the other outputs stay zero."""
+    bsz, hq, d = q16.shape
+    hkv = tiers[0].k.signs.shape[0]
+    grp = hq // hkv
+    out = np.zeros((bsz, hq, d), dtype=np.float64)
+    want = set(heads) if heads is not None else None
+    for b in range(bsz):
+        for g in range(hkv):
+            todo = [h for h in range(g * grp, (g + 1) * grp) if want is None or (b, h) in want]
+            if not todo:
+                continue
+            keys, values = dequantised_kv(tiers, b, g)
+            if keys is None:
+                continue
+            for h in todo:
+                out[b, h] = attend(q16[b, h].astype(np.float64), keys, values)
+    return out.astype(np.float32)

@@ -1,0 +1,242 @@
+"""Seeded synthetic inputs for the rotate-then-quantize KV-cache decode path.
+
+This module is the one piece shared by the CPU oracle (``oracle/``), the CUDA
+path's tests and ``bench.py``.  It holds NO arithmetic of the method itself:
+no rotation, no quantisation, no attention.  It only draws random numbers and
+lays out shapes, so that both sides receive byte-identical inputs.
+
+Every random draw comes from a numpy PCG64 stream keyed by
+``SeedSequence([config seed, stream id, *indices])``, so that the K/V of one
+(sequence, kv head) can be regenerated on its own: the oracle recomputes a few
+sampled heads of a multi-gigabyte workload without materialising the rest.
+
+Workload shapes follow the pages' own workloads:
+  * "Shrinking the LLM KV Cache by 8x on CPU: AdapTQ" (The Results): 4-bit
+    rotated codes, 4096-token contexts.
+  * "FoveatedKV" (Results table): 7B GQA shapes, H_kv=8, H_q=32, D=128,
+    contexts 1K..32K, top 10% of tokens fp16 and the rest fp8-E4M3 keys plus
+    INT4 values.
+  * "I Ported a Google Research Paper to Apple Silicon" (VeloxQuant-MLX,
+    Installing and Using It): fp16 keys/values ~ N(0,1), head_dim 128.
+The pages' model activations are not available, so K/V are Gaussian (or
+Student-t) with planted outlier channels, the property the pages' rotation is
+meant to tame ("The Problem: The Tyranny of Outliers", AdapTQ page).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+# Stream ids: one independent PCG64 stream family per kind of draw.
+S_K, S_V, S_Q, S_OUTLIER, S_TIER, S_LENS, S_PAGES, S_SIGNS, S_SIGMA, S_NEWTOK = range(10)
+
+# Storage format names (the same four the C header enumerates).
+CODEBOOK, FP16, FP8_E4M3, INT4_G32 = "codebook", "fp16", "fp8_e4m3", "int4_g32"
+
+
+@dataclasses.dataclass(frozen=True)
+class Tier:
+    """One precision tier of the cache: how K and V rows of its tokens are stored."""
+
+    k_format: str
+    v_format: str
+    k_bits: int = 0  # code bits, codebook format only
+    v_bits: int = 0
+    codebook: str = "lloyd_max"  # or "uniform"
+    fraction: float = 1.0  # share of each (sequence, kv head)'s tokens held here
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    seq_len: int  # every sequence's length (upper bound when ragged)
+    tiers: Tuple[Tier, ...]
+    seed: int
+    ragged_min: int = 0  # >0: lengths uniform in [ragged_min, seq_len]
+    kv_dist: str = "normal"  # "normal" | "student_t4" | "normal_channel_sigma"
+    outlier_mode: str = "none"  # "fixed_channels" | "pairs" | "none"
+    outlier_count: int = 0
+    outlier_scale: float = 1.0
+    page_size: int = 16
+    shuffle_pages: bool = False
+    prefill_chunk: int = 0  # tokens quantised-and-appended after the first seq_len
+    decode_steps: int = 0
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    def scaled(self, **kw) -> "Config":
+        return dataclasses.replace(self, **kw)
+
+
+LM4 = Tier(CODEBOOK, CODEBOOK, 4, 4)
+
+CONFIGS: Dict[str, Config] = {
+    # tiny: B1, 8/8 heads, D128, ctx 1024, 4 fixed outlier channels x20, 4-bit LM K and V, seed 0
+    "tiny": Config("tiny", 1, 8, 8, 128, 1024, (LM4,), seed=0,
+                   outlier_mode="fixed_channels", outlier_count=4, outlier_scale=20.0),
+    # Llama-7B-shaped layer: B8, 32/32 heads, D128, ctx 8192, 1% outlier channels x50, 4-bit LM
+    "llama7b": Config("llama7b", 8, 32, 32, 128, 8192, (LM4,), seed=1,
+                      outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
+    # GQA long-context: B32, 32/8 heads, D128, ctx 32768; top 10% fp16, rest fp8 K + INT4-g32 V
+    "gqa32k": Config("gqa32k", 32, 32, 8, 128, 32768,
+                     (Tier(FP16, FP16, fraction=0.1), Tier(FP8_E4M3, INT4_G32, fraction=0.9)),
+                     seed=2, outlier_mode="pairs", outlier_count=10, outlier_scale=30.0),
+    # ragged: 64 sequences, lengths U[512, 65536], 32/8 heads, 3-bit LM K / 2-bit LM V,
+    # 16-token pages in shuffled order, Student-t(4)/sqrt(2)
+    "ragged": Config("ragged", 64, 32, 8, 128, 65536, (Tier(CODEBOOK, CODEBOOK, 3, 2),),
+                     seed=3, ragged_min=512, kv_dist="student_t4", shuffle_pages=True),
+    # append + decode: B4, 16/16 heads, D256, ctx 131072 + 16384-token chunk, 4-bit LM,
+    # 128 decode steps, per-channel std log-uniform in [0.1, 10]
+    "append": Config("append", 4, 16, 16, 256, 131072, (LM4,), seed=4,
+                     kv_dist="normal_channel_sigma", prefill_chunk=16384, decode_steps=128),
+}
+
+
+def rng(cfg: Config, stream: int, *idx: int) -> np.random.Generator:
+    return np.random.default_rng(np.random.SeedSequence([cfg.seed, stream, *idx]))
+
+
+# ----------------------------------------------------------------------------- lengths
+
+
+def seq_lens(cfg: Config) -> np.ndarray:
+    """Total context length of every sequence (int64 [B])."""
+    if cfg.ragged_min > 0:
+        return rng(cfg, S_LENS).integers(cfg.ragged_min, cfg.seq_len, size=cfg.batch,
+                                         endpoint=True).astype(np.int64)
+    return np.full(cfg.batch, cfg.seq_len, dtype=np.int64)
+
+
+def tier_lens(cfg: Config, total: int) -> List[int]:
+    """Tokens per tier for one (sequence, kv head) of `total` tokens.  The first tier
+    gets round(fraction*total); the last tier takes the rest."""
+    out, left = [], total
+    for i, t in enumerate(cfg.tiers):
+        n = left if i == len(cfg.tiers) - 1 else min(left, int(round(t.fraction * total)))
+        out.append(n)
+        left -= n
+    return out
+
+
+# ----------------------------------------------------------------------------- values
+
+
+def outlier_multipliers(cfg: Config) -> np.ndarray:
+    """float32 [Hkv, D] channel multipliers (1 everywhere but the outlier channels).
+    The same channels are applied to K and V."""
+    m = np.ones((cfg.num_kv_heads, cfg.head_dim), dtype=np.float32)
+    if cfg.outlier_mode == "fixed_channels":
+        ch = rng(cfg, S_OUTLIER).permutation(cfg.head_dim)[: cfg.outlier_count]
+        m[:, ch] = cfg.outlier_scale
+    elif cfg.outlier_mode == "pairs":
+        flat = rng(cfg, S_OUTLIER).choice(cfg.num_kv_heads * cfg.head_dim,
+                                          size=cfg.outlier_count, replace=False)
+        m.reshape(-1)[flat] = cfg.outlier_scale
+    return m
+
+
+def channel_sigma(cfg: Config, which: int) -> np.ndarray:
+    """float32 [Hkv, D] per-channel std, log-uniform in [0.1, 10] (K and V drawn apart)."""
+    r = rng(cfg, S_SIGMA, which)
+    return np.exp(r.uniform(math.log(0.1), math.log(10.0),
+                            size=(cfg.num_kv_heads, cfg.head_dim))).astype(np.float32)
+
+
+def _draw(cfg: Config, r: np.random.Generator, n: int) -> np.ndarray:
+    if cfg.kv_dist == "student_t4":
+        return (r.standard_t(4.0, size=(n, cfg.head_dim)) / math.sqrt(2.0)).astype(np.float32)
+    return r.standard_normal((n, cfg.head_dim), dtype=np.float32)
+
+
+def kv_head(cfg: Config, which: int, b: int, h: int, n: int, stream: int = -1) -> np.ndarray:
+    """fp16 [n, D] keys (which=0) or values (which=1) of sequence b, kv head h.
+    `stream` selects a separate family (used for appended / decode-step tokens)."""
+    key = (S_K if which == 0 else S_V)
+    r = rng(cfg, key, b, h) if stream < 0 else rng(cfg, S_NEWTOK, which, stream, b, h)
+    x = _draw(cfg, r, n)
+    if cfg.kv_dist == "normal_channel_sigma":
+        x *= channel_sigma(cfg, which)[h]
+    x *= outlier_multipliers(cfg)[h]
+    return x.astype(np.float16)
+
+
+def queries(cfg: Config, step: int = 0) -> np.ndarray:
+    """fp16 [B, Hq, D] decode queries, q ~ N(0, 1)."""
+    r = rng(cfg, S_Q, step)
+    return r.standard_normal((cfg.batch, cfg.num_q_heads, cfg.head_dim),
+                             dtype=np.float32).astype(np.float16)
+
+
+def signs(cfg: Config, which: int, layer: int = 0) -> np.ndarray:
+    """int8 [Hkv, D] Rademacher signs (+1/-1) for K (which=0) or V (which=1), drawn
+    independently per (layer, kv head, K|V).  They are an input of the method."""
+    r = rng(cfg, S_SIGNS, layer, which)
+    return np.where(r.integers(0, 2, size=(cfg.num_kv_heads, cfg.head_dim)) == 0,
+                    1, -1).astype(np.int8)
+
+
+def tier_members(cfg: Config, b: int, h: int, total: int) -> List[np.ndarray]:
+    """Token positions (sorted) held by each tier for sequence b, kv head h.  With one
+    tier all tokens are in it; otherwise the first tier takes the tokens with the highest
+    seeded U(0,1) score (ties cannot occur with continuous draws) and the rest follow."""
+    lens = tier_lens(cfg, total)
+    if len(cfg.tiers) == 1:
+        return [np.arange(total)]
+    score = rng(cfg, S_TIER, b, h).random(total)
+    order = np.argsort(-score, kind="stable")
+    out, at = [], 0
+    for n in lens:
+        out.append(np.sort(order[at: at + n]))
+        at += n
+    return out
+
+
+# ----------------------------------------------------------------------------- paging
+
+
+@dataclasses.dataclass
+class PageMap:
+    """Block tables of one tier: physical page of logical page p of sequence b."""
+
+    block_table: np.ndarray  # int32 [B, max_pages], -1 where unused
+    lens: np.ndarray  # int64 [B] tokens held per sequence in this tier
+    num_pages: int
+    page_size: int
+
+    def slots(self, b: int, positions: np.ndarray) -> np.ndarray:
+        """Pool slot (physical page * page_size + offset) of token positions of seq b."""
+        positions = np.asarray(positions, dtype=np.int64)
+        page = self.block_table[b, positions // self.page_size].astype(np.int64)
+        return (page * self.page_size + positions % self.page_size).astype(np.int32)
+
+
+def page_map(cfg: Config, lens: np.ndarray, tier: int = 0, spare_pages: int = 0) -> PageMap:
+    """Assign physical pages to every sequence.  Identity order unless the config shuffles
+    pages (then a seeded permutation of the pool)."""
+    ps = cfg.page_size
+    per = [(int(n) + ps - 1) // ps for n in lens]
+    total = sum(per) + spare_pages
+    phys = np.arange(total, dtype=np.int32)
+    if cfg.shuffle_pages:
+        phys = rng(cfg, S_PAGES, tier).permutation(total).astype(np.int32)
+    maxp = max(1, max(per) if per else 1)
+    bt = np.full((len(lens), maxp), -1, dtype=np.int32)
+    at = 0
+    for b, n in enumerate(per):
+        bt[b, :n] = phys[at: at + n]
+        at += n
+    return PageMap(bt, np.asarray(lens, dtype=np.int64), total, ps)
+
+
+def kv_bytes_fp16(cfg: Config, total_tokens: int) -> int:
+    """Bytes of an unquantised fp16 K+V cache holding `total_tokens` per kv head."""
+    return total_tokens * cfg.num_kv_heads * cfg.head_dim * 2 * 2
