@@ -19,7 +19,8 @@ Readings taken (the page leaves them open):
   * quadrature: composite trapezoid on a fixed grid of step 2^-17 over the support;
     each cell uses the grid nodes strictly inside it plus its two end points.
   * "uniform b-bit codes": symmetric levels c_i = (i - (n-1)/2) * delta, the step
-    delta minimising the N(0,1) mean squared error, boundaries at midpoints.
+    delta minimising the N(0,1) mean squared error (the root of its derivative),
+    boundaries at midpoints.
 
 Tables handed to the quantiser are float32: C32 = fp32(c) and the decision
 boundaries Bd32_i = fp32((C32_i + C32_{i+1}) / 2), computed from the float32
@@ -103,25 +104,33 @@ def uniform_mse(delta: float, n: int) -> float:
     return float(np.sum(cell))
 
 
+def uniform_mse_slope(delta: float, n: int) -> float:
+    """d MSE / d delta of the symmetric uniform quantiser, in closed form.  With level
+    c_i = k_i delta (k_i = i - (n-1)/2) on cell [a_i, b_i], the boundary terms of the
+    derivative cancel (midpoints are equidistant from both levels), leaving
+    -2 sum_i k_i [ phi(a_i) - phi(b_i) - k_i delta (Phi(b_i) - Phi(a_i)) ]."""
+    k = np.arange(n) - (n - 1) / 2.0
+    a = np.where(np.arange(n) == 0, -np.inf, (k - 0.5) * delta)
+    b = np.where(np.arange(n) == n - 1, np.inf, (k + 0.5) * delta)
+    pa = np.where(np.isfinite(a), normal_pdf(np.where(np.isfinite(a), a, 0.0)), 0.0)
+    pb = np.where(np.isfinite(b), normal_pdf(np.where(np.isfinite(b), b, 0.0)), 0.0)
+    return float(-2.0 * np.sum(k * (pa - pb - k * delta * (ndtr(b) - ndtr(a)))))
+
+
 def uniform_codebook(bits: int) -> Tuple[np.ndarray, np.ndarray, float]:
-    """Symmetric uniform levels with the MSE-optimal step, found by golden-section search.
+    """Symmetric uniform levels with the MSE-optimal step: the root of d MSE / d delta,
+    found by bisection (the slope is negative below the optimum and positive above).
     Returns (centroids, boundaries, delta)."""
     n = 2 ** bits
-    lo, hi = 1e-3, 8.0 / max(1, n - 1) * 2.0
-    gr = (math.sqrt(5.0) - 1.0) / 2.0
-    a, b = lo, hi
-    x1, x2 = b - gr * (b - a), a + gr * (b - a)
-    f1, f2 = uniform_mse(x1, n), uniform_mse(x2, n)
-    while b - a > 1e-13:
-        if f1 < f2:
-            b, x2, f2 = x2, x1, f1
-            x1 = b - gr * (b - a)
-            f1 = uniform_mse(x1, n)
+    lo, hi = 1e-3, 2.0 * 8.0 / max(1, n - 1)
+    assert uniform_mse_slope(lo, n) < 0 < uniform_mse_slope(hi, n)
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        if uniform_mse_slope(mid, n) < 0:
+            lo = mid
         else:
-            a, x1, f1 = x1, x2, f2
-            x2 = a + gr * (b - a)
-            f2 = uniform_mse(x2, n)
-    delta = (a + b) / 2.0
+            hi = mid
+    delta = 0.5 * (lo + hi)
     c = (np.arange(n) - (n - 1) / 2.0) * delta
     return c, (c[:-1] + c[1:]) / 2.0, delta
 
