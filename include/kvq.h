@@ -1,0 +1,183 @@
+/*
+ * kvq.h -- rotate-then-quantize KV-cache compression and decode attention that reads
+ * the compressed cache directly.  C ABI of libkvq.so (CUDA, sm_103a / GB300).
+ *
+ * The method (sources named by page title and section):
+ *   - "Shrinking the LLM KV Cache by 8x on CPU: The Engineering Behind AdapTQ",
+ *     "The Math Fix: Hadamard Accelerated Rotation (HAR)": a random sign flip and a
+ *     Fast Walsh-Hadamard Transform spread outlier energy over all coordinates before
+ *     scalar quantisation; "Engineering the Hot Path": the query is rotated once and
+ *     the attention loop never expands the cache back to full precision.
+ *   - "I Ported a Google Research Paper to Apple Silicon" (VeloxQuant-MLX), "Stage 1:
+ *     Random Rotation" (x~ = H diag(s) x / sqrt(d)), "Stage 2: Lloyd-Max Scalar
+ *     Quantization" (unit norm, fp16 norm, nearest Lloyd-Max centroid per coordinate),
+ *     "The Bit-Packing Problem" (little-endian bit stream per vector).
+ *   - "FoveatedKV", "The VR headset thing" (a near tier of fp16 tokens and a far tier of
+ *     fp8 E4M3 keys and INT4 values, all in one softmax) and "Making it fast" (one fused
+ *     split-K dispatch over both tiers, query pre-scaled by 1/sqrt(D), online softmax
+ *     computing each exp once).
+ *   - "XQuant KV Cache Rematerialization", step 4: scores = q K^T / sqrt(d), softmax,
+ *     times V -- the result every entry point below must reproduce.
+ *
+ * Conventions that hold for every function:
+ *   - Pointers are DEVICE pointers unless the comment says "host".
+ *   - The caller owns every buffer.  The library allocates nothing, keeps no mutable
+ *     global state, never synchronises, and is safe to call from several threads.
+ *   - GPU work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and ordered with the caller's other work on that stream.
+ *   - Arguments are checked on the host before anything is launched; a failed check
+ *     returns a status != KVQ_OK and launches nothing.  A launch failure returns
+ *     KVQ_ERR_CUDA.  Faults inside a kernel surface at the caller's next synchronisation.
+ *   - fp16 data is passed as raw IEEE binary16 bits (uint16_t).
+ *   - Inputs must be finite.  Outputs must not alias inputs.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_API __attribute__((visibility("default")))
+
+#define KVQ_MAX_TIERS 4  /* decode attends over at most this many tiers at once */
+#define KVQ_INT4_GROUP 32 /* coordinates sharing one fp16 scale in KVQ_FMT_INT4_G32 */
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size, misaligned buffer       */
+  KVQ_ERR_UNSUPPORTED = 2,        /* valid but not built: head_dim, bits, format pair */
+  KVQ_ERR_WORKSPACE_TOO_SMALL = 3,
+  KVQ_ERR_CUDA = 4                /* a CUDA launch or runtime call failed            */
+} kvq_status;
+
+/* How the rows of one side (K or V) of a tier are stored.  Every format stores the
+ * ROTATED vector x~ = H diag(s) x / sqrt(D) of the fp16 input x.
+ *   KVQ_FMT_CODEBOOK : b-bit indices (b = 2, 3, 4) of the nearest centroid of
+ *                      u = sqrt(D) x~ / ||x~||, packed little-endian (element j in bits
+ *                      j*b .. j*b+b-1 of the row's bit stream, bit k of the stream is
+ *                      bit k%8 of byte k/8); side data: fp16 ||x~|| per row.  Decodes
+ *                      to ||x~||_fp16 * C[idx] / sqrt(D).
+ *   KVQ_FMT_FP16     : x~ rounded to fp16 (near tier).
+ *   KVQ_FMT_FP8_E4M3 : x~ rounded to OCP fp8 E4M3, nearest-even, saturating at +-448
+ *                      (far-tier keys).
+ *   KVQ_FMT_INT4_G32 : per 32 consecutive coordinates, s = fp16(max|x~| / 7) and
+ *                      q = clamp(rint(x~ / s), -7, 7) stored as the nibble q + 8
+ *                      (even coordinate in the low nibble); side data: the fp16 scales
+ *                      (far-tier values).
+ * Rounding decisions are taken on float32 values. */
+typedef enum kvq_format {
+  KVQ_FMT_CODEBOOK = 0,
+  KVQ_FMT_FP16 = 1,
+  KVQ_FMT_FP8_E4M3 = 2,
+  KVQ_FMT_INT4_G32 = 3
+} kvq_format;
+
+/* One tier of a paged cache.  A token of a sequence at position t lives in physical
+ * page block_table[t / page_size] at slot t % page_size; "slot" = page * page_size +
+ * offset addresses the pool directly.
+ *   rows : uint8 [num_pages][num_kv_heads][page_size][row_bytes], 16-byte aligned
+ *   aux  : fp16  [num_pages][num_kv_heads][page_size]          (codebook: norms)
+ *          fp16  [num_pages][num_kv_heads][page_size][D/32]     (INT4: group scales)
+ *          unused (may be NULL) for fp16 / fp8.
+ * row_bytes / aux bytes per row come from kvq_row_bytes().  Codebook tables are fp32:
+ * centroids [2^bits] increasing, bounds [2^bits - 1] with centroids[i] < bounds[i] <
+ * centroids[i+1]; a coordinate gets the index #{i : u > bounds[i]}.  Signs are the
+ * Rademacher diagonal, int8 +1/-1 [num_kv_heads][head_dim]; every tier attended in one
+ * decode call must use the same K signs and the same V signs. */
+typedef struct kvq_cache {
+  int32_t head_dim;     /* D: 128 or 256 */
+  int32_t num_kv_heads; /* Hkv >= 1 */
+  int32_t page_size;    /* tokens per page, 16 */
+  int32_t num_pages;    /* pages in the pool */
+  int32_t k_format;     /* kvq_format of keys   */
+  int32_t v_format;     /* kvq_format of values */
+  int32_t k_bits;       /* 2, 3 or 4 when k_format == KVQ_FMT_CODEBOOK, else ignored */
+  int32_t v_bits;
+  void* k_rows;
+  void* v_rows;
+  void* k_aux;
+  void* v_aux;
+  const float* k_centroids; /* codebook format only */
+  const float* k_bounds;
+  const float* v_centroids;
+  const float* v_bounds;
+  const int8_t* k_signs;
+  const int8_t* v_signs;
+} kvq_cache;
+
+/* One tier as seen by a decode call: the cache plus each sequence's pages and length.
+ *   block_table : int32 [batch][max_pages]; entries past a sequence's length unused
+ *   seq_lens    : int32 [batch], 0 <= seq_lens[b] <= max_pages * page_size           */
+typedef struct kvq_tier_view {
+  const kvq_cache* cache; /* host pointer */
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int32_t max_pages;
+} kvq_tier_view;
+
+/* Human-readable name of a status.  Never NULL. */
+KVQ_API const char* kvq_status_string(kvq_status status);
+
+/* Bytes of one stored row and of its side data (host outputs) for a format, code bits
+ * and head_dim.  Layouts are those of kvq_format above. */
+KVQ_API kvq_status kvq_row_bytes(int32_t format, int32_t bits, int32_t head_dim,
+                                 size_t* row_bytes, size_t* aux_bytes);
+
+/* Lloyd-Max codebook for N(0,1) with 2^bits levels (bits 1..8), computed on the host in
+ * double precision: boundaries at the midpoints of neighbouring centroids, each centroid
+ * the conditional mean of N(0,1) over its cell (VeloxQuant-MLX page, "Stage 2"), the
+ * outer cells ending at +-8.  host centroids [2^bits], host bounds [2^bits - 1]. */
+KVQ_API kvq_status kvq_lloyd_max_codebook(int32_t bits, double* centroids, double* bounds);
+
+/* Symmetric uniform codebook c_i = (i - (2^bits - 1)/2) * delta with the step delta that
+ * minimises the N(0,1) mean squared error; boundaries at midpoints.  Host outputs. */
+KVQ_API kvq_status kvq_uniform_codebook(int32_t bits, double* centroids, double* bounds);
+
+/* float32 tables for the device: centroids32[i] = (float)centroids[i] and bounds32[i] =
+ * (float)(((double)centroids32[i] + centroids32[i+1]) / 2).  All host arrays. */
+KVQ_API kvq_status kvq_codebook_tables(int32_t bits, const double* centroids,
+                                       float* centroids32, float* bounds32);
+
+/* Quantise-and-append (one launch): for every token i < num_tokens and kv head h, rotate
+ * k[i][h][:] (fp16, [num_tokens][num_kv_heads][head_dim]) with k_signs[h], encode it in
+ * cache->k_format and store it at pool slot slot_mapping[i]; the same for v with v_signs.
+ * k or v may be NULL to append only the other side.  slot_mapping: int32 [num_tokens];
+ * a negative slot skips the token; slots >= num_pages * page_size are skipped too.
+ * Two tokens of one call must not share a slot.  k, v: 16-byte aligned. */
+KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k,
+                                       const uint16_t* v, int32_t num_tokens,
+                                       const int32_t* slot_mapping, void* stream);
+
+/* Workspace bytes kvq_decode_attention needs for these tiers and shapes (host output).
+ * split_tokens: tokens per split-K chunk (a multiple of page_size), or 0 to let the
+ * library choose; pass the same value to kvq_decode_attention. */
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t num_tiers,
+                                             int32_t batch, int32_t num_q_heads,
+                                             int32_t split_tokens, size_t* bytes);
+
+/* Decode attention for one new query per sequence over all tiers (two launches: a fused
+ * split-K pass over every tier, then a combine pass):
+ *   out[b][h] = softmax_t( q[b][h] . K[t] / sqrt(D) ) V[t]
+ * over every cached token t < seq_lens[b] of every tier of kv head h / (Hq / Hkv), where
+ * K[t], V[t] are the dequantised cache rows with the rotation undone.  The query is
+ * rotated with the K signs inside the kernel and the result is rotated back with the V
+ * signs, so the cache is never expanded.  A sequence with no cached token gives zeros.
+ *   tiers : host array [num_tiers], 1..KVQ_MAX_TIERS, same head_dim / num_kv_heads
+ *   q     : fp16 [batch][num_q_heads][head_dim]; num_q_heads / num_kv_heads in {1,2,4,8}
+ *   out   : fp32 [batch][num_q_heads][head_dim]
+ *   workspace : >= kvq_decode_workspace_size() bytes, 256-byte aligned, scratch only. */
+KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_tiers,
+                                        const uint16_t* q, int32_t batch,
+                                        int32_t num_q_heads, int32_t split_tokens,
+                                        float* out, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,247 @@
+"""Rotate-then-quantize KV-cache compression and decode attention for GB300 (sm_103a).
+
+This module is a thin ctypes binding over ``libkvq.so`` (C ABI in ``include/kvq.h``):
+each ``kvq_*`` function here marshals torch tensors (device pointers, the current CUDA
+stream) into the C call of the same name and raises ``KvqError`` on a failed status.
+All arithmetic of the method runs in the library's CUDA kernels; there is no CPU path.
+PyTorch is used for device memory and streams only.
+
+``PagedCache`` is a convenience owner of one tier's device buffers (pool rows, side
+data, codebook tables, signs) laid out as the header describes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+FMT_CODEBOOK, FMT_FP16, FMT_FP8_E4M3, FMT_INT4_G32 = 0, 1, 2, 3
+FORMATS = {"codebook": FMT_CODEBOOK, "fp16": FMT_FP16, "fp8_e4m3": FMT_FP8_E4M3, "int4_g32": FMT_INT4_G32}
+MAX_TIERS = 4
+INT4_GROUP = 32
+
+STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARGUMENT", 2: "KVQ_ERR_UNSUPPORTED",
+          3: "KVQ_ERR_WORKSPACE_TOO_SMALL", 4: "KVQ_ERR_CUDA"}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class KvqCache(ctypes.Structure):
+    """Mirror of ``struct kvq_cache``."""
+
+    _fields_ = [
+        ("head_dim", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("k_format", ctypes.c_int32), ("v_format", ctypes.c_int32),
+        ("k_bits", ctypes.c_int32), ("v_bits", ctypes.c_int32),
+        ("k_rows", ctypes.c_void_p), ("v_rows", ctypes.c_void_p),
+        ("k_aux", ctypes.c_void_p), ("v_aux", ctypes.c_void_p),
+        ("k_centroids", ctypes.c_void_p), ("k_bounds", ctypes.c_void_p),
+        ("v_centroids", ctypes.c_void_p), ("v_bounds", ctypes.c_void_p),
+        ("k_signs", ctypes.c_void_p), ("v_signs", ctypes.c_void_p),
+    ]
+
+
+class KvqTierView(ctypes.Structure):
+    """Mirror of ``struct kvq_tier_view``."""
+
+    _fields_ = [("cache", ctypes.POINTER(KvqCache)), ("block_table", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("max_pages", ctypes.c_int32)]
+
+
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkvq.so.  Raises if it has not been built (no fallback exists)."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m quantized_decode_attention_rht_gb300.build`")
+        h = ctypes.CDLL(LIB_PATH)
+        h.kvq_status_string.restype = ctypes.c_char_p
+        h.kvq_status_string.argtypes = [ctypes.c_int]
+        i32, vp, sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+        dp, fp = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)
+        szp = ctypes.POINTER(ctypes.c_size_t)
+        sigs = {
+            "kvq_row_bytes": [i32, i32, i32, szp, szp],
+            "kvq_lloyd_max_codebook": [i32, dp, dp],
+            "kvq_uniform_codebook": [i32, dp, dp],
+            "kvq_codebook_tables": [i32, dp, fp, fp],
+            "kvq_quantize_append": [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp],
+            "kvq_decode_workspace_size": [ctypes.POINTER(KvqTierView), i32, i32, i32, i32, szp],
+            "kvq_decode_attention": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz, vp],
+        }
+        for name, args in sigs.items():
+            f = getattr(h, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        _lib_handle = h
+    return _lib_handle
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise KvqError(status, what)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+# ----------------------------------------------------------------------------- host-side entry points
+
+
+def kvq_status_string(status: int) -> str:
+    return lib().kvq_status_string(status).decode()
+
+
+def kvq_row_bytes(fmt, bits: int, head_dim: int):
+    fmt = FORMATS.get(fmt, fmt)
+    row, aux = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().kvq_row_bytes(fmt, bits, head_dim, ctypes.byref(row), ctypes.byref(aux)), "kvq_row_bytes")
+    return row.value, aux.value
+
+
+def _codebook(fn, bits):
+    n = 1 << bits
+    c = np.zeros(n, dtype=np.float64)
+    b = np.zeros(n - 1, dtype=np.float64)
+    _check(fn(bits, c.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+              b.ctypes.data_as(ctypes.POINTER(ctypes.c_double))), fn.__name__)
+    return c, b
+
+
+def kvq_lloyd_max_codebook(bits: int):
+    return _codebook(lib().kvq_lloyd_max_codebook, bits)
+
+
+def kvq_uniform_codebook(bits: int):
+    return _codebook(lib().kvq_uniform_codebook, bits)
+
+
+def kvq_codebook_tables(bits: int, centroids: np.ndarray):
+    n = 1 << bits
+    c = np.ascontiguousarray(centroids, dtype=np.float64)
+    c32 = np.zeros(n, dtype=np.float32)
+    b32 = np.zeros(n - 1, dtype=np.float32)
+    _check(lib().kvq_codebook_tables(bits, c.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+                                     c32.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                     b32.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), "kvq_codebook_tables")
+    return c32, b32
+
+
+# ----------------------------------------------------------------------------- GPU entry points
+
+
+def kvq_quantize_append(cache: KvqCache, k, v, slot_mapping, stream=None) -> None:
+    """k, v: fp16 CUDA tensors [T, Hkv, D] (either may be None); slot_mapping: int32 [T]."""
+    t = (k if k is not None else v).shape[0]
+    _check(lib().kvq_quantize_append(ctypes.byref(cache), _ptr(k), _ptr(v), t, _ptr(slot_mapping),
+                                     _stream(stream)), "kvq_quantize_append")
+
+
+def _views(tiers: Sequence["TierView"]):
+    arr = (KvqTierView * len(tiers))()
+    for i, t in enumerate(tiers):
+        arr[i].cache = ctypes.pointer(t.cache.struct)
+        arr[i].block_table = _ptr(t.block_table)
+        arr[i].seq_lens = _ptr(t.seq_lens)
+        arr[i].max_pages = int(t.block_table.shape[1]) if t.block_table is not None else 0
+    return arr
+
+
+def kvq_decode_workspace_size(tiers, batch: int, num_q_heads: int, split_tokens: int = 0) -> int:
+    arr = _views(tiers)
+    n = ctypes.c_size_t()
+    _check(lib().kvq_decode_workspace_size(arr, len(tiers), batch, num_q_heads, split_tokens, ctypes.byref(n)),
+           "kvq_decode_workspace_size")
+    return n.value
+
+
+def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream=None) -> None:
+    """q: fp16 [B, Hq, D]; out: fp32 [B, Hq, D]; workspace: uint8 CUDA tensor."""
+    arr = _views(tiers)
+    b, hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().kvq_decode_attention(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out), _ptr(workspace),
+                                      ws_bytes, _stream(stream)), "kvq_decode_attention")
+
+
+# ----------------------------------------------------------------------------- device buffers
+
+
+class PagedCache:
+    """Owns the device buffers of one tier (torch allocations) and its ``KvqCache`` struct.
+
+    k_format / v_format: "codebook" | "fp16" | "fp8_e4m3" | "int4_g32"; codebook tiers take
+    `k_bits` / `v_bits` and a codebook kind ("lloyd_max" or "uniform") computed by the library.
+    k_signs / v_signs: int8 [Hkv, D] tensors or arrays of +1/-1 (shared by every tier)."""
+
+    def __init__(self, head_dim, num_kv_heads, num_pages, k_format, v_format, k_bits=0, v_bits=0,
+                 k_signs=None, v_signs=None, page_size=16, codebook="lloyd_max", device="cuda"):
+        import torch
+        self.head_dim, self.num_kv_heads, self.num_pages, self.page_size = head_dim, num_kv_heads, num_pages, page_size
+        self.k_format, self.v_format = FORMATS.get(k_format, k_format), FORMATS.get(v_format, v_format)
+        self.k_bits, self.v_bits = k_bits, v_bits
+        dev = torch.device(device)
+
+        def side(fmt, bits):
+            row, aux = kvq_row_bytes(fmt, bits, head_dim)
+            rows = torch.zeros((num_pages, num_kv_heads, page_size, row), dtype=torch.uint8, device=dev)
+            a = None
+            if aux:
+                a = torch.zeros((num_pages, num_kv_heads, page_size, aux // 2), dtype=torch.float16, device=dev)
+            cent = bnd = None
+            if fmt == FMT_CODEBOOK:
+                c = (kvq_lloyd_max_codebook if codebook == "lloyd_max" else kvq_uniform_codebook)(bits)[0]
+                c32, b32 = kvq_codebook_tables(bits, c)
+                cent = torch.from_numpy(c32).to(dev)
+                bnd = torch.from_numpy(b32).to(dev)
+            return rows, a, cent, bnd
+
+        self.k_rows, self.k_aux, self.k_centroids, self.k_bounds = side(self.k_format, k_bits)
+        self.v_rows, self.v_aux, self.v_centroids, self.v_bounds = side(self.v_format, v_bits)
+        self.k_signs = torch.as_tensor(np.asarray(k_signs, dtype=np.int8)).to(dev) if not hasattr(k_signs, "data_ptr") else k_signs
+        self.v_signs = torch.as_tensor(np.asarray(v_signs, dtype=np.int8)).to(dev) if not hasattr(v_signs, "data_ptr") else v_signs
+        s = KvqCache()
+        s.head_dim, s.num_kv_heads, s.page_size, s.num_pages = head_dim, num_kv_heads, page_size, num_pages
+        s.k_format, s.v_format, s.k_bits, s.v_bits = self.k_format, self.v_format, k_bits, v_bits
+        s.k_rows, s.v_rows = _ptr(self.k_rows), _ptr(self.v_rows)
+        s.k_aux, s.v_aux = _ptr(self.k_aux), _ptr(self.v_aux)
+        s.k_centroids, s.k_bounds = _ptr(self.k_centroids), _ptr(self.k_bounds)
+        s.v_centroids, s.v_bounds = _ptr(self.v_centroids), _ptr(self.v_bounds)
+        s.k_signs, s.v_signs = _ptr(self.k_signs), _ptr(self.v_signs)
+        self.struct = s
+
+    def append(self, k, v, slot_mapping, stream=None) -> None:
+        kvq_quantize_append(self.struct, k, v, slot_mapping, stream)
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.k_rows, self.v_rows, self.k_aux, self.v_aux)
+                   if t is not None)
+
+
+class TierView:
+    """A tier as seen by one decode call: cache + block table [B, max_pages] + lens [B] (int32)."""
+
+    def __init__(self, cache: PagedCache, block_table, seq_lens):
+        self.cache, self.block_table, self.seq_lens = cache, block_table, seq_lens

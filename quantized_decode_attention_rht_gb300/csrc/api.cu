@@ -1,0 +1,262 @@
+// C ABI of libkvq.so: argument checks, split-K planning and kernel launches.
+#include <cstring>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+bool decode_supports(int k_fmt, int k_bits, int v_fmt, int v_bits);
+}
+
+namespace {
+
+using namespace kvq;
+
+constexpr int kSms = 152;  // GB300; the plan only needs the order of magnitude
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+kvq_status side_bytes(int fmt, int bits, int d, size_t* row, size_t* aux) {
+  if (d != 128 && d != 256) return KVQ_ERR_UNSUPPORTED;
+  switch (fmt) {
+    case KVQ_FMT_CODEBOOK:
+      if (bits < 2 || bits > 4) return KVQ_ERR_UNSUPPORTED;
+      *row = (size_t)d * bits / 8;
+      *aux = 2;
+      return KVQ_OK;
+    case KVQ_FMT_FP16: *row = 2 * (size_t)d; *aux = 0; return KVQ_OK;
+    case KVQ_FMT_FP8_E4M3: *row = d; *aux = 0; return KVQ_OK;
+    case KVQ_FMT_INT4_G32: *row = d / 2; *aux = 2 * (size_t)(d / KVQ_INT4_GROUP); return KVQ_OK;
+    default: return KVQ_ERR_INVALID_ARGUMENT;
+  }
+}
+
+kvq_status check_side(const kvq_cache* c, int fmt, int bits, const void* rows, const void* aux,
+                      const float* cent, const float* bounds, const int8_t* signs, bool need_bounds) {
+  size_t rb, ab;
+  kvq_status st = side_bytes(fmt, bits, c->head_dim, &rb, &ab);
+  if (st != KVQ_OK) return st;
+  if (!rows || !aligned(rows, 16) || !signs) return KVQ_ERR_INVALID_ARGUMENT;
+  if (ab && (!aux || !aligned(aux, 2))) return KVQ_ERR_INVALID_ARGUMENT;
+  if (fmt == KVQ_FMT_CODEBOOK && (!cent || (need_bounds && !bounds))) return KVQ_ERR_INVALID_ARGUMENT;
+  return KVQ_OK;
+}
+
+kvq_status check_cache(const kvq_cache* c) {
+  if (!c) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (c->num_kv_heads < 1 || c->page_size < 1 || c->num_pages < 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if ((long long)c->num_pages * c->page_size > 0x7FFFFFFFLL) return KVQ_ERR_INVALID_ARGUMENT;
+  return KVQ_OK;
+}
+
+int side_row_bytes(int fmt, int bits, int d) {
+  size_t rb = 0, ab = 0;
+  side_bytes(fmt, bits, d, &rb, &ab);
+  return (int)rb;
+}
+
+// Split-K plan: tokens per chunk for each tier (a multiple of page_size).
+struct Plan {
+  int chunk[KVQ_MAX_TIERS];
+  int splits[KVQ_MAX_TIERS];
+  int total;
+};
+
+kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hkv, int split_tokens, Plan* plan) {
+  const int ps = tiers[0].cache->page_size;
+  if (split_tokens < 0 || split_tokens % ps) return KVQ_ERR_INVALID_ARGUMENT;
+  plan->total = 0;
+  for (int i = 0; i < n; ++i) {
+    const long long max_len = (long long)tiers[i].max_pages * ps;
+    int chunk = split_tokens;
+    if (chunk == 0) {
+      // aim at ~16 CTAs per SM in total, chunks of 256 .. 4096 tokens
+      const long long work = (long long)batch * hkv * max_len;
+      long long want = work / (kSms * 16) + 1;
+      long long c = 256;
+      while (c < want && c < 4096) c *= 2;
+      chunk = (int)c;
+      if (chunk % ps) chunk = (chunk / ps + 1) * ps;
+    }
+    plan->chunk[i] = chunk;
+    plan->splits[i] = max_len == 0 ? 0 : (int)((max_len + chunk - 1) / chunk);
+    plan->total += plan->splits[i];
+  }
+  return KVQ_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+kvq_status check_tiers(const kvq_tier_view* tiers, int n, int batch, int hq) {
+  if (!tiers || n < 1 || n > KVQ_MAX_TIERS || batch < 0 || hq < 1) return KVQ_ERR_INVALID_ARGUMENT;
+  const kvq_cache* c0 = tiers[0].cache;
+  kvq_status st = check_cache(c0);
+  if (st != KVQ_OK) return st;
+  if (hq % c0->num_kv_heads) return KVQ_ERR_INVALID_ARGUMENT;
+  const int g = hq / c0->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return KVQ_ERR_UNSUPPORTED;
+  for (int i = 0; i < n; ++i) {
+    const kvq_cache* c = tiers[i].cache;
+    if ((st = check_cache(c)) != KVQ_OK) return st;
+    if (c->head_dim != c0->head_dim || c->num_kv_heads != c0->num_kv_heads || c->page_size != c0->page_size)
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->k_signs != c0->k_signs || c->v_signs != c0->v_signs) return KVQ_ERR_INVALID_ARGUMENT;
+    if (tiers[i].max_pages < 0 || (tiers[i].max_pages > 0 && (!tiers[i].block_table || !tiers[i].seq_lens)))
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (!tiers[i].seq_lens) return KVQ_ERR_INVALID_ARGUMENT;
+    if ((st = check_side(c, c->k_format, c->k_bits, c->k_rows, c->k_aux, c->k_centroids, c->k_bounds,
+                         c->k_signs, false)) != KVQ_OK)
+      return st;
+    if ((st = check_side(c, c->v_format, c->v_bits, c->v_rows, c->v_aux, c->v_centroids, c->v_bounds,
+                         c->v_signs, false)) != KVQ_OK)
+      return st;
+    if (!decode_supports(c->k_format, c->k_bits, c->v_format, c->v_bits)) return KVQ_ERR_UNSUPPORTED;
+  }
+  return KVQ_OK;
+}
+
+size_t workspace_bytes(int batch, int hq, int d, int total_splits) {
+  const size_t parts = (size_t)batch * hq * total_splits;
+  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+KVQ_API const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARGUMENT: return "KVQ_ERR_INVALID_ARGUMENT";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "KVQ_ERR_WORKSPACE_TOO_SMALL";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA";
+  }
+  return "KVQ_ERR_UNKNOWN";
+}
+
+KVQ_API kvq_status kvq_row_bytes(int32_t format, int32_t bits, int32_t head_dim, size_t* row_bytes,
+                                 size_t* aux_bytes) {
+  if (!row_bytes || !aux_bytes) return KVQ_ERR_INVALID_ARGUMENT;
+  return side_bytes(format, bits, head_dim, row_bytes, aux_bytes);
+}
+
+KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k, const uint16_t* v,
+                                       int32_t num_tokens, const int32_t* slot_mapping, void* stream) {
+  kvq_status st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (num_tokens < 0 || (!k && !v)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!slot_mapping || !aligned(slot_mapping, 4)) return KVQ_ERR_INVALID_ARGUMENT;
+  if ((k && !aligned(k, 16)) || (v && !aligned(v, 16))) return KVQ_ERR_INVALID_ARGUMENT;
+  const kvq_cache* c = cache;
+  if (k && (st = check_side(c, c->k_format, c->k_bits, c->k_rows, c->k_aux, c->k_centroids, c->k_bounds,
+                            c->k_signs, true)) != KVQ_OK)
+    return st;
+  if (v && (st = check_side(c, c->v_format, c->v_bits, c->v_rows, c->v_aux, c->v_centroids, c->v_bounds,
+                            c->v_signs, true)) != KVQ_OK)
+    return st;
+  QuantParams p;
+  memset(&p, 0, sizeof(p));
+  p.x[0] = k;
+  p.x[1] = v;
+  const int fmts[2] = {c->k_format, c->v_format}, bits[2] = {c->k_bits, c->v_bits};
+  void* rows[2] = {c->k_rows, c->v_rows};
+  void* aux[2] = {c->k_aux, c->v_aux};
+  const float* bnd[2] = {c->k_bounds, c->v_bounds};
+  const int8_t* sg[2] = {c->k_signs, c->v_signs};
+  for (int i = 0; i < 2; ++i) {
+    p.side[i].rows = static_cast<uint8_t*>(rows[i]);
+    p.side[i].aux = static_cast<__half*>(aux[i]);
+    p.side[i].bounds = bnd[i];
+    p.side[i].signs = sg[i];
+    p.side[i].fmt = fmts[i];
+    p.side[i].bits = bits[i];
+    p.side[i].row_bytes = side_row_bytes(fmts[i], bits[i], c->head_dim);
+  }
+  p.slots = slot_mapping;
+  p.num_tokens = num_tokens;
+  p.hkv = c->num_kv_heads;
+  p.page_size = c->page_size;
+  p.num_slots = c->num_pages * c->page_size;
+  p.kind_first = k ? 0 : 1;
+  p.num_kinds = (k && v) ? 2 : 1;
+  p.num_vectors = (long long)p.num_kinds * num_tokens * c->num_kv_heads;
+  if (p.num_slots == 0) return KVQ_OK;
+  cudaError_t e = launch_quantize(p, c->head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t num_tiers, int32_t batch,
+                                             int32_t num_q_heads, int32_t split_tokens, size_t* bytes) {
+  if (!bytes) return KVQ_ERR_INVALID_ARGUMENT;
+  kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
+  if (st != KVQ_OK) return st;
+  Plan plan;
+  if ((st = make_plan(tiers, num_tiers, batch, tiers[0].cache->num_kv_heads, split_tokens, &plan)) != KVQ_OK)
+    return st;
+  *bytes = workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total);
+  return KVQ_OK;
+}
+
+KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_tiers, const uint16_t* q,
+                                        int32_t batch, int32_t num_q_heads, int32_t split_tokens, float* out,
+                                        void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
+  if (st != KVQ_OK) return st;
+  if (batch == 0) return KVQ_OK;
+  if (!q || !out || !aligned(q, 4) || !aligned(out, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  const kvq_cache* c0 = tiers[0].cache;
+  const int d = c0->head_dim, hkv = c0->num_kv_heads;
+  Plan plan;
+  if ((st = make_plan(tiers, num_tiers, batch, hkv, split_tokens, &plan)) != KVQ_OK) return st;
+  const size_t need = workspace_bytes(batch, num_q_heads, d, plan.total);
+  if (need > 0 && (!workspace || !aligned(workspace, 256))) return KVQ_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+
+  DecParams p;
+  memset(&p, 0, sizeof(p));
+  p.num_tiers = num_tiers;
+  int at = 0;
+  for (int i = 0; i < num_tiers; ++i) {
+    const kvq_cache* c = tiers[i].cache;
+    DecTier& t = p.tier[i];
+    t.k_rows = static_cast<const uint8_t*>(c->k_rows);
+    t.v_rows = static_cast<const uint8_t*>(c->v_rows);
+    t.k_aux = static_cast<const __half*>(c->k_aux);
+    t.v_aux = static_cast<const __half*>(c->v_aux);
+    t.k_cent = c->k_centroids;
+    t.v_cent = c->v_centroids;
+    t.block_table = tiers[i].block_table;
+    t.seq_lens = tiers[i].seq_lens;
+    t.k_fmt = c->k_format;
+    t.v_fmt = c->v_format;
+    t.k_bits = c->k_bits;
+    t.v_bits = c->v_bits;
+    t.k_row_bytes = side_row_bytes(c->k_format, c->k_bits, d);
+    t.v_row_bytes = side_row_bytes(c->v_format, c->v_bits, d);
+    t.max_pages = tiers[i].max_pages;
+    t.split_begin = at;
+    t.num_splits = plan.splits[i];
+    t.chunk = plan.chunk[i];
+    at += plan.splits[i];
+  }
+  p.q = reinterpret_cast<const __half*>(q);
+  p.k_signs = c0->k_signs;
+  p.v_signs = c0->v_signs;
+  p.out = out;
+  const size_t parts = (size_t)batch * num_q_heads * plan.total;
+  p.ws_acc = static_cast<float*>(workspace);
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(parts * d * sizeof(float), 256));
+  p.batch = batch;
+  p.hq = num_q_heads;
+  p.hkv = hkv;
+  p.page_size = c0->page_size;
+  p.total_splits = plan.total;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(p, d, num_q_heads / hkv, s);
+  if (e == cudaSuccess) e = launch_combine(p, d, s);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // extern "C"

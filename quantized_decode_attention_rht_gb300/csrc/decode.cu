@@ -1,0 +1,425 @@
+// Split-K decode attention over the packed cache, and the combine pass.
+//
+// Pass 1 (decode_tier_kernel): one CTA per (split, kv head, sequence) walks a chunk of the
+// sequence's pages.  In its prologue it rotates the G = Hq/Hkv queries of the kv head with
+// the K signs, x~ = H diag(s) q / sqrt(D) (AdapTQ page, "Engineering the Hot Path": the
+// query is rotated once and compared with the stored rotated codes), pre-scaled by
+// 1/sqrt(D) (FoveatedKV page, "Making it fast") and by log2(e) so scores come out in base-2
+// units.  Per token it dequantises the K row in registers, forms the G scores, updates an
+// online softmax (running max / sum, one exp2 per score), and accumulates the value rows,
+// still in the rotated domain.  Partials (max, sum, acc[D]) go to the workspace.
+// Pass 2 (combine_kernel): per (sequence, query head) merge the partials of every split of
+// every tier, normalise, and undo the V rotation, y = s_V * (H y~) / sqrt(D).
+//
+// Lane layout: LPT lanes share a token, each holding DPL = D/LPT consecutive coordinates
+// of the G rotated queries and of the G value accumulators in registers; a warp advances
+// TPS = 32/LPT tokens per step.  The four warps of a CTA take alternate pages and merge
+// their softmax states at the end.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------- storage formats
+template <int BITS>
+struct Codebook {
+  static constexpr int bits = BITS;
+};
+struct Fp16 {};
+struct Fp8 {};
+struct Int4 {};
+
+// Funnel-shifted window over a row: the lane's N words start exactly at bit `bit0`.
+template <int N>
+__device__ __forceinline__ void load_window(const uint8_t* row, int row_words, int bit0, uint32_t (&w)[N]) {
+  const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row);
+  const int w0 = bit0 >> 5, sh = bit0 & 31;
+  uint32_t raw[N + 1];
+#pragma unroll
+  for (int i = 0; i <= N; ++i) raw[i] = (w0 + i < row_words) ? __ldg(r32 + w0 + i) : 0u;
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(raw[i], raw[i + 1], sh);
+}
+
+// Dequantise the lane's DPL coordinates [e0, e0 + DPL) of one row (rotated domain).
+// `scale` receives the per-row (codebook: norm / sqrt(D)) or per-group (INT4) factor that
+// multiplies every coordinate; it is applied outside the inner loops.
+template <class F, int D, int DPL>
+struct Row;
+
+template <int BITS, int D, int DPL>
+struct Row<Codebook<BITS>, D, DPL> {
+  __device__ __forceinline__ static void load(const uint8_t* rows, const __half* aux, size_t rowid,
+                                              int row_bytes, int e0, const float* lut,
+                                              float (&x)[DPL], float& scale) {
+    constexpr int NW = (DPL * BITS + 31) / 32;
+    uint32_t w[NW];
+    load_window<NW>(rows + rowid * row_bytes, row_bytes / 4, e0 * BITS, w);
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) {
+      const int o = j * BITS;
+      uint32_t v = w[o / 32] >> (o % 32);
+      if ((o % 32) + BITS > 32) v |= w[o / 32 + 1] << (32 - (o % 32));
+      x[j] = lut[v & ((1u << BITS) - 1u)];
+    }
+    constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
+    scale = __half2float(aux[rowid]) * inv_sqrt_d;
+  }
+};
+
+template <int D, int DPL>
+struct Row<Fp16, D, DPL> {
+  __device__ __forceinline__ static void load(const uint8_t* rows, const __half*, size_t rowid, int row_bytes,
+                                              int e0, const float*, float (&x)[DPL], float& scale) {
+    const uint2* src = reinterpret_cast<const uint2*>(rows + rowid * row_bytes + 2 * e0);
+#pragma unroll
+    for (int k = 0; k < DPL / 4; ++k) {
+      const uint2 u = __ldg(src + k);
+      const __half2 a = *reinterpret_cast<const __half2*>(&u.x);
+      const __half2 b = *reinterpret_cast<const __half2*>(&u.y);
+      x[4 * k] = __low2float(a);
+      x[4 * k + 1] = __high2float(a);
+      x[4 * k + 2] = __low2float(b);
+      x[4 * k + 3] = __high2float(b);
+    }
+    scale = 1.0f;
+  }
+};
+
+template <int D, int DPL>
+struct Row<Fp8, D, DPL> {
+  __device__ __forceinline__ static void load(const uint8_t* rows, const __half*, size_t rowid, int row_bytes,
+                                              int e0, const float*, float (&x)[DPL], float& scale) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(rows + rowid * row_bytes + e0);
+#pragma unroll
+    for (int k = 0; k < DPL / 4; ++k) {
+      const uint32_t u = __ldg(src + k);
+      uint32_t h01, h23;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((uint16_t)(u & 0xFFFF)));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((uint16_t)(u >> 16)));
+      const __half2 a = *reinterpret_cast<const __half2*>(&h01);
+      const __half2 b = *reinterpret_cast<const __half2*>(&h23);
+      x[4 * k] = __low2float(a);
+      x[4 * k + 1] = __high2float(a);
+      x[4 * k + 2] = __low2float(b);
+      x[4 * k + 3] = __high2float(b);
+    }
+    scale = 1.0f;
+  }
+};
+
+template <int D, int DPL>
+struct Row<Int4, D, DPL> {
+  __device__ __forceinline__ static void load(const uint8_t* rows, const __half* aux, size_t rowid,
+                                              int row_bytes, int e0, const float*, float (&x)[DPL],
+                                              float& scale) {
+    constexpr int NW = (DPL * 4 + 31) / 32;
+    uint32_t w[NW];
+    load_window<NW>(rows + rowid * row_bytes, row_bytes / 4, e0 * 4, w);
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) x[j] = (float)((int)((w[j / 8] >> (4 * (j % 8))) & 0xFu) - 8);
+    scale = __half2float(aux[rowid * (D / kGroup) + e0 / kGroup]);
+  }
+};
+
+template <class F>
+__device__ __forceinline__ bool is_codebook() { return false; }
+template <>
+__device__ __forceinline__ bool is_codebook<Codebook<2>>() { return true; }
+template <>
+__device__ __forceinline__ bool is_codebook<Codebook<3>>() { return true; }
+template <>
+__device__ __forceinline__ bool is_codebook<Codebook<4>>() { return true; }
+
+template <int D, int G>
+struct Shape {
+  static constexpr int DPL = (D / 32 > 32 / G) ? D / 32 : 32 / G;  // coordinates per lane
+  static constexpr int LPT = D / DPL;                             // lanes per token
+  static constexpr int TPS = 32 / LPT;                            // tokens per warp step
+};
+
+// ---------------------------------------------------------------- pass 1
+template <int D, int G, class KF, class VF>
+__global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParams p, int tier_index) {
+  using S = Shape<D, G>;
+  constexpr int DPL = S::DPL, LPT = S::LPT, TPS = S::TPS;
+  const DecTier& T = p.tier[tier_index];
+  const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int len = T.seq_lens[b];
+  const int t_begin = split * T.chunk;
+  if (t_begin >= len) return;  // the combine pass only reads splits that hold tokens
+  const int t_end = min(len, t_begin + T.chunk);
+
+  __shared__ float q_s[G][D];
+  __shared__ float lut_k[256], lut_v[256];
+  __shared__ float w_m[kWarps][G], w_l[kWarps][G];
+  __shared__ float w_acc[kWarps][G][D];
+
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // ---- rotate and pre-scale the group's queries: q' = H (s_K * q) * log2(e) / D
+  for (int i = tid; i < G * D; i += kWarps * 32) {
+    const int g = i / D, j = i % D;
+    const float qv = __half2float(p.q[((size_t)b * p.hq + hk * G + g) * D + j]);
+    q_s[g][j] = p.k_signs[hk * D + j] < 0 ? -qv : qv;
+  }
+  if (is_codebook<KF>()) for (int i = tid; i < 256; i += kWarps * 32) lut_k[i] = i < 16 ? T.k_cent[min(i, (1 << T.k_bits) - 1)] : 0.f;
+  if (is_codebook<VF>()) for (int i = tid; i < 256; i += kWarps * 32) lut_v[i] = i < 16 ? T.v_cent[min(i, (1 << T.v_bits) - 1)] : 0.f;
+  __syncthreads();
+  for (int hs = 1; hs < D; hs <<= 1) {
+    for (int i = tid; i < G * D / 2; i += kWarps * 32) {
+      const int g = i / (D / 2), k = i % (D / 2);
+      const int j = (k / hs) * 2 * hs + (k % hs);
+      const float a = q_s[g][j], c = q_s[g][j + hs];
+      q_s[g][j] = a + c;
+      q_s[g][j + hs] = a - c;
+    }
+    __syncthreads();
+  }
+  const int r = lane % LPT, gi = lane / LPT, e0 = r * DPL;
+  float qr[G][DPL], acc[G][DPL], m[G], l[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) {
+      qr[g][j] = q_s[g][e0 + j] * (kLog2e / (float)D);
+      acc[g][j] = 0.f;
+    }
+  }
+
+  const int p_begin = t_begin / p.page_size, p_end = (t_end + p.page_size - 1) / p.page_size;
+  for (int lp = p_begin + warp; lp < p_end; lp += kWarps) {
+    const int phys = T.block_table[(size_t)b * T.max_pages + lp];
+    const size_t row_base = ((size_t)phys * p.hkv + hk) * p.page_size;
+    for (int s0 = 0; s0 < p.page_size; s0 += TPS) {
+      const int off = s0 + gi;
+      const int t = lp * p.page_size + off;
+      const bool valid = t < t_end;
+      const size_t rowid = row_base + off;
+      float x[DPL], ks = 0.f;
+      if (valid) Row<KF, D, DPL>::load(T.k_rows, T.k_aux, rowid, T.k_row_bytes, e0, lut_k, x, ks);
+      float sc[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float a = 0.f;
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) a = fmaf(qr[g][j], x[j], a);
+        }
+#pragma unroll
+        for (int o = 1; o < LPT; o <<= 1) a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+        sc[g] = valid ? a * ks : -INFINITY;
+      }
+      // online softmax over the TPS tokens of this step
+      float pr[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float mx = sc[g];
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (mx > m[g]) {
+          const float f = exp2f(m[g] - mx);  // m = -inf first: f = 0
+          l[g] *= f;
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) acc[g][j] *= f;
+          m[g] = mx;
+        }
+        pr[g] = valid ? exp2f(sc[g] - m[g]) : 0.f;
+        l[g] += pr[g];
+      }
+      if (valid) {
+        float vs;
+        Row<VF, D, DPL>::load(T.v_rows, T.v_aux, rowid, T.v_row_bytes, e0, lut_v, x, vs);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float wgt = pr[g] * vs;
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) acc[g][j] = fmaf(wgt, x[j], acc[g][j]);
+        }
+      }
+    }
+  }
+  // ---- merge the token groups of the warp (same running max in every lane)
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1) {
+      l[g] += __shfl_xor_sync(0xFFFFFFFFu, l[g], o);
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[g][j] += __shfl_xor_sync(0xFFFFFFFFu, acc[g][j], o);
+    }
+  }
+  if (gi == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) w_acc[warp][g][e0 + j] = acc[g][j];
+      if (r == 0) {
+        w_m[warp][g] = m[g];
+        w_l[warp][g] = l[g];
+      }
+    }
+  }
+  __syncthreads();
+  // ---- merge the warps and write this split's partial
+  const int split_slot = T.split_begin + split;
+  for (int i = tid; i < G * D; i += kWarps * 32) {
+    const int g = i / D, j = i % D;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, w_m[w][g]);
+    float a = 0.f, s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (w_m[w][g] == -INFINITY) continue;  // a warp that saw no token
+      const float f = exp2f(w_m[w][g] - mx);
+      a += w_acc[w][g][j] * f;
+      s += w_l[w][g] * f;
+    }
+    const size_t part = ((size_t)b * p.hq + hk * G + g) * p.total_splits + split_slot;
+    p.ws_acc[part * D + j] = a;
+    if (j == 0) {
+      p.ws_ml[2 * part] = mx;
+      p.ws_ml[2 * part + 1] = s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- pass 2
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const DecParams p) {
+  constexpr int PER = D / 128;
+  const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int hk = hq / (p.hq / p.hkv);
+  __shared__ float y_s[D];
+  __shared__ float red[128];
+  const size_t base = ((size_t)b * p.hq + hq) * p.total_splits;
+  // global max over the valid splits of every tier
+  float mx = -INFINITY;
+  for (int ti = 0; ti < p.num_tiers; ++ti) {
+    const DecTier& T = p.tier[ti];
+    const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
+    for (int s = tid; s < n; s += 128) mx = fmaxf(mx, p.ws_ml[2 * (base + T.split_begin + s)]);
+  }
+  red[tid] = mx;
+  __syncthreads();
+  for (int o = 64; o > 0; o >>= 1) {
+    if (tid < o) red[tid] = fmaxf(red[tid], red[tid + o]);
+    __syncthreads();
+  }
+  mx = red[0];
+  __syncthreads();
+  float acc[PER] = {}, lsum = 0.f;
+  if (mx != -INFINITY) {
+    for (int ti = 0; ti < p.num_tiers; ++ti) {
+      const DecTier& T = p.tier[ti];
+      const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
+      for (int s = 0; s < n; ++s) {
+        const size_t part = base + T.split_begin + s;
+        const float ms = p.ws_ml[2 * part];
+        if (ms == -INFINITY) continue;
+        const float f = exp2f(ms - mx);
+        lsum += p.ws_ml[2 * part + 1] * f;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) acc[k] += p.ws_acc[part * D + tid + 128 * k] * f;
+      }
+    }
+  }
+  const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) y_s[tid + 128 * k] = acc[k] * inv;
+  __syncthreads();
+  // undo the V rotation: y = s_V * (H y~) / sqrt(D)
+  for (int hs = 1; hs < D; hs <<= 1) {
+    for (int i = tid; i < D / 2; i += 128) {
+      const int j = (i / hs) * 2 * hs + (i % hs);
+      const float a = y_s[j], c = y_s[j + hs];
+      y_s[j] = a + c;
+      y_s[j + hs] = a - c;
+    }
+    __syncthreads();
+  }
+  constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int j = tid + 128 * k;
+    const float v = y_s[j] * inv_sqrt_d;
+    p.out[((size_t)b * p.hq + hq) * D + j] = p.v_signs[hk * D + j] < 0 ? -v : v;
+  }
+}
+
+template <int D, int G, class KF, class VF>
+cudaError_t launch_tier(const DecParams& p, int ti, cudaStream_t stream) {
+  const DecTier& T = p.tier[ti];
+  if (T.num_splits == 0) return cudaSuccess;
+  dim3 grid(T.num_splits, p.hkv, p.batch);
+  decode_tier_kernel<D, G, KF, VF><<<grid, kWarps * 32, 0, stream>>>(p, ti);
+  return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_tier_fmt(const DecParams& p, int ti, cudaStream_t stream) {
+  const DecTier& T = p.tier[ti];
+  const int kf = T.k_fmt, vf = T.v_fmt;
+  if (kf == KVQ_FMT_CODEBOOK && vf == KVQ_FMT_CODEBOOK) {
+    const int kb = T.k_bits, vb = T.v_bits;
+    if (kb == 4 && vb == 4) return launch_tier<D, G, Codebook<4>, Codebook<4>>(p, ti, stream);
+    if (kb == 4 && vb == 3) return launch_tier<D, G, Codebook<4>, Codebook<3>>(p, ti, stream);
+    if (kb == 4 && vb == 2) return launch_tier<D, G, Codebook<4>, Codebook<2>>(p, ti, stream);
+    if (kb == 3 && vb == 3) return launch_tier<D, G, Codebook<3>, Codebook<3>>(p, ti, stream);
+    if (kb == 3 && vb == 2) return launch_tier<D, G, Codebook<3>, Codebook<2>>(p, ti, stream);
+    if (kb == 2 && vb == 2) return launch_tier<D, G, Codebook<2>, Codebook<2>>(p, ti, stream);
+    return cudaErrorNotSupported;
+  }
+  if (kf == KVQ_FMT_FP16 && vf == KVQ_FMT_FP16) return launch_tier<D, G, Fp16, Fp16>(p, ti, stream);
+  if (kf == KVQ_FMT_FP8_E4M3 && vf == KVQ_FMT_INT4_G32) return launch_tier<D, G, Fp8, Int4>(p, ti, stream);
+  if (kf == KVQ_FMT_FP8_E4M3 && vf == KVQ_FMT_FP16) return launch_tier<D, G, Fp8, Fp16>(p, ti, stream);
+  return cudaErrorNotSupported;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecParams& p, int group, cudaStream_t stream) {
+  for (int ti = 0; ti < p.num_tiers; ++ti) {
+    cudaError_t e;
+    switch (group) {
+      case 1: e = launch_tier_fmt<D, 1>(p, ti, stream); break;
+      case 2: e = launch_tier_fmt<D, 2>(p, ti, stream); break;
+      case 4: e = launch_tier_fmt<D, 4>(p, ti, stream); break;
+      case 8: e = launch_tier_fmt<D, 8>(p, ti, stream); break;
+      default: e = cudaErrorNotSupported;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+bool decode_supports(int k_fmt, int k_bits, int v_fmt, int v_bits) {
+  if (k_fmt == KVQ_FMT_CODEBOOK && v_fmt == KVQ_FMT_CODEBOOK)
+    return (k_bits == 4 && v_bits >= 2 && v_bits <= 4) || (k_bits == 3 && (v_bits == 3 || v_bits == 2)) ||
+           (k_bits == 2 && v_bits == 2);
+  if (k_fmt == KVQ_FMT_FP16 && v_fmt == KVQ_FMT_FP16) return true;
+  if (k_fmt == KVQ_FMT_FP8_E4M3 && (v_fmt == KVQ_FMT_INT4_G32 || v_fmt == KVQ_FMT_FP16)) return true;
+  return false;
+}
+
+cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStream_t stream) {
+  if (head_dim == 128) return launch_decode_d<128>(p, group, stream);
+  if (head_dim == 256) return launch_decode_d<256>(p, group, stream);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
+  dim3 grid(p.hq, p.batch);
+  if (head_dim == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
+  else if (head_dim == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(p);
+  else return cudaErrorNotSupported;
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,78 @@
+// Internal declarations shared by the kernels and the C-ABI layer of libkvq.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kGroup = KVQ_INT4_GROUP;
+
+// ------------------------------------------------------------------------ quantize
+struct QuantSide {
+  uint8_t* rows;
+  __half* aux;
+  const float* bounds;
+  const int8_t* signs;
+  int fmt, bits, row_bytes;
+};
+
+struct QuantParams {
+  const uint16_t* x[2];  // K, V inputs [T][Hkv][D] fp16 (either may be null)
+  QuantSide side[2];
+  const int32_t* slots;
+  int num_tokens, hkv, page_size, num_slots;
+  int kind_first, num_kinds;  // kinds present: [kind_first, kind_first + num_kinds)
+  long long num_vectors;      // num_kinds * num_tokens * hkv
+};
+
+cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t stream);
+
+// ------------------------------------------------------------------------ decode
+struct DecTier {
+  const uint8_t* k_rows;
+  const uint8_t* v_rows;
+  const __half* k_aux;
+  const __half* v_aux;
+  const float* k_cent;
+  const float* v_cent;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  int k_fmt, v_fmt, k_bits, v_bits, k_row_bytes, v_row_bytes;
+  int max_pages, split_begin, num_splits, chunk;
+};
+
+struct DecParams {
+  DecTier tier[KVQ_MAX_TIERS];
+  int num_tiers;
+  const __half* q;
+  const int8_t* k_signs;
+  const int8_t* v_signs;
+  float* out;
+  float* ws_acc;  // [B][Hq][S][D]
+  float* ws_ml;   // [B][Hq][S][2]  (running max in log2 units, sum of exp2)
+  int batch, hq, hkv, page_size, total_splits;
+};
+
+cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStream_t stream);
+cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream);
+
+// ------------------------------------------------------------------------ device helpers
+__device__ __forceinline__ float fp8e4m3_to_float(uint32_t byte) {
+  // exact: every E4M3 value is an fp16 value; the hardware conversion takes two bytes
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)byte));
+  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFF)));
+}
+
+// Two floats -> two E4M3 bytes (lo = first element), nearest-even, saturating.
+__device__ __forceinline__ uint32_t float2_to_fp8x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+}  // namespace kvq

@@ -1,0 +1,154 @@
+"""The C ABI without a GPU: the library builds and loads, exports exactly the entry points
+include/kvq.h declares, its host-side codebooks agree with the oracle's, and argument
+checks fail before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import codebook as ocb
+from oracle import formats as ofmt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from quantized_decode_attention_rht_gb300 import build
+    build.build()
+    import quantized_decode_attention_rht_gb300 as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", text)))
+
+
+def test_exports_match_header(kvq):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(kvq.lib(), n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert exported == names
+
+
+def test_status_strings(kvq):
+    for s, name in kvq.STATUS.items():
+        assert kvq.kvq_status_string(s) == name
+    assert kvq.kvq_status_string(99) == "KVQ_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_row_bytes_match_oracle(kvq, d):
+    for fmt in ("codebook", "fp16", "fp8_e4m3", "int4_g32"):
+        for bits in ((2, 3, 4) if fmt == "codebook" else (0,)):
+            assert kvq.kvq_row_bytes(fmt, bits, d) == (ofmt.row_bytes(fmt, bits, d), ofmt.aux_bytes(fmt, d))
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_row_bytes("codebook", 5, d)
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_row_bytes("fp16", 0, 64)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_lloyd_max_library_matches_oracle(kvq, bits):
+    c, b = kvq.kvq_lloyd_max_codebook(bits)
+    oc, ob, _ = ocb.lloyd_max(bits)
+    np.testing.assert_allclose(c, oc, rtol=0, atol=1e-9)
+    np.testing.assert_allclose(b, ob, rtol=0, atol=1e-9)
+    c32, b32 = kvq.kvq_codebook_tables(bits, c)
+    oc32, ob32 = ocb.float32_tables(oc)
+    assert np.array_equal(c32, oc32) and np.array_equal(b32, ob32)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_uniform_library_matches_oracle(kvq, bits):
+    c, b = kvq.kvq_uniform_codebook(bits)
+    oc, ob, _ = ocb.uniform_codebook(bits)
+    np.testing.assert_allclose(c, oc, rtol=0, atol=1e-9)
+    c32, b32 = kvq.kvq_codebook_tables(bits, c)
+    oc32, ob32 = ocb.float32_tables(oc)
+    assert np.array_equal(c32, oc32) and np.array_equal(b32, ob32)
+
+
+def _fake_cache(kvq, **kw):
+    """A cache struct with aligned, never-dereferenced fake device addresses."""
+    s = kvq.KvqCache()
+    s.head_dim, s.num_kv_heads, s.page_size, s.num_pages = 128, 2, 16, 4
+    s.k_format = s.v_format = kvq.FMT_CODEBOOK
+    s.k_bits = s.v_bits = 4
+    base = 1 << 40
+    for i, f in enumerate(("k_rows", "v_rows", "k_aux", "v_aux", "k_centroids", "k_bounds", "v_centroids",
+                           "v_bounds", "k_signs", "v_signs")):
+        setattr(s, f, base + 4096 * i)
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def _quant(kvq, cache, k=1 << 41, v=1 << 41, n=3, slots=1 << 42):
+    return kvq.lib().kvq_quantize_append(ctypes.byref(cache), k, v, n, slots, None)
+
+
+def test_quantize_argument_checks(kvq):
+    L = kvq.lib()
+    assert L.kvq_quantize_append(None, 1 << 41, None, 3, 1 << 42, None) == 1
+    assert _quant(kvq, _fake_cache(kvq, head_dim=64)) == 2
+    assert _quant(kvq, _fake_cache(kvq, k_bits=5)) == 2
+    assert _quant(kvq, _fake_cache(kvq, k_format=7)) == 1
+    assert _quant(kvq, _fake_cache(kvq, k_rows=None)) == 1
+    assert _quant(kvq, _fake_cache(kvq, k_rows=(1 << 40) + 8)) == 1  # rows not 16-byte aligned
+    assert _quant(kvq, _fake_cache(kvq, k_bounds=None)) == 1
+    assert _quant(kvq, _fake_cache(kvq), k=None, v=None) == 1
+    assert _quant(kvq, _fake_cache(kvq), n=-1) == 1
+    assert _quant(kvq, _fake_cache(kvq), slots=None) == 1
+    assert _quant(kvq, _fake_cache(kvq), k=(1 << 41) + 2) == 1  # input not 16-byte aligned
+    assert _quant(kvq, _fake_cache(kvq), n=0) == 0  # nothing to do
+
+
+def _views(kvq, caches, max_pages=8):
+    arr = (kvq.KvqTierView * len(caches))()
+    for i, c in enumerate(caches):
+        arr[i].cache = ctypes.pointer(c)
+        arr[i].block_table = 1 << 43
+        arr[i].seq_lens = 1 << 44
+        arr[i].max_pages = max_pages
+    return arr
+
+
+def _ws(kvq, caches, batch=2, hq=4, split=0, max_pages=8):
+    n = ctypes.c_size_t()
+    st = kvq.lib().kvq_decode_workspace_size(_views(kvq, caches, max_pages), len(caches), batch, hq, split,
+                                             ctypes.byref(n))
+    return st, n.value
+
+
+def test_decode_argument_checks(kvq):
+    c = _fake_cache(kvq)
+    assert _ws(kvq, [c])[0] == 0
+    assert _ws(kvq, [c], hq=6)[0] == 2  # Hq/Hkv = 3 is not built
+    assert _ws(kvq, [c], hq=3)[0] == 1  # Hq not a multiple of Hkv
+    assert _ws(kvq, [c] * 5)[0] == 1  # more tiers than KVQ_MAX_TIERS
+    assert _ws(kvq, [c, _fake_cache(kvq, k_signs=(1 << 40) + 4096 * 20)])[0] == 1  # tiers disagree on signs
+    assert _ws(kvq, [c, _fake_cache(kvq, num_kv_heads=4)])[0] == 1
+    assert _ws(kvq, [c], split=24)[0] == 1  # split not a multiple of the page size
+    assert _ws(kvq, [_fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_CODEBOOK)])[0] == 2
+    # decode with too small a workspace fails before any launch
+    L = kvq.lib()
+    st = L.kvq_decode_attention(_views(kvq, [c]), 1, 1 << 45, 2, 4, 0, 1 << 46, 1 << 47, 16, None)
+    assert st == 3
+
+
+def test_workspace_size_formula(kvq):
+    c = _fake_cache(kvq)
+    # 2 sequences, 4 query heads, 8 pages of 16 tokens, 32-token splits -> 4 splits
+    st, n = _ws(kvq, [c], batch=2, hq=4, split=32, max_pages=8)
+    parts = 2 * 4 * 4
+    want = -(-parts * 128 * 4 // 256) * 256 + -(-parts * 2 * 4 // 256) * 256
+    assert st == 0 and n == want
