@@ -111,16 +111,14 @@ def new_side(fmt, bits, centroids32, bounds32, signs, num_pages, num_kv_heads, p
 def write(side: Side, slots: np.ndarray, x16: np.ndarray, page_size: int) -> None:
     """Encode x16 [T, Hkv, d] and store token i at pool slot slots[i] (slot = page *
     page_size + offset); a negative slot skips the token."""
-    hkv = x16.shape[1]
-    for h in range(hkv):
-        rows, aux = encode(x16[:, h, :], side.signs[h], side.fmt, side.bits, side.bounds32)
-        for i, slot in enumerate(np.asarray(slots)):
-            if slot < 0:
-                continue
-            page, off = divmod(int(slot), page_size)
-            side.rows[page, h, off] = rows[i]
-            if side.aux is not None:
-                side.aux[page, h, off] = aux[i]
+    slots = np.asarray(slots, dtype=np.int64)
+    keep = slots >= 0
+    page, off = slots[keep] // page_size, slots[keep] % page_size
+    for h in range(x16.shape[1]):
+        rows, aux = encode(x16[keep, h, :], side.signs[h], side.fmt, side.bits, side.bounds32)
+        side.rows[page, h, off] = rows
+        if side.aux is not None:
+            side.aux[page, h, off] = aux
 
 
 def gather(side: Side, block_row: np.ndarray, length: int, h: int, page_size: int):

@@ -1,0 +1,224 @@
+"""Helpers shared by the GPU parity tests: building the library, building oracle pools
+and uploading them byte for byte, and the decision-boundary allowances.
+
+The allowances follow from where the two sides may legitimately differ.  The oracle
+rotates in float64 and takes every rounding decision on the exact value rounded to
+float32; the kernel rotates in float32.  The kernel's Walsh-Hadamard result carries an
+absolute error of at most (log2(D) + 2) * 2^-24 * sum|x| / sqrt(D) per coordinate (one
+rounding per butterfly stage on partial sums bounded by sum|x|, plus the final scale), so
+a stored value may differ from the oracle's only where the exact value lies within that
+distance of a rounding boundary.  For codebook indices the criterion is the one fixed for
+this method: a differing index is allowed only where the exact u is within 1e-6 of a
+decision boundary, and such elements must be fewer than 1e-4 of all."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention as oatt
+from oracle import cache as ocache
+from oracle import codebook as ocb
+from oracle import formats as ofmt
+from oracle import rotation as orot
+
+U_BOUNDARY = 1e-6
+MAX_BOUNDARY_FRACTION = 1e-4
+ATOL_OUT = 2e-3
+
+
+def torch_cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+_built = False
+
+
+def kvq_module():
+    global _built
+    torch_cuda()
+    import quantized_decode_attention_rht_gb300 as kvq
+    if not _built:
+        from quantized_decode_attention_rht_gb300 import build
+        build.build()
+        _built = True
+    kvq.lib()
+    return kvq
+
+
+_TABLES = {}
+
+
+def tables(kind, bits):
+    if (kind, bits) not in _TABLES:
+        _TABLES[(kind, bits)] = ocb.tables(kind, bits)
+    return _TABLES[(kind, bits)]
+
+
+def fwht_error_bound(x16: np.ndarray) -> np.ndarray:
+    """Per-vector bound on the absolute error of the kernel's float32 rotated coordinates."""
+    d = x16.shape[-1]
+    return (math.log2(d) + 2) * 2.0 ** -24 * np.sum(np.abs(x16.astype(np.float64)), axis=-1) / math.sqrt(d)
+
+
+def pool_rows(tensor, slots):
+    """Rows of a device pool tensor [P, Hkv, ps, ...] at the given slots -> numpy [T, Hkv, ...]."""
+    a = tensor.cpu().numpy()
+    ps = a.shape[2]
+    slots = np.asarray(slots)
+    return a[slots // ps, :, slots % ps]
+
+
+# ----------------------------------------------------------------------------- codes
+
+
+def check_codebook_codes(x16, signs, bits, rows_gpu, norms_gpu, kind="lloyd_max"):
+    """x16 [T, d] of one head, signs [d]; rows_gpu [T, row_bytes]; norms_gpu fp16 [T].
+    Returns (mismatches, near-boundary count, elements)."""
+    c32, b32 = tables(kind, bits)
+    d = x16.shape[-1]
+    rows_o, norm_o = ocache.encode(x16, signs, "codebook", bits, b32)
+    idx_o = ofmt.unpack_bits(rows_o, bits, d)
+    idx_g = ofmt.unpack_bits(rows_gpu, bits, d)
+    xr = orot.rotate(x16.astype(np.float64), signs)
+    n = np.sqrt(np.sum(xr * xr, axis=-1))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = np.where(n[:, None] > 0, math.sqrt(d) * xr / n[:, None], 0.0)
+    dist = np.min(np.abs(u[..., None] - b32.astype(np.float64)), axis=-1)
+    near = dist < U_BOUNDARY
+    bad = idx_o != idx_g
+    assert not np.any(bad & ~near), f"{int(np.sum(bad & ~near))} codes differ away from a boundary"
+    assert np.all(np.abs(idx_o - idx_g)[bad] == 1)
+    # norms: equal, or one fp16 ulp apart where the exact norm sits on a rounding midpoint
+    ng = np.asarray(norms_gpu, dtype=np.float16)
+    diff = ng != norm_o
+    if np.any(diff):
+        a, b = ng[diff].astype(np.float64), norm_o[diff].astype(np.float64)
+        assert np.all(np.abs(np.asarray(ng[diff]).view(np.uint16).astype(np.int64) -
+                             np.asarray(norm_o[diff]).view(np.uint16).astype(np.int64)) == 1)
+        mid = (a + b) / 2
+        assert np.all(np.abs(n[diff] - mid) <= 1.2e-5 * n[diff]), "norm differs away from a midpoint"
+    return int(np.sum(bad)), int(np.sum(near)), idx_o.size, int(np.sum(diff))
+
+
+def check_float_rows(x16, signs, fmt, rows_gpu):
+    """fp16 / fp8 rows: every stored value must be the format's rounding of SOME value within
+    the kernel's rotation error tau of the exact rotated coordinate, i.e. lie between the
+    roundings of x~ - tau and x~ + tau (rounding is monotone; +0 and -0 compare equal).
+    Returns (values differing from the oracle's, values)."""
+    rows_o, _ = ocache.encode(x16, signs, fmt)
+    xr = orot.rotate(x16.astype(np.float64), signs)
+    tau = fwht_error_bound(x16)[:, None]
+    if fmt == "fp16":
+        def rnd(z):
+            return ofmt.to_f16(z).astype(np.float64)
+        vo = np.ascontiguousarray(rows_o).view(np.float16).astype(np.float64)
+        vg = np.ascontiguousarray(rows_gpu).view(np.float16).astype(np.float64)
+    else:
+        def rnd(z):
+            return ofmt.e4m3_decode(ofmt.e4m3_encode(ofmt.to_f32(z)))
+        vo, vg = ofmt.e4m3_decode(rows_o), ofmt.e4m3_decode(rows_gpu)
+    lo, hi = rnd(xr - tau), rnd(xr + tau)
+    ok = (vg >= lo) & (vg <= hi)
+    if not np.all(ok):
+        i = np.argwhere(~ok)[0]
+        raise AssertionError(f"{int(np.sum(~ok))} {fmt} values outside [RN(x-tau), RN(x+tau)]; first at {tuple(i)}: "
+                             f"gpu {vg[tuple(i)]!r} oracle {vo[tuple(i)]!r} exact {xr[tuple(i)]!r} tau {tau[i[0], 0]!r}")
+    return int(np.sum(vo != vg)), vo.size
+
+
+def check_int4_rows(x16, signs, rows_gpu, scales_gpu):
+    """INT4-g32 rows: each stored scale must be the rounding of max|x~|/7 for some max within
+    tau of the exact one, and each level the rounding of (x~ +- tau) / s with the scale the
+    GPU stored (plus one float32 rounding of the quotient).  Returns (levels differing from the
+    oracle's, scales differing, levels)."""
+    d = x16.shape[-1]
+    n = len(x16)
+    rows_o, sc_o = ocache.encode(x16, signs, "int4_g32")
+    xr = orot.rotate(x16.astype(np.float64), signs)
+    tau = fwht_error_bound(x16)[:, None]
+    g = xr.reshape(n, d // 32, 32)
+    amax = np.max(np.abs(g), axis=-1)
+    s_lo = ofmt.to_f16(ofmt.to_f32(np.maximum(amax - tau, 0) / 7)).astype(np.float64)
+    s_hi = ofmt.to_f16(ofmt.to_f32((amax + tau) / 7)).astype(np.float64)
+    sg = np.asarray(scales_gpu, dtype=np.float16).astype(np.float64)
+    assert np.all((sg >= s_lo) & (sg <= s_hi)), "group scale outside the rounding interval"
+    q_g = ofmt.unpack_bits(rows_gpu, 4, d).reshape(n, d // 32, 32).astype(np.int64) - 8
+    q_o = ofmt.unpack_bits(rows_o, 4, d).reshape(n, d // 32, 32).astype(np.int64) - 8
+    s = sg[..., None]
+    t3 = tau[..., None] + 8 * 2.0 ** -24 * s
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lo = np.where(s > 0, np.clip(np.rint(ofmt.to_f32((g - t3) / np.where(s > 0, s, 1)).astype(np.float64)), -7, 7), 0)
+        hi = np.where(s > 0, np.clip(np.rint(ofmt.to_f32((g + t3) / np.where(s > 0, s, 1)).astype(np.float64)), -7, 7), 0)
+    ok = (q_g >= lo) & (q_g <= hi)
+    assert np.all(ok), f"{int(np.sum(~ok))} INT4 levels outside the rounding interval"
+    return int(np.sum(q_g != q_o)), int(np.sum(sg != sc_o.astype(np.float64))), q_g.size
+
+
+# ----------------------------------------------------------------------------- exact-bytes decode setup
+
+
+class Built:
+    """An oracle pool and the GPU cache holding the same bytes."""
+
+    def __init__(self, ora_tiers, gpu_caches, views, k_signs, v_signs):
+        self.ora, self.gpu, self.views, self.k_signs, self.v_signs = ora_tiers, gpu_caches, views, k_signs, v_signs
+
+
+def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16, shuffle_seed=None):
+    """tier_specs: list of workloads.Tier; tier_kv: per tier, per sequence, (k [L, Hkv, D], v)
+    fp16.  The ORACLE encodes every row into numpy pools; those bytes are uploaded into the
+    GPU caches unchanged.  Returns Built."""
+    hkv, d = k_signs.shape
+    batch = len(tier_kv[0])
+    rng = np.random.default_rng(shuffle_seed)
+    ora_tiers, gpu, views = [], [], []
+    ks_dev = torch.from_numpy(k_signs).cuda()
+    vs_dev = torch.from_numpy(v_signs).cuda()
+    for spec, seqs in zip(tier_specs, tier_kv):
+        lens = np.array([k.shape[0] for k, _ in seqs])
+        per = [(int(n) + page_size - 1) // page_size for n in lens]
+        num_pages = max(1, sum(per) + 2)
+        phys = rng.permutation(num_pages) if shuffle_seed is not None else np.arange(num_pages)
+        maxp = max(1, max(per))
+        bt = np.zeros((batch, maxp), dtype=np.int32)
+        at = 0
+        for b, n in enumerate(per):
+            bt[b, :n] = phys[at: at + n]
+            at += n
+        kc = tables(spec.codebook, spec.k_bits) if spec.k_format == "codebook" else (None, None)
+        vc = tables(spec.codebook, spec.v_bits) if spec.v_format == "codebook" else (None, None)
+        ks = ocache.new_side(spec.k_format, spec.k_bits, kc[0], kc[1], k_signs, num_pages, hkv, page_size, d)
+        vs = ocache.new_side(spec.v_format, spec.v_bits, vc[0], vc[1], v_signs, num_pages, hkv, page_size, d)
+        for b, (k, v) in enumerate(seqs):
+            t = np.arange(k.shape[0])
+            slots = bt[b, t // page_size] * page_size + t % page_size
+            ocache.write(ks, slots, k, page_size)
+            ocache.write(vs, slots, v, page_size)
+        ora_tiers.append(oatt.TierState(ks, vs, bt, lens, page_size))
+        c = kvq.PagedCache(d, hkv, num_pages, spec.k_format, spec.v_format, spec.k_bits, spec.v_bits,
+                           ks_dev, vs_dev, page_size, spec.codebook)
+        c.k_rows.copy_(torch.from_numpy(ks.rows))
+        c.v_rows.copy_(torch.from_numpy(vs.rows))
+        if ks.aux is not None:
+            c.k_aux.copy_(torch.from_numpy(ks.aux.reshape(c.k_aux.shape)))
+        if vs.aux is not None:
+            c.v_aux.copy_(torch.from_numpy(vs.aux.reshape(c.v_aux.shape)))
+        gpu.append(c)
+        views.append(kvq.TierView(c, torch.from_numpy(bt).cuda(), torch.from_numpy(lens.astype(np.int32)).cuda()))
+    return Built(ora_tiers, gpu, views, k_signs, v_signs)
+
+
+def gpu_decode(kvq, torch, views, q16, split_tokens=0):
+    q = torch.from_numpy(q16).cuda()
+    b, hq, d = q16.shape
+    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, kvq.kvq_decode_workspace_size(views, b, hq, split_tokens)), dtype=torch.uint8,
+                     device="cuda")
+    kvq.kvq_decode_attention(views, q, out, ws, split_tokens)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()

@@ -1,0 +1,184 @@
+"""GPU parity of kvq_decode_attention against the oracle.
+
+Exact-bytes cases: the ORACLE encodes the cache; the same bytes are uploaded to the GPU;
+GPU decode attention must match the oracle's dequantise-then-attend within 2e-3 max-abs.
+Shapes follow each workload at sizes the oracle finishes in seconds, spanning several
+pages and split-K chunks with ragged tails."""
+import math
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import attention as oatt
+from tests import gpu_util as gu
+
+
+def seqs_for(cfg, lens):
+    """Per tier, per sequence (k, v) for the given total lengths."""
+    per_seq = [W.sequence_tiers(cfg, b, int(n)) for b, n in enumerate(lens)]
+    return [[per_seq[b][t] for b in range(len(lens))] for t in range(len(cfg.tiers))]
+
+
+def run_exact(cfg, lens, split_tokens=0, shuffle=None, q=None):
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_module()
+    tiers_kv = seqs_for(cfg, lens)
+    built = gu.build_exact(kvq, torch, list(cfg.tiers), tiers_kv, W.signs(cfg, 0), W.signs(cfg, 1),
+                           cfg.page_size, shuffle)
+    if q is None:
+        q = W.queries(cfg.scaled(batch=len(lens)))
+    got = gu.gpu_decode(kvq, torch, built.views, q, split_tokens)
+    want = oatt.decode_attention(q, built.ora)
+    return got, want, built, q
+
+
+EXACT_CASES = {
+    "tiny_full": (W.CONFIGS["tiny"], [1024]),
+    "llama7b": (W.CONFIGS["llama7b"].scaled(batch=2, num_q_heads=4, num_kv_heads=4), [1000, 777]),
+    "gqa32k": (W.CONFIGS["gqa32k"].scaled(batch=2, num_q_heads=8, num_kv_heads=2), [3000, 2111]),
+    "ragged": (W.CONFIGS["ragged"].scaled(batch=5, num_q_heads=8, num_kv_heads=2, seq_len=2500, ragged_min=1), None),
+    "append_d256": (W.CONFIGS["append"].scaled(batch=2, num_q_heads=4, num_kv_heads=4, seq_len=1500), [1500, 1499]),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", list(EXACT_CASES))
+def test_decode_matches_oracle(name):
+    cfg, lens = EXACT_CASES[name]
+    if lens is None:
+        lens = list(W.seq_lens(cfg))
+    got, want, _, _ = run_exact(cfg, lens, shuffle=7 if cfg.shuffle_pages else None)
+    err = np.abs(got - want)
+    scale = np.abs(want).max()
+    print(f"{name}: max-abs {err.max():.3e} (output max {scale:.3f})")
+    assert np.all(np.isfinite(got))
+    assert err.max() <= gu.ATOL_OUT
+    assert err.max() <= 1e-4 * max(1.0, scale)  # fp32 accumulation: far inside the bound
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_decode_edge_lengths_and_groups(group):
+    """Lengths 0, 1, 15, 16, 17 and a multi-chunk one in one batch, for every group size."""
+    hkv = 2
+    cfg = W.CONFIGS["llama7b"].scaled(batch=6, num_q_heads=hkv * group, num_kv_heads=hkv)
+    lens = [0, 1, 15, 16, 17, 700]
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=64, shuffle=3)
+    assert np.all(got[0] == 0)  # empty context
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
+@pytest.mark.gpu
+def test_decode_two_tier_edge_lengths():
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=5, num_q_heads=8, num_kv_heads=2)
+    lens = [1, 9, 10, 11, 1234]  # near tier holds round(0.1 L): 0, 1, 1, 1, 123 tokens
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=32)
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
+@pytest.mark.gpu
+def test_split_invariance():
+    """Split-K over 1, 2, 7 chunks and one chunk per page gives the same output."""
+    cfg = W.CONFIGS["ragged"].scaled(batch=2, num_q_heads=8, num_kv_heads=2)
+    lens = [1777, 1760]
+    outs = []
+    for split in (1792, 896, 256, 16):
+        got, want, _, _ = run_exact(cfg, lens, split_tokens=split)
+        outs.append(got)
+        assert np.abs(got - want).max() <= gu.ATOL_OUT
+    for o in outs[1:]:
+        np.testing.assert_allclose(o, outs[0], rtol=0, atol=2e-6 * max(1.0, np.abs(outs[0]).max()))
+
+
+@pytest.mark.gpu
+def test_fp16_cache_equals_plain_attention():
+    """With the cache stored as fp16 (no codes), decode attention equals plain
+    softmax(q K^T / sqrt(d)) V over the original fp16 keys/values, up to the fp16 rounding
+    of the stored rotated vectors (relative 2^-11 per element)."""
+    torch = gu.torch_cuda()
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=2, num_q_heads=8, num_kv_heads=2, tiers=(W.Tier("fp16", "fp16"),),
+                                     outlier_mode="none")
+    lens = [900, 533]
+    got, _, _, q = run_exact(cfg, lens)
+    g = cfg.group
+    for b, n in enumerate(lens):
+        ks, vs = W.sequence_kv(cfg, b, n)
+        for h in range(cfg.num_q_heads):
+            k = torch.from_numpy(ks[h // g].astype(np.float64))
+            v = torch.from_numpy(vs[h // g].astype(np.float64))
+            qq = torch.from_numpy(q[b, h].astype(np.float64))
+            ref = torch.nn.functional.scaled_dot_product_attention(qq[None, None, None], k[None, None],
+                                                                   v[None, None])[0, 0, 0].numpy()
+            # fp16 rounding of rotated K shifts scores by <= 2^-11 * |q||k|/sqrt(d) ~ 5e-3 here
+            assert np.abs(got[b, h] - ref).max() < 2e-2
+            assert np.linalg.norm(got[b, h] - ref) / np.linalg.norm(ref) < 5e-3
+
+
+# ----------------------------------------------------------------------------- full sizes
+
+
+def oracle_sampled(cfg, b, g, total, tier_override=None):
+    """Oracle keys/values (original domain) of sequence b, kv head g, encoded by the oracle
+    from the same seeded inputs; tiers split as the workload splits them."""
+    from oracle import cache as ocache
+    ks, vs = W.sequence_kv(cfg, b, total)
+    members = W.tier_members(cfg, b, g, total)
+    sk, sv = W.signs(cfg, 0)[g], W.signs(cfg, 1)[g]
+    K, V = [], []
+    for t, tier in enumerate(cfg.tiers):
+        k = ks[g][members[t]]
+        v = vs[g][members[t]]
+        if tier_override is not None and t in tier_override:
+            k, v = tier_override[t](k, v)
+        kt = gu.tables(tier.codebook, tier.k_bits) if tier.k_format == "codebook" else (None, None)
+        vt = gu.tables(tier.codebook, tier.v_bits) if tier.v_format == "codebook" else (None, None)
+        rk, ak = ocache.encode(k, sk, tier.k_format, tier.k_bits, kt[1])
+        rv, av = ocache.encode(v, sv, tier.v_format, tier.v_bits, vt[1])
+        K.append(ocache.decode(rk, ak, tier.k_format, sk, cfg.head_dim, tier.k_bits, kt[0]))
+        V.append(ocache.decode(rv, av, tier.v_format, sv, cfg.head_dim, tier.v_bits, vt[0]))
+    return np.concatenate(K), np.concatenate(V)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["tiny", "llama7b", "gqa32k", "ragged", "append"])
+def test_full_size_sampled_heads(name):
+    """Every workload at its full size, quantised by the GPU and decoded with the split plan
+    the benchmark uses; sampled (sequence, query head) outputs recomputed by the oracle from
+    the same seeded inputs (the oracle encodes its own copy).  Codes may differ only at
+    decision boundaries, so the bound is the 2e-3 output tolerance."""
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_module()
+    cfg = W.CONFIGS[name]
+    wl = W.GpuWorkload(cfg)
+    override = {}
+    if cfg.prefill_chunk:
+        # append the prefill chunk through the library, then decode at the new length
+        for b in range(cfg.batch):
+            k, v = W.chunk_kv(cfg, b, 0, cfg.prefill_chunk)
+            wl.append(len(cfg.tiers) - 1, b, int(wl.lens[b]) + np.arange(cfg.prefill_chunk), k, v)
+        wl.set_len(len(cfg.tiers) - 1, wl.tier_len[-1] + cfg.prefill_chunk)
+    q = W.queries(cfg)
+    got = gu.gpu_decode(kvq, torch, wl.views(), q)
+    rng = np.random.default_rng(11)
+    picks = [(int(rng.integers(cfg.batch)), int(rng.integers(cfg.num_q_heads))) for _ in range(3)]
+    picks.append((cfg.batch - 1, cfg.num_q_heads - 1))
+    for b, h in picks:
+        g = h // cfg.group
+        total = int(wl.lens[b])
+        K, V = oracle_sampled(cfg, b, g, total)
+        if cfg.prefill_chunk:
+            from oracle import cache as ocache
+            tier = cfg.tiers[-1]
+            k, v = W.chunk_kv(cfg, b, 0, cfg.prefill_chunk)
+            kt = gu.tables(tier.codebook, tier.k_bits)
+            rk, ak = ocache.encode(k[:, g], W.signs(cfg, 0)[g], tier.k_format, tier.k_bits, kt[1])
+            rv, av = ocache.encode(v[:, g], W.signs(cfg, 1)[g], tier.v_format, tier.v_bits, kt[1])
+            K = np.concatenate([K, ocache.decode(rk, ak, tier.k_format, W.signs(cfg, 0)[g], cfg.head_dim,
+                                                 tier.k_bits, kt[0])])
+            V = np.concatenate([V, ocache.decode(rv, av, tier.v_format, W.signs(cfg, 1)[g], cfg.head_dim,
+                                                 tier.v_bits, kt[0])])
+        want = oatt.attend(q[b, h].astype(np.float64), K, V)
+        err = np.abs(got[b, h] - want).max()
+        print(f"{name} b={b} h={h}: max-abs {err:.3e}")
+        assert err <= gu.ATOL_OUT

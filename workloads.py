@@ -240,3 +240,106 @@ def page_map(cfg: Config, lens: np.ndarray, tier: int = 0, spare_pages: int = 0)
 def kv_bytes_fp16(cfg: Config, total_tokens: int) -> int:
     """Bytes of an unquantised fp16 K+V cache holding `total_tokens` per kv head."""
     return total_tokens * cfg.num_kv_heads * cfg.head_dim * 2 * 2
+
+
+# ----------------------------------------------------------------------------- assembly
+
+
+def capacity(cfg: Config) -> int:
+    """Largest number of tokens any sequence reaches (context + appended chunk + steps)."""
+    return cfg.seq_len + cfg.prefill_chunk + cfg.decode_steps
+
+
+def sequence_kv(cfg: Config, b: int, total: int):
+    """Per-head fp16 keys and values of sequence b's first `total` positions:
+    two lists over kv heads of [total, D] arrays."""
+    ks = [kv_head(cfg, 0, b, h, total) for h in range(cfg.num_kv_heads)]
+    vs = [kv_head(cfg, 1, b, h, total) for h in range(cfg.num_kv_heads)]
+    return ks, vs
+
+
+def sequence_tiers(cfg: Config, b: int, total: int):
+    """Token-major K/V of sequence b split into tiers: a list over tiers of
+    (k [L_t, Hkv, D], v [L_t, Hkv, D]) fp16.  Slot t of a tier holds, for kv head h, the
+    t-th (in position order) token of h that belongs to the tier."""
+    ks, vs = sequence_kv(cfg, b, total)
+    lens = tier_lens(cfg, total)
+    out = [(np.empty((n, cfg.num_kv_heads, cfg.head_dim), np.float16),
+            np.empty((n, cfg.num_kv_heads, cfg.head_dim), np.float16)) for n in lens]
+    for h in range(cfg.num_kv_heads):
+        for t, members in enumerate(tier_members(cfg, b, h, total)):
+            out[t][0][:, h] = ks[h][members]
+            out[t][1][:, h] = vs[h][members]
+    return out
+
+
+def chunk_kv(cfg: Config, b: int, stream: int, n: int):
+    """Token-major fp16 K/V [n, Hkv, D] of n appended tokens of sequence b, drawn from the
+    appended-token stream `stream` (0 = prefill chunk, 1 + s = decode step s)."""
+    k = np.stack([kv_head(cfg, 0, b, h, n, stream=stream) for h in range(cfg.num_kv_heads)], axis=1)
+    v = np.stack([kv_head(cfg, 1, b, h, n, stream=stream) for h in range(cfg.num_kv_heads)], axis=1)
+    return k, v
+
+
+class GpuWorkload:
+    """The cache of a config built on the GPU through the library's quantize-append, one
+    sequence at a time (host fp16 -> device -> kvq_quantize_append).  Holds one PagedCache
+    and block table per tier, sized for `capacity(cfg)` tokens per sequence."""
+
+    def __init__(self, cfg: Config, device: str = "cuda", fill: bool = True):
+        import torch
+        import quantized_decode_attention_rht_gb300 as kvq
+
+        self.cfg = cfg
+        self.lens = seq_lens(cfg)  # context length per sequence
+        cap = np.array([min(capacity(cfg), int(n) + cfg.prefill_chunk + cfg.decode_steps)
+                        for n in self.lens])
+        ntier = len(cfg.tiers)
+        # capacity per tier: every appended token goes to the last tier
+        cap_t = [np.array([tier_lens(cfg, int(n))[t] for n in self.lens]) for t in range(ntier)]
+        cap_t[-1] = cap_t[-1] + (cap - self.lens)
+        self.maps = [page_map(cfg, cap_t[t], tier=t) for t in range(ntier)]
+        self.tier_len = [np.array([tier_lens(cfg, int(n))[t] for n in self.lens]) for t in range(ntier)]
+        ks, vs = signs(cfg, 0), signs(cfg, 1)
+        self.k_signs = torch.from_numpy(ks).to(device)
+        self.v_signs = torch.from_numpy(vs).to(device)
+        self.caches = []
+        for t, tier in enumerate(cfg.tiers):
+            self.caches.append(kvq.PagedCache(cfg.head_dim, cfg.num_kv_heads, self.maps[t].num_pages,
+                                              tier.k_format, tier.v_format, tier.k_bits, tier.v_bits,
+                                              self.k_signs, self.v_signs, cfg.page_size, tier.codebook, device))
+        self.block_tables = [torch.from_numpy(np.maximum(m.block_table, 0)).to(device) for m in self.maps]
+        self.seq_lens_dev = [torch.from_numpy(l.astype(np.int32)).to(device) for l in self.tier_len]
+        self.device = device
+        if fill:
+            for b in range(cfg.batch):
+                for t, (k, v) in enumerate(sequence_tiers(cfg, b, int(self.lens[b]))):
+                    self.append(t, b, np.arange(k.shape[0]), k, v)
+            torch.cuda.synchronize()
+
+    def append(self, tier: int, b: int, positions, k: np.ndarray, v: np.ndarray, stream=None):
+        """Quantise-and-append host fp16 K/V [n, Hkv, D] at `positions` of sequence b."""
+        import torch
+        slots = torch.from_numpy(self.maps[tier].slots(b, positions)).to(self.device)
+        kd = torch.from_numpy(np.ascontiguousarray(k)).to(self.device)
+        vd = torch.from_numpy(np.ascontiguousarray(v)).to(self.device)
+        self.caches[tier].append(kd, vd, slots, stream)
+
+    def set_len(self, tier: int, lens: np.ndarray):
+        import torch
+        self.tier_len[tier] = np.asarray(lens)
+        self.seq_lens_dev[tier].copy_(torch.from_numpy(self.tier_len[tier].astype(np.int32)))
+
+    def views(self):
+        import quantized_decode_attention_rht_gb300 as kvq
+        return [kvq.TierView(c, bt, sl) for c, bt, sl in zip(self.caches, self.block_tables, self.seq_lens_dev)]
+
+    def cache_bytes(self) -> int:
+        """Algorithmic bytes of the cache rows + side data that one decode call reads."""
+        total = 0
+        import quantized_decode_attention_rht_gb300 as kvq
+        for t, tier in enumerate(self.cfg.tiers):
+            rk, ak = kvq.kvq_row_bytes(tier.k_format, tier.k_bits, self.cfg.head_dim)
+            rv, av = kvq.kvq_row_bytes(tier.v_format, tier.v_bits, self.cfg.head_dim)
+            total += int(self.tier_len[t].sum()) * self.cfg.num_kv_heads * (rk + ak + rv + av)
+        return total
