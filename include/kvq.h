@@ -22,7 +22,8 @@
  * Conventions that hold for every function:
  *   - Pointers are DEVICE pointers unless the comment says "host".
  *   - The caller owns every buffer.  The library allocates nothing, keeps no mutable
- *     global state, never synchronises, and is safe to call from several threads.
+ *     global state (kvq_decode_attention_noalloc, at the end, is the one exception),
+ *     never synchronises, and is safe to call from several threads.
  *   - GPU work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
  *     stream) and ordered with the caller's other work on that stream.
  *   - Arguments are checked on the host before anything is launched; a failed check
@@ -175,6 +176,29 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
                                         int32_t num_q_heads, int32_t split_tokens,
                                         float* out, void* workspace,
                                         size_t workspace_bytes, void* stream);
+
+/* Decode attention for callers that cannot allocate device memory.
+ *
+ * Same computation, arguments and results as kvq_decode_attention, without the workspace
+ * arguments: the split-K scratch is a static device array inside the library, of
+ * KVQ_NOALLOC_SCRATCH_BYTES bytes, that every GPU which loads the library holds until the
+ * process exits.  This has no counterpart in the pages; it exists for callers that may not
+ * call cudaMalloc or any allocating routine -- for example a plugin running inside a
+ * serving framework that hands out no device memory, or a serving loop whose memory budget
+ * is fixed at start-up and forbids later allocations.  This entry point allocates nothing.
+ *
+ * The first call made while a given device is current looks up that device's scratch
+ * address (cudaGetSymbolAddress) and remembers it; make that first call before any stream
+ * capture.  Shapes needing more than KVQ_NOALLOC_SCRATCH_BYTES of scratch (see
+ * kvq_decode_workspace_size) return KVQ_ERR_WORKSPACE_TOO_SMALL and launch nothing.
+ * Every call on a device shares the one array and it keeps the last call's contents
+ * (nothing in it needs to start at zero); calls whose work overlaps on the GPU (different
+ * streams, or different host threads) race on it and must be serialised by the caller. */
+#define KVQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_tier_view* tiers, int32_t num_tiers,
+                                                const uint16_t* q, int32_t batch,
+                                                int32_t num_q_heads, int32_t split_tokens,
+                                                float* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "kvq_quantize_append": [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp],
             "kvq_decode_workspace_size": [ctypes.POINTER(KvqTierView), i32, i32, i32, i32, szp],
             "kvq_decode_attention": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz, vp],
+            "kvq_decode_attention_noalloc": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp],
         }
         for name, args in sigs.items():
             f = getattr(h, name)
@@ -184,6 +185,19 @@ def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().kvq_decode_attention(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out), _ptr(workspace),
                                       ws_bytes, _stream(stream)), "kvq_decode_attention")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def kvq_decode_attention_noalloc(tiers, q, out, split_tokens: int = 0, stream=None) -> None:
+    """Decode attention using the library's static device scratch (no allocation anywhere);
+    for callers that may not allocate device memory.  Calls that overlap on the GPU race on
+    the shared scratch."""
+    arr = _views(tiers)
+    b, hq, _ = q.shape
+    _check(lib().kvq_decode_attention_noalloc(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out),
+                                              _stream(stream)), "kvq_decode_attention_noalloc")
 
 
 # ----------------------------------------------------------------------------- device buffers

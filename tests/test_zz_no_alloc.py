@@ -1,0 +1,72 @@
+"""kvq_decode_attention_noalloc, the decode entry point for callers that may not allocate
+device memory (plugins inside a framework that owns all device memory, serving loops with a
+memory budget fixed at start-up): it uses the library's static device scratch instead of a
+caller-provided workspace.  Its results must match kvq_decode_attention's on the same inputs,
+on consecutive calls (the scratch keeps the previous call's contents)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads as W
+from tests import gpu_util as gu
+
+
+def _two_tier_cache(kvq, torch, cfg, lens):
+    ks, vs = W.signs(cfg, 0), W.signs(cfg, 1)
+    ks_d, vs_d = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    per_seq = [W.sequence_tiers(cfg, b, n) for b, n in enumerate(lens)]
+    views = []
+    for t, tier in enumerate(cfg.tiers):
+        tl = np.array([per_seq[b][t][0].shape[0] for b in range(len(lens))])
+        pm = W.page_map(cfg, tl, tier=t)
+        cache = kvq.PagedCache(cfg.head_dim, cfg.num_kv_heads, max(1, pm.num_pages), tier.k_format, tier.v_format,
+                               tier.k_bits, tier.v_bits, ks_d, vs_d, cfg.page_size)
+        for b in range(len(lens)):
+            k, v = per_seq[b][t]
+            slots = pm.slots(b, np.arange(k.shape[0]))
+            cache.append(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), torch.from_numpy(slots).cuda())
+        views.append(kvq.TierView(cache, torch.from_numpy(np.maximum(pm.block_table, 0)).cuda(),
+                                  torch.from_numpy(tl.astype(np.int32)).cuda()))
+    return views
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_workspace_entry_point():
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_module()
+    lens = [2100, 999, 16]
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=len(lens), num_q_heads=8, num_kv_heads=2)
+    views = _two_tier_cache(kvq, torch, cfg, lens)
+    for step in range(2):  # two calls in a row, different queries
+        q = torch.from_numpy(W.queries(cfg, step=step)).cuda()
+        ref = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        ws = torch.empty(kvq.kvq_decode_workspace_size(views, len(lens), cfg.num_q_heads), dtype=torch.uint8,
+                         device="cuda")
+        kvq.kvq_decode_attention(views, q, ref, ws)
+        out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+        kvq.kvq_decode_attention_noalloc(views, q, out)
+        torch.cuda.synchronize()
+        err = (out - ref).abs().max().item()
+        assert torch.isfinite(out).all().item()
+        assert err <= gu.ATOL_OUT, err
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    gu.torch_cuda()
+    kvq = gu.kvq_module()
+    s = kvq.KvqCache()
+    s.head_dim, s.num_kv_heads, s.page_size, s.num_pages = 128, 8, 16, 4
+    s.k_format = s.v_format = kvq.FMT_CODEBOOK
+    s.k_bits = s.v_bits = 4
+    for i, f in enumerate(("k_rows", "v_rows", "k_aux", "v_aux", "k_centroids", "k_bounds", "v_centroids",
+                           "v_bounds", "k_signs", "v_signs")):
+        setattr(s, f, (1 << 40) + 4096 * i)  # never dereferenced: the size check comes first
+    views = (kvq.KvqTierView * 1)()
+    views[0].cache = ctypes.pointer(s)
+    views[0].block_table = 1 << 43
+    views[0].seq_lens = 1 << 44
+    views[0].max_pages = 1 << 16  # 1M tokens with 16-token splits: far more scratch than it has
+    st = kvq.lib().kvq_decode_attention_noalloc(views, 1, 1 << 45, 64, 32, 16, 1 << 46, None)
+    assert st == 3  # KVQ_ERR_WORKSPACE_TOO_SMALL
