@@ -38,6 +38,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="gqa32k")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per GPU (default: the workload's); smaller cases for profiling")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -133,10 +135,12 @@ def barrier(ws: int):
 # ----------------------------------------------------------------------------- workload
 
 
-def rank_config(name: str, rank: int):
+def rank_config(name: str, rank: int, batch: int = 0):
     """Each rank holds its own batch of sequences (weak scaling): same shapes, its own seed."""
     import workloads as W
     cfg = W.CONFIGS[name]
+    if batch:
+        cfg = cfg.scaled(batch=batch)
     return cfg if rank == 0 else cfg.scaled(seed=cfg.seed + 1000 * rank)
 
 
@@ -336,7 +340,7 @@ def run_ours(args):
     import workloads as W
 
     kvq.lib()
-    cfg = rank_config(args.config, rank)
+    cfg = rank_config(args.config, rank, args.batch)
     wl = W.GpuWorkload(cfg)
     views = wl.views()
     last = len(cfg.tiers) - 1

@@ -250,12 +250,26 @@ def capacity(cfg: Config) -> int:
     return cfg.seq_len + cfg.prefill_chunk + cfg.decode_steps
 
 
+_POOL = None
+
+
+def _pool():
+    """Threads for generation: every (sequence, head) has its own stream and numpy's bulk
+    random fills release the GIL, so heads are drawn in parallel with identical results."""
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures
+        import os
+        _POOL = concurrent.futures.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
 def sequence_kv(cfg: Config, b: int, total: int):
     """Per-head fp16 keys and values of sequence b's first `total` positions:
     two lists over kv heads of [total, D] arrays."""
-    ks = [kv_head(cfg, 0, b, h, total) for h in range(cfg.num_kv_heads)]
-    vs = [kv_head(cfg, 1, b, h, total) for h in range(cfg.num_kv_heads)]
-    return ks, vs
+    jobs = [(w, h) for w in (0, 1) for h in range(cfg.num_kv_heads)]
+    out = list(_pool().map(lambda j: kv_head(cfg, j[0], b, j[1], total), jobs))
+    return out[: cfg.num_kv_heads], out[cfg.num_kv_heads:]
 
 
 def sequence_tiers(cfg: Config, b: int, total: int):
