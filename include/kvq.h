@@ -191,9 +191,10 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
  * address (cudaGetSymbolAddress) and remembers it; make that first call before any stream
  * capture.  Shapes needing more than KVQ_NOALLOC_SCRATCH_BYTES of scratch (see
  * kvq_decode_workspace_size) return KVQ_ERR_WORKSPACE_TOO_SMALL and launch nothing.
- * Every call on a device shares the one array and it keeps the last call's contents
- * (nothing in it needs to start at zero); calls whose work overlaps on the GPU (different
- * streams, or different host threads) race on it and must be serialised by the caller. */
+ * Every call on a device shares the one array and it keeps the last call's contents (each
+ * call clears, on its stream, the part that must start at zero); calls whose work overlaps
+ * on the GPU (different streams, or different host threads) race on it and must be
+ * serialised by the caller. */
 #define KVQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_tier_view* tiers, int32_t num_tiers,
                                                 const uint16_t* q, int32_t batch,

@@ -1,4 +1,5 @@
 // C ABI of libkvq.so: argument checks, split-K planning and kernel launches.
+#include <algorithm>
 #include <cstring>
 
 #include "kvq_internal.cuh"
@@ -60,16 +61,38 @@ struct Plan {
   int chunk[KVQ_MAX_TIERS];
   int splits[KVQ_MAX_TIERS];
   int total;
+  bool fast;  // every tier qualifies for the fused tensor-core kernel
 };
 
-kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hkv, int split_tokens, Plan* plan) {
-  const int ps = tiers[0].cache->page_size;
+size_t token_bytes(const kvq_cache* c) {
+  size_t rk, ak, rv, av;
+  side_bytes(c->k_format, c->k_bits, c->head_dim, &rk, &ak);
+  side_bytes(c->v_format, c->v_bits, c->head_dim, &rv, &av);
+  return rk + ak + rv + av;
+}
+
+kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int split_tokens, Plan* plan) {
+  const kvq_cache* c0 = tiers[0].cache;
+  const int ps = c0->page_size, hkv = c0->num_kv_heads, group = hq / hkv;
   if (split_tokens < 0 || split_tokens % ps) return KVQ_ERR_INVALID_ARGUMENT;
+  plan->fast = ps == 16;
+  for (int i = 0; i < n; ++i)
+    plan->fast = plan->fast && gqa_fast_supported(c0->head_dim, group, tiers[i].cache->k_format,
+                                                  tiers[i].cache->v_format);
+  if (split_tokens > gqa_max_chunk_tokens()) plan->fast = false;
+  // fused kernel: items of about equal bytes, ~4 per warp of a full GPU
+  size_t total_bytes = 0;
+  for (int i = 0; i < n; ++i)
+    total_bytes += (size_t)batch * hkv * tiers[i].max_pages * ps * token_bytes(tiers[i].cache);
+  const size_t item_bytes = std::max<size_t>(64 << 10, total_bytes / (kSms * 8 * 4));
   plan->total = 0;
   for (int i = 0; i < n; ++i) {
     const long long max_len = (long long)tiers[i].max_pages * ps;
     int chunk = split_tokens;
-    if (chunk == 0) {
+    if (chunk == 0 && plan->fast) {
+      const size_t tok = item_bytes / token_bytes(tiers[i].cache);
+      chunk = (int)std::min<size_t>(gqa_max_chunk_tokens(), std::max<size_t>(ps, tok / ps * ps));
+    } else if (chunk == 0) {
       // aim at ~16 CTAs per SM in total, chunks of 256 .. 4096 tokens
       const long long work = (long long)batch * hkv * max_len;
       long long want = work / (kSms * 16) + 1;
@@ -115,9 +138,10 @@ kvq_status check_tiers(const kvq_tier_view* tiers, int n, int batch, int hq) {
   return KVQ_OK;
 }
 
+// Workspace: partial accumulators [B][Hq][S][D], (max, sum) [B][Hq][S][2], work counter.
 size_t workspace_bytes(int batch, int hq, int d, int total_splits) {
   const size_t parts = (size_t)batch * hq * total_splits;
-  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256);
+  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256) + 256;
 }
 
 }  // namespace
@@ -193,8 +217,7 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
   kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
   if (st != KVQ_OK) return st;
   Plan plan;
-  if ((st = make_plan(tiers, num_tiers, batch, tiers[0].cache->num_kv_heads, split_tokens, &plan)) != KVQ_OK)
-    return st;
+  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, &plan)) != KVQ_OK) return st;
   *bytes = workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total);
   return KVQ_OK;
 }
@@ -209,7 +232,7 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
   const kvq_cache* c0 = tiers[0].cache;
   const int d = c0->head_dim, hkv = c0->num_kv_heads;
   Plan plan;
-  if ((st = make_plan(tiers, num_tiers, batch, hkv, split_tokens, &plan)) != KVQ_OK) return st;
+  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, &plan)) != KVQ_OK) return st;
   const size_t need = workspace_bytes(batch, num_q_heads, d, plan.total);
   if (need > 0 && (!workspace || !aligned(workspace, 256))) return KVQ_ERR_INVALID_ARGUMENT;
   if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
@@ -253,8 +276,10 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
   p.hkv = hkv;
   p.page_size = c0->page_size;
   p.total_splits = plan.total;
+  int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + need - 256);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(p, d, num_q_heads / hkv, s);
+  const bool fast = plan.fast && aligned(q, 16);
+  cudaError_t e = fast ? launch_decode_gqa(p, counter, s) : launch_decode(p, d, num_q_heads / hkv, s);
   if (e == cudaSuccess) e = launch_combine(p, d, s);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

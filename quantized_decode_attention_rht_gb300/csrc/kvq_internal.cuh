@@ -58,6 +58,12 @@ struct DecParams {
 };
 
 cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStream_t stream);
+// Fused tensor-core decode for head_dim 128, 4 query heads per kv head, tiers stored as
+// fp16/fp16 or fp8-E4M3/INT4-g32 (one launch for every tier).  `counter` is one int of
+// device scratch, cleared by the launcher.
+bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
+int gqa_max_chunk_tokens();
+cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t stream);
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream);
 
 // ------------------------------------------------------------------------ device helpers

@@ -48,8 +48,8 @@ extern "C" KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_tier_view* 
   if (need > kNoAllocScratchBytes) return KVQ_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   if ((st = scratch_for_current_device(&scratch)) != KVQ_OK) return st;
-  // Nothing in the scratch has to start at zero: the split-K pass writes every partial the
-  // combine pass reads.
+  // The decode call itself clears the one word of scratch that must start at zero (its work
+  // counter); the split-K pass writes every partial before the combine pass reads it.
   return kvq_decode_attention(tiers, num_tiers, q, batch, num_q_heads, split_tokens, out, scratch,
                               kNoAllocScratchBytes, stream);
 }
