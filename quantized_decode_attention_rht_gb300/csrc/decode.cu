@@ -8,8 +8,8 @@
 // units.  Per token it dequantises the K row in registers, forms the G scores, updates an
 // online softmax (running max / sum, one exp2 per score), and accumulates the value rows,
 // still in the rotated domain.  Partials (max, sum, acc[D]) go to the workspace.
-// Pass 2 (combine_kernel): per (sequence, query head) merge the partials of every split of
-// every tier, normalise, and undo the V rotation, y = s_V * (H y~) / sqrt(D).
+// Pass 2 (combine_kernel): one warp per (sequence, query head) merges the partials of every
+// split of every tier, normalises, and undoes the V rotation, y = s_V * (H y~) / sqrt(D).
 //
 // Lane layout: LPT lanes share a token, each holding DPL = D/LPT consecutive coordinates
 // of the G rotated queries and of the G value accumulators in registers; a warp advances
@@ -290,65 +290,87 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 }
 
 // ---------------------------------------------------------------- pass 2
+// One warp per (sequence, query head): lane l holds the D/32 consecutive coordinates
+// [l*D/32, (l+1)*D/32).  Merge the partials of every split of every tier (global max,
+// rescaled sums), normalise, then undo the V rotation with a Walsh-Hadamard transform
+// (in-register stages for the lane's coordinates, shuffles across lanes).
 template <int D>
 __global__ void __launch_bounds__(128) combine_kernel(const DecParams p) {
-  constexpr int PER = D / 128;
-  const int hq = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (pair >= p.batch * p.hq) return;
+  const int b = pair / p.hq, hq = pair % p.hq;
   const int hk = hq / (p.hq / p.hkv);
-  __shared__ float y_s[D];
-  __shared__ float red[128];
   const size_t base = ((size_t)b * p.hq + hq) * p.total_splits;
-  // global max over the valid splits of every tier
   float mx = -INFINITY;
   for (int ti = 0; ti < p.num_tiers; ++ti) {
     const DecTier& T = p.tier[ti];
     const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
-    for (int s = tid; s < n; s += 128) mx = fmaxf(mx, p.ws_ml[2 * (base + T.split_begin + s)]);
+    for (int s = lane; s < n; s += 32) mx = fmaxf(mx, p.ws_ml[2 * (base + T.split_begin + s)]);
   }
-  red[tid] = mx;
-  __syncthreads();
-  for (int o = 64; o > 0; o >>= 1) {
-    if (tid < o) red[tid] = fmaxf(red[tid], red[tid + o]);
-    __syncthreads();
-  }
-  mx = red[0];
-  __syncthreads();
-  float acc[PER] = {}, lsum = 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  float acc[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  float lsum = 0.f;
   if (mx != -INFINITY) {
     for (int ti = 0; ti < p.num_tiers; ++ti) {
       const DecTier& T = p.tier[ti];
       const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
+#pragma unroll 4
       for (int s = 0; s < n; ++s) {
         const size_t part = base + T.split_begin + s;
-        const float ms = p.ws_ml[2 * part];
-        if (ms == -INFINITY) continue;
-        const float f = exp2f(ms - mx);
-        lsum += p.ws_ml[2 * part + 1] * f;
+        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * part);
+        const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
+        lsum = fmaf(ml.y, f, lsum);
+        const float4* src = reinterpret_cast<const float4*>(p.ws_acc + part * D + lane * PER);
 #pragma unroll
-        for (int k = 0; k < PER; ++k) acc[k] += p.ws_acc[part * D + tid + 128 * k] * f;
+        for (int k = 0; k < PER / 4; ++k) {
+          const float4 v = src[k];
+          acc[4 * k] = fmaf(v.x, f, acc[4 * k]);
+          acc[4 * k + 1] = fmaf(v.y, f, acc[4 * k + 1]);
+          acc[4 * k + 2] = fmaf(v.z, f, acc[4 * k + 2]);
+          acc[4 * k + 3] = fmaf(v.w, f, acc[4 * k + 3]);
+        }
       }
     }
   }
   const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) y_s[tid + 128 * k] = acc[k] * inv;
-  __syncthreads();
-  // undo the V rotation: y = s_V * (H y~) / sqrt(D)
-  for (int hs = 1; hs < D; hs <<= 1) {
-    for (int i = tid; i < D / 2; i += 128) {
-      const int j = (i / hs) * 2 * hs + (i % hs);
-      const float a = y_s[j], c = y_s[j + hs];
-      y_s[j] = a + c;
-      y_s[j + hs] = a - c;
+  for (int k = 0; k < PER; ++k) acc[k] *= inv;
+  // y = s_V * (H y~) / sqrt(D): coordinate index = lane * PER + k
+#pragma unroll
+  for (int hs = 1; hs < PER; hs <<= 1) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      if ((k & hs) == 0) {
+        const float a = acc[k], c = acc[k + hs];
+        acc[k] = a + c;
+        acc[k + hs] = a - c;
+      }
     }
-    __syncthreads();
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, acc[k], m);
+      acc[k] = (lane & m) ? (o - acc[k]) : (acc[k] + o);
+    }
   }
   constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
+  const int8_t* sg = p.v_signs + hk * D + lane * PER;
+  float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)b * p.hq + hq) * D + lane * PER);
 #pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int j = tid + 128 * k;
-    const float v = y_s[j] * inv_sqrt_d;
-    p.out[((size_t)b * p.hq + hq) * D + j] = p.v_signs[hk * D + j] < 0 ? -v : v;
+  for (int k = 0; k < PER / 4; ++k) {
+    float4 v;
+    v.x = (sg[4 * k] < 0 ? -acc[4 * k] : acc[4 * k]) * inv_sqrt_d;
+    v.y = (sg[4 * k + 1] < 0 ? -acc[4 * k + 1] : acc[4 * k + 1]) * inv_sqrt_d;
+    v.z = (sg[4 * k + 2] < 0 ? -acc[4 * k + 2] : acc[4 * k + 2]) * inv_sqrt_d;
+    v.w = (sg[4 * k + 3] < 0 ? -acc[4 * k + 3] : acc[4 * k + 3]) * inv_sqrt_d;
+    dst[k] = v;
   }
 }
 
@@ -415,9 +437,11 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
 }
 
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
-  dim3 grid(p.hq, p.batch);
-  if (head_dim == 128) combine_kernel<128><<<grid, 128, 0, stream>>>(p);
-  else if (head_dim == 256) combine_kernel<256><<<grid, 128, 0, stream>>>(p);
+  const int pairs = p.batch * p.hq;
+  const int blocks = (pairs + 3) / 4;
+  if (blocks == 0) return cudaSuccess;
+  if (head_dim == 128) combine_kernel<128><<<blocks, 128, 0, stream>>>(p);
+  else if (head_dim == 256) combine_kernel<256><<<blocks, 128, 0, stream>>>(p);
   else return cudaErrorNotSupported;
   return cudaGetLastError();
 }
