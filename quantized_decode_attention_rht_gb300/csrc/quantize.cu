@@ -1,249 +1,347 @@
 // Quantise-and-append: fp16 K/V vectors -> rotated, encoded rows in the paged pool.
 //
-// One vector (token, kv head, K|V) is held by LPV = D/32 consecutive lanes, 32 contiguous
-// coordinates per lane.  Steps per vector, as on the pages:
-//   1. multiply by the Rademacher signs, then the Walsh-Hadamard butterflies -- five
-//      in-register stages over a lane's 32 coordinates and log2(LPV) stages across lanes
-//      with shuffles (AdapTQ page, "The Math Fix"; VeloxQuant-MLX page, "Stage 1");
-//   2. codebook format: norm of the rotated vector, fp16 norm, u = sqrt(D) y / ||y||, index
-//      of the centroid cell of every coordinate, little-endian bit packing (VeloxQuant-MLX
-//      page, "Stage 2" and "The Bit-Packing Problem");
-//      fp16 / fp8 E4M3 / INT4-g32 formats: the rotated vector rounded to the format
-//      (FoveatedKV page, "The VR headset thing");
+// Each thread holds 64 coordinates of one vector (D / 64 neighbouring lanes per vector).
+// Steps per vector, as on the pages:
+//   1. multiply by the Rademacher signs (a flip of the fp16 sign bit), then the
+//      Walsh-Hadamard butterflies in registers with packed f32x2 adds, and log2(D / 64)
+//      stages across lanes with shuffles (AdapTQ page, "The Math Fix"; VeloxQuant-MLX page,
+//      "Stage 1");
+//   2. codebook format: norm of the rotated vector, fp16 norm, u = sqrt(D) y / ||y||, the
+//      index of u's centroid cell, little-endian bit packing (VeloxQuant-MLX page, "Stage 2"
+//      and "The Bit-Packing Problem"); fp16 / fp8 E4M3 / INT4-g32 formats: the rotated vector
+//      rounded to the format (FoveatedKV page, "The VR headset thing");
 //   3. store the row at its pool slot.
+// One launch per side (K, V), specialised to that side's format so the kernel holds a single
+// short path; a persistent grid walks the vectors; the decision table is built once per
+// block.
 // The kernel is HBM-bound: 2*D bytes read and one row (+ side data) written per vector.
+#include <algorithm>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kMaxCells = 256;
+constexpr int kCoords = 64;  // coordinates of one vector held by one thread
+constexpr int kMaxCells = 512;
+typedef unsigned long long u64;
 
-// Decision grid for the codebook index #{i : u > bounds[i]}: cells of width w (a power of
-// two no larger than the smallest gap between boundaries) hold at most one boundary, so
-// idx = count[cell] + (u > beta[cell]).  floor(u / w) is exact for a power-of-two w.
-struct Grid {
-  int cell_lo, ncells, nb;
+// ---------------------------------------------------------------- packed fp32 helpers
+__device__ __forceinline__ u64 pk(float a, float b) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(u64 r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+  u64 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ u64 sub2(u64 a, u64 b) {
+  u64 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+  u64 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+  u64 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------- decision table
+// The code index #{i : u > bounds[i]} through cells of width w (a power of two no larger
+// than the smallest gap between boundaries, so a cell holds at most one boundary).  With
+// t = u / w, the cell is k = rint(t) (cell k covers t in [k - 1/2, k + 1/2)) and
+//   index = count[k] + (t > beta[k]),
+// count[k] = boundaries below the cell, beta[k] = the boundary inside it (in units of w) or
+// +inf.  When t sits exactly between two cells rint may pick either, and both give the same
+// index.  |u| <= sqrt(D), so the table spans every reachable cell and needs no clamping.
+struct Table {
   float inv_w;
-  bool linear;  // fall back to counting when the grid would be too large
-  float bounds[255];
-  int count[kMaxCells];
-  float beta[kMaxCells];
+  int k0, ncells, nb;  // k0 = lowest cell
+  int linear;
+  float bounds[16];
+  float2 cell[kMaxCells];  // {count (int bits), beta}
 };
 
-__device__ void build_grid(Grid& g, const float* bounds, int nb) {
-  // single thread; nb <= 15 in practice
-  g.nb = nb;
-  for (int i = 0; i < nb; ++i) g.bounds[i] = bounds[i];
+__device__ void build_table(Table& t, const float* bounds, int nb, int head_dim) {
+  // every thread of the block calls this
+  if (threadIdx.x < 16) t.bounds[threadIdx.x] = threadIdx.x < nb ? bounds[threadIdx.x] : INFINITY;
+  __syncthreads();
   float gap = INFINITY;
-  for (int i = 0; i + 1 < nb; ++i) gap = fminf(gap, g.bounds[i + 1] - g.bounds[i]);
-  g.linear = true;
-  if (nb < 1) return;
+  for (int i = 0; i + 1 < nb; ++i) gap = fminf(gap, t.bounds[i + 1] - t.bounds[i]);
+  bool ok = nb >= 1 && nb <= 15 && (nb == 1 || (gap > 0.0f && gap >= 1e-3f));
   float w = 1.0f;
-  if (nb > 1) {
-    if (!(gap > 0.0f) || gap < 1e-3f) return;
+  if (ok && nb > 1) {
     int e;
-    frexpf(gap, &e);          // gap = m * 2^e, m in [0.5, 1)
+    frexpf(gap, &e);
     w = ldexpf(1.0f, e - 1);  // largest power of two <= gap
   }
-  const float inv_w = 1.0f / w;  // exact: power of two
-  const int lo = (int)floorf(g.bounds[0] * inv_w);
-  const int hi = (int)floorf(g.bounds[nb - 1] * inv_w);
-  if (hi - lo + 1 > kMaxCells) return;
-  g.cell_lo = lo;
-  g.ncells = hi - lo + 1;
-  g.inv_w = inv_w;
-  for (int c = 0; c < g.ncells; ++c) {
-    const float a = (float)(lo + c) * w, b = (float)(lo + c + 1) * w;
+  const float inv_w = 1.0f / w;  // exact
+  const int kmax = (int)ceilf(sqrtf((float)head_dim) * inv_w) + 1;
+  const int ncells = 2 * kmax + 1;
+  ok = ok && ncells <= kMaxCells;
+  for (int c = threadIdx.x; ok && c < ncells; c += blockDim.x) {
+    const float k = (float)(c - kmax);
+    const float lo = (k - 0.5f) * w, hi = (k + 0.5f) * w;  // exact: w a power of two
     int cnt = 0;
     float beta = INFINITY;
     for (int i = 0; i < nb; ++i) {
-      if (g.bounds[i] < a) ++cnt;
-      else if (g.bounds[i] < b) beta = g.bounds[i];
+      if (t.bounds[i] < lo) ++cnt;
+      else if (t.bounds[i] < hi) beta = t.bounds[i] * inv_w;
     }
-    g.count[c] = cnt;
-    g.beta[c] = beta;
+    t.cell[c] = make_float2(__int_as_float(cnt), beta);
   }
-  g.linear = false;
-}
-
-__device__ __forceinline__ uint32_t code_index(const Grid& g, float u) {
-  if (g.linear) {
-    uint32_t idx = 0;
-    for (int i = 0; i < g.nb; ++i) idx += (u > g.bounds[i]) ? 1u : 0u;
-    return idx;
-  }
-  const int c = (int)floorf(u * g.inv_w) - g.cell_lo;
-  if (c < 0) return 0;
-  if (c >= g.ncells) return (uint32_t)g.nb;
-  return (uint32_t)g.count[c] + ((u > g.beta[c]) ? 1u : 0u);
-}
-
-// Pack 32 codes of B bits into B little-endian words.
-template <int B>
-__device__ __forceinline__ void pack32(const uint32_t (&idx)[32], uint32_t (&w)[B]) {
-#pragma unroll
-  for (int k = 0; k < B; ++k) w[k] = 0;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    const int o = e * B;
-    w[o / 32] |= idx[e] << (o % 32);
-    if ((o % 32) + B > 32) w[o / 32 + 1] |= idx[e] >> (32 - (o % 32));
-  }
-}
-
-template <int LPV>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p) {
-  constexpr int D = 32 * LPV;
-  __shared__ Grid grids[2];
-  if (threadIdx.x < 2) {
-    const int kind = threadIdx.x;
-    const QuantSide& s = p.side[kind];
-    grids[kind].linear = true;
-    grids[kind].nb = 0;
-    if (s.fmt == KVQ_FMT_CODEBOOK && s.bounds) build_grid(grids[kind], s.bounds, (1 << s.bits) - 1);
+  if (threadIdx.x == 0) {
+    t.inv_w = ok ? inv_w : 1.0f;  // the fallback compares u against the bounds directly
+    t.k0 = -kmax;
+    t.ncells = ncells;
+    t.nb = nb;
+    t.linear = ok ? 0 : 1;
   }
   __syncthreads();
+}
 
-  const int lane = threadIdx.x & 31;
-  const int r = lane % LPV;                                   // lane within the vector
-  const unsigned gmask = ((LPV == 32) ? 0xFFFFFFFFu : ((1u << LPV) - 1u)) << (lane - r);
-  const long long v = (long long)blockIdx.x * (kThreads / LPV) + threadIdx.x / LPV;
-  const bool in_range = v < p.num_vectors;
-  const long long per_kind = (long long)p.num_tokens * p.hkv;
-  const int kind = p.kind_first + (in_range ? (int)(v / per_kind) : 0);
-  const long long rem = in_range ? v % per_kind : 0;
-  const int token = (int)(rem / p.hkv);
-  const int h = (int)(rem % p.hkv);
-  const QuantSide& side = p.side[kind];
-  const int slot = in_range ? p.slots[token] : -1;
-  const bool store = in_range && slot >= 0 && slot < p.num_slots;
+// 12582912 = 1.5 * 2^23: adding it rounds t (|t| < 2^22) to the integer held in the low
+// mantissa bits, 0x4B400000 + rint(t).
+constexpr float kMagic = 12582912.0f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
 
-  // ---- load 32 fp16 coordinates and the signs; y = s * x
-  float y[32];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(p.x[kind] + ((size_t)token * p.hkv + h) * D + r * 32);
-    const uint4* sg = reinterpret_cast<const uint4*>(side.signs + (size_t)h * D + r * 32);
-    uint4 xs[4], ss[2];
+// Code indices of coordinates t = y[e] * scale (scale = sqrt(D) / ||y|| / w), packed
+// little-endian and stored (E * BITS / 8 bytes at row).
+template <int BITS, int E>
+__device__ __forceinline__ void encode_codebook(const Table& tb, const float (&y)[E], float scale, uint8_t* row,
+                                                bool store) {
+  constexpr int W = E * BITS / 32;
+  uint32_t w[W];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) xs[i] = in_range ? src[i] : make_uint4(0, 0, 0, 0);
+  for (int k = 0; k < W; ++k) w[k] = 0;
+  const u64 sc2 = pk(scale, scale), mg2 = pk(kMagic, kMagic);
+  // cell address = base + 8 * (bits - kMagicBits - k0), in 32-bit shared-space arithmetic
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(tb.cell)) -
+                        8u * (kMagicBits + static_cast<uint32_t>(tb.k0));
+  const bool lin = tb.linear;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) ss[i] = in_range ? sg[i] : make_uint4(0, 0, 0, 0);
-    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
-    const int8_t* sb = reinterpret_cast<const int8_t*>(ss);
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const uint16_t bits = (uint16_t)(xw[e / 2] >> (16 * (e % 2)));
-      const float f = __half2float(__ushort_as_half(bits));
-      y[e] = sb[e] < 0 ? -f : f;
-    }
-  }
-  // ---- Walsh-Hadamard butterflies: in-register stages, then across lanes
-#pragma unroll
-  for (int hs = 1; hs < 32; hs <<= 1) {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      if ((e & hs) == 0) {
-        const float a = y[e], b = y[e + hs];
-        y[e] = a + b;
-        y[e + hs] = a - b;
+  for (int e = 0; e < E; e += 2) {
+    float t0, t1, f0, f1;
+    upk(mul2(pk(y[e], y[e + 1]), sc2), t0, t1);
+    upk(add2(pk(t0, t1), mg2), f0, f1);
+    uint32_t i0, i1;
+    if (!lin) {
+      float2 c0, c1;
+      asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(c0.x), "=f"(c0.y) : "r"(base + 8u * __float_as_uint(f0)));
+      asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(c1.x), "=f"(c1.y) : "r"(base + 8u * __float_as_uint(f1)));
+      i0 = __float_as_uint(c0.x) + (t0 > c0.y ? 1u : 0u);
+      i1 = __float_as_uint(c1.x) + (t1 > c1.y ? 1u : 0u);
+    } else {  // no table: count the boundaries (in units of w = 1)
+      i0 = i1 = 0;
+      for (int i = 0; i < tb.nb; ++i) {
+        i0 += t0 > tb.bounds[i] ? 1u : 0u;
+        i1 += t1 > tb.bounds[i] ? 1u : 0u;
       }
     }
+    const int o0 = e * BITS, o1 = (e + 1) * BITS;
+    w[o0 / 32] += i0 * (1u << (o0 % 32));  // fields are disjoint: add = or
+    if ((o0 % 32) + BITS > 32) w[o0 / 32 + 1] += i0 >> (32 - (o0 % 32));
+    w[o1 / 32] += i1 * (1u << (o1 % 32));
+    if ((o1 % 32) + BITS > 32) w[o1 / 32 + 1] += i1 >> (32 - (o1 % 32));
   }
+  if (store) {
+    if (W % 4 == 0) {
 #pragma unroll
-  for (int m = 1; m < LPV; m <<= 1) {
+      for (int k = 0; k < W / 4; ++k)
+        reinterpret_cast<uint4*>(row)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    } else {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float o = __shfl_xor_sync(gmask, y[e], m, LPV);
-      y[e] = (r & m) ? (o - y[e]) : (y[e] + o);
+      for (int k = 0; k < W / 2; ++k) reinterpret_cast<uint2*>(row)[k] = make_uint2(w[2 * k], w[2 * k + 1]);
     }
   }
-  // y = H s x (unnormalised); the rotated vector is x~ = y / sqrt(D)
+}
+
+enum { F_CB = 0, F_F16 = 1, F_F8 = 2, F_I4 = 3 };
+
+// One side (K or V) of a quantise-and-append call.  TPV threads per vector, kE coordinates
+// each; FMT / BITS fix the storage format so the kernel holds one path only.
+template <int TPV, int kE, int FMT, int BITS>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p, int kind) {
+  constexpr int D = kE * TPV;
+  const QuantSide& side = p.side[kind];
+  __shared__ Table table;
+  if constexpr (FMT == F_CB) build_table(table, side.bounds, (1 << BITS) - 1, D);
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPV;  // which kE-coordinate part
+  const unsigned gmask = (TPV == 32 ? 0xFFFFFFFFu : ((1u << TPV) - 1u)) << (lane - sub);
+  const int nvec = p.num_tokens * p.hkv;
+  const int stride = gridDim.x * (kThreads / TPV);
+  const uint16_t* x = p.x[kind];
   constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
   constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
 
-  uint8_t* row = side.rows + ((size_t)(slot / p.page_size) * p.hkv + h) * (size_t)p.page_size * side.row_bytes +
-                 (size_t)(slot % p.page_size) * side.row_bytes;
-  const size_t aux_row = ((size_t)(slot / p.page_size) * p.hkv + h) * p.page_size + (slot % p.page_size);
+  for (int v = blockIdx.x * (kThreads / TPV) + threadIdx.x / TPV; v < nvec; v += stride) {
+    const int token = v / p.hkv, h = v - token * p.hkv;
+    const int slot = p.slots[token];
+    const bool store = slot >= 0 && slot < p.num_slots;
 
-  if (side.fmt == KVQ_FMT_CODEBOOK) {
-    float ss = 0.0f;
+    // ---- load kE fp16 coordinates and their signs; y = s * x
+    float y[kE];
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(x + ((size_t)token * p.hkv + h) * D + sub * kE);
+      const uint4* sg = reinterpret_cast<const uint4*>(side.signs + (size_t)h * D + sub * kE);
+      uint4 xs[kE / 8], ss[kE / 16];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) ss = fmaf(y[e], y[e], ss);
+      for (int i = 0; i < kE / 8; ++i) xs[i] = __ldg(src + i);
 #pragma unroll
-    for (int m = 1; m < LPV; m <<= 1) ss += __shfl_xor_sync(gmask, ss, m, LPV);
-    const float ny = sqrtf(ss);
-    const float inv = ny > 0.0f ? sqrt_d / ny : 0.0f;  // u = sqrt(D) y / ||y||
-    const Grid& g = grids[kind];
-    uint32_t idx[32];
+      for (int i = 0; i < kE / 16; ++i) ss[i] = __ldg(sg + i);
+      const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(ss);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) idx[e] = code_index(g, y[e] * inv);
-    if (store) {
-      if (r == 0) side.aux[aux_row] = __float2half_rn(ny * inv_sqrt_d);
-      if (side.bits == 4) {
-        uint32_t w[4];
-        pack32<4>(idx, w);
-        reinterpret_cast<uint4*>(row)[r] = make_uint4(w[0], w[1], w[2], w[3]);
-      } else if (side.bits == 3) {
-        uint32_t w[3];
-        pack32<3>(idx, w);
-        uint32_t* dst = reinterpret_cast<uint32_t*>(row) + 3 * r;
-        dst[0] = w[0]; dst[1] = w[1]; dst[2] = w[2];
-      } else {
-        uint32_t w[2];
-        pack32<2>(idx, w);
-        reinterpret_cast<uint2*>(row)[r] = make_uint2(w[0], w[1]);
+      for (int k = 0; k < kE / 2; ++k) {
+        // sign bytes 2k, 2k+1 (int8 +-1: bit 7 set for -1) -> fp16 sign bits 15, 31
+        const uint32_t m = __byte_perm(sw[k >> 1], 0, (k & 1) ? 0x3424 : 0x1404) & 0x80008000u;
+        const uint32_t xv = xw[k] ^ m;
+        const __half2 h2 = *reinterpret_cast<const __half2*>(&xv);
+        y[2 * k] = __low2float(h2);
+        y[2 * k + 1] = __high2float(h2);
       }
     }
-  } else if (side.fmt == KVQ_FMT_FP16) {
-    if (store) {
-      uint32_t w[16];
+    // ---- Walsh-Hadamard: stage 1 in scalar, stages 2.. on f32x2 pairs, then across lanes
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t lo = __half_as_ushort(__float2half_rn(y[2 * k] * inv_sqrt_d));
-        const uint32_t hi = __half_as_ushort(__float2half_rn(y[2 * k + 1] * inv_sqrt_d));
-        w[k] = lo | (hi << 16);
+    for (int e = 0; e < kE; e += 2) {
+      const float a = y[e], c = y[e + 1];
+      y[e] = a + c;
+      y[e + 1] = a - c;
+    }
+#pragma unroll
+    for (int hs = 2; hs < kE; hs <<= 1) {
+#pragma unroll
+      for (int e = 0; e < kE; e += 2) {
+        if ((e & hs) == 0) {
+          const u64 a = pk(y[e], y[e + 1]), c = pk(y[e + hs], y[e + hs + 1]);
+          upk(add2(a, c), y[e], y[e + 1]);
+          upk(sub2(a, c), y[e + hs], y[e + hs + 1]);
+        }
       }
-      uint4* dst = reinterpret_cast<uint4*>(row) + 4 * r;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
-  } else if (side.fmt == KVQ_FMT_FP8_E4M3) {
-    if (store) {
-      uint32_t w[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t a = float2_to_fp8x2(y[4 * k] * inv_sqrt_d, y[4 * k + 1] * inv_sqrt_d);
-        const uint32_t b = float2_to_fp8x2(y[4 * k + 2] * inv_sqrt_d, y[4 * k + 3] * inv_sqrt_d);
-        w[k] = a | (b << 16);
+    for (int m = 1; m < TPV; m <<= 1) {
+      const float sgn = (sub & m) ? -1.0f : 1.0f;  // upper lane keeps partner - own
+#pragma unroll
+      for (int e = 0; e < kE; ++e) y[e] = fmaf(sgn, y[e], __shfl_xor_sync(gmask, y[e], m, TPV));
+    }
+    // y = H s x (unnormalised); the rotated vector is x~ = y / sqrt(D)
+    const int slot_c = store ? slot : 0;
+    const size_t prow = ((size_t)(slot_c / p.page_size) * p.hkv + h) * p.page_size + (slot_c % p.page_size);
+    uint8_t* row = side.rows + prow * side.row_bytes;
+
+    if constexpr (FMT == F_CB) {
+      u64 acc = pk(0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < kE; e += 2) {
+        const u64 v2 = pk(y[e], y[e + 1]);
+        acc = fma2(v2, v2, acc);
       }
-      uint4* dst = reinterpret_cast<uint4*>(row) + 2 * r;
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-    }
-  } else {  // KVQ_FMT_INT4_G32: the lane's 32 coordinates are one group
-    float x[32];
-    float amax = 0.0f;
+      float a0, a1;
+      upk(acc, a0, a1);
+      float ss = a0 + a1;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      x[e] = y[e] * inv_sqrt_d;
-      amax = fmaxf(amax, fabsf(x[e]));
-    }
-    const __half s16 = __float2half_rn(amax / 7.0f);
-    const float s = __half2float(s16);
-    uint32_t idx[32];
+      for (int m = 1; m < TPV; m <<= 1) ss += __shfl_xor_sync(gmask, ss, m, TPV);
+      const float ny = sqrtf(ss);
+      const float inv = ny > 0.0f ? sqrt_d / ny : 0.0f;  // u = sqrt(D) y / ||y||
+      encode_codebook<BITS, kE>(table, y, inv * table.inv_w, row + sub * (kE * BITS / 8), store);
+      if (store && sub == 0) side.aux[prow] = __float2half_rn(ny * inv_sqrt_d);
+    } else if constexpr (FMT == F_F16) {
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(row) + sub * (kE / 8);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float q = s > 0.0f ? fminf(fmaxf(rintf(x[e] / s), -7.0f), 7.0f) : 0.0f;
-      idx[e] = (uint32_t)((int)q + 8);
+        for (int k = 0; k < kE / 8; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __half2 h2 = __floats2half2_rn(y[8 * k + 2 * j] * inv_sqrt_d, y[8 * k + 2 * j + 1] * inv_sqrt_d);
+            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    } else if constexpr (FMT == F_F8) {
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(row) + sub * (kE / 16);
+#pragma unroll
+        for (int k = 0; k < kE / 16; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = 16 * k + 4 * j;
+            const uint32_t a = float2_to_fp8x2(y[e] * inv_sqrt_d, y[e + 1] * inv_sqrt_d);
+            const uint32_t b = float2_to_fp8x2(y[e + 2] * inv_sqrt_d, y[e + 3] * inv_sqrt_d);
+            w[j] = a | (b << 16);
+          }
+          dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    } else {  // F_I4: kE / 32 groups of 32 coordinates per thread
+      constexpr int NG = kE / kGroup;
+      uint32_t w[NG * 4];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(y[kGroup * g + e] * inv_sqrt_d));
+        const __half s16 = __float2half_rn(amax / 7.0f);
+        const float s = __half2float(s16);
+        const float r = s > 0.0f ? 1.0f / s : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[4 * g + k] = 0;
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) {
+          const float xv = y[kGroup * g + e] * inv_sqrt_d;
+          // level = rint(x / s): x * (1/s) is within one ulp of the quotient; where that
+          // leaves the result next to a half-integer, divide exactly
+          float tq = xv * r;
+          if (s > 0.0f && fabsf(fabsf(tq - rintf(tq)) - 0.5f) < 1e-5f) tq = xv / s;
+          const float q = s > 0.0f ? fminf(fmaxf(rintf(tq), -7.0f), 7.0f) : 0.0f;
+          w[4 * g + e / 8] |= (uint32_t)((int)q + 8) << (4 * (e % 8));
+        }
+        if (store) side.aux[prow * (D / kGroup) + sub * NG + g] = s16;
+      }
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(row) + sub * NG;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+      }
     }
-    if (store) {
-      uint32_t w[4];
-      pack32<4>(idx, w);
-      reinterpret_cast<uint4*>(row)[r] = make_uint4(w[0], w[1], w[2], w[3]);
-      side.aux[aux_row * (D / kGroup) + r] = s16;
-    }
+  }
+}
+
+template <int TPV, int FMT, int BITS>
+cudaError_t launch_side(const QuantParams& p, int kind, int sms, cudaStream_t stream) {
+  const long long nvec = (long long)p.num_tokens * p.hkv;
+  const long long vpb = kThreads / TPV;
+  const unsigned blocks = (unsigned)std::min<long long>((nvec + vpb - 1) / vpb, (long long)sms * 2);
+  quantize_kernel<TPV, kCoords, FMT, BITS><<<blocks, kThreads, 0, stream>>>(p, kind);
+  return cudaGetLastError();
+}
+
+template <int TPV>
+cudaError_t launch_tpv(const QuantParams& p, int kind, int sms, cudaStream_t stream) {
+  const QuantSide& s = p.side[kind];
+  switch (s.fmt) {
+    case KVQ_FMT_CODEBOOK:
+      if (s.bits == 4) return launch_side<TPV, F_CB, 4>(p, kind, sms, stream);
+      if (s.bits == 3) return launch_side<TPV, F_CB, 3>(p, kind, sms, stream);
+      return launch_side<TPV, F_CB, 2>(p, kind, sms, stream);
+    case KVQ_FMT_FP16: return launch_side<TPV, F_F16, 0>(p, kind, sms, stream);
+    case KVQ_FMT_FP8_E4M3: return launch_side<TPV, F_F8, 0>(p, kind, sms, stream);
+    default: return launch_side<TPV, F_I4, 0>(p, kind, sms, stream);
   }
 }
 
@@ -251,14 +349,18 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p)
 
 cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t stream) {
   if (p.num_vectors == 0) return cudaSuccess;
-  const int lpv = head_dim / 32;
-  const long long vpb = kThreads / lpv;
-  const long long blocks = (p.num_vectors + vpb - 1) / vpb;
-  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  if (lpv == 4) quantize_kernel<4><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-  else if (lpv == 8) quantize_kernel<8><<<(unsigned)blocks, kThreads, 0, stream>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if ((long long)p.num_tokens * p.hkv > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  for (int kind = p.kind_first; kind < p.kind_first + p.num_kinds; ++kind) {
+    // kCoords coordinates per thread: 2 lanes per vector for head_dim 128, 4 for 256
+    e = head_dim == 128 ? launch_tpv<2>(p, kind, sms, stream)
+                        : (head_dim == 256 ? launch_tpv<4>(p, kind, sms, stream) : cudaErrorInvalidValue);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace kvq
