@@ -160,8 +160,9 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
                                              int32_t batch, int32_t num_q_heads,
                                              int32_t split_tokens, size_t* bytes);
 
-/* Decode attention for one new query per sequence over all tiers (two launches: a fused
- * split-K pass over every tier, then a combine pass):
+/* Decode attention for one new query per sequence over all tiers (a split-K pass -- one
+ * launch for every tier on the fp16 and fp8 + INT4 path, one launch per tier on the
+ * codebook path -- then a combine pass):
  *   out[b][h] = softmax_t( q[b][h] . K[t] / sqrt(D) ) V[t]
  * over every cached token t < seq_lens[b] of every tier of kv head h / (Hq / Hkv), where
  * K[t], V[t] are the dequantised cache rows with the rotation undone.  The query is

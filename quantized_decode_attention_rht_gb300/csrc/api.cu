@@ -57,11 +57,13 @@ int side_row_bytes(int fmt, int bits, int d) {
 }
 
 // Split-K plan: tokens per chunk for each tier (a multiple of page_size).
+enum PlanKind { PLAN_GENERIC = 0, PLAN_GQA, PLAN_CB };
+
 struct Plan {
   int chunk[KVQ_MAX_TIERS];
   int splits[KVQ_MAX_TIERS];
   int total;
-  bool fast;  // every tier qualifies for the fused tensor-core kernel
+  PlanKind kind;  // GQA: the fused fp16 / fp8+INT4 kernel; CB: the fused codebook kernel
 };
 
 size_t token_bytes(const kvq_cache* c) {
@@ -75,23 +77,29 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
   const kvq_cache* c0 = tiers[0].cache;
   const int ps = c0->page_size, hkv = c0->num_kv_heads, group = hq / hkv;
   if (split_tokens < 0 || split_tokens % ps) return KVQ_ERR_INVALID_ARGUMENT;
-  plan->fast = ps == 16;
-  for (int i = 0; i < n; ++i)
-    plan->fast = plan->fast && gqa_fast_supported(c0->head_dim, group, tiers[i].cache->k_format,
-                                                  tiers[i].cache->v_format);
-  if (split_tokens > gqa_max_chunk_tokens()) plan->fast = false;
-  // fused kernel: items of about equal bytes, ~4 per warp of a full GPU
+  bool gqa = ps == 16 && split_tokens <= gqa_max_chunk_tokens(), cb = ps == 16;
+  for (int i = 0; i < n; ++i) {
+    const kvq_cache* c = tiers[i].cache;
+    gqa = gqa && gqa_fast_supported(c0->head_dim, group, c->k_format, c->v_format);
+    cb = cb && cb_fast_supported(c0->head_dim, group, c->k_format, c->v_format);
+    // bulk copies of the norm runs need 16-byte aligned sources
+    cb = cb && aligned(c->k_aux, 16) && aligned(c->v_aux, 16);
+  }
+  plan->kind = gqa ? PLAN_GQA : (cb ? PLAN_CB : PLAN_GENERIC);
+  // fused kernels: items of about equal bytes, several per warp of a full GPU
   size_t total_bytes = 0;
   for (int i = 0; i < n; ++i)
     total_bytes += (size_t)batch * hkv * tiers[i].max_pages * ps * token_bytes(tiers[i].cache);
-  const size_t item_bytes = std::max<size_t>(64 << 10, total_bytes / (kSms * 8 * 4));
+  const size_t item_bytes = plan->kind == PLAN_GQA ? std::max<size_t>(64 << 10, total_bytes / (kSms * 8 * 4))
+                                                   : std::max<size_t>(16 << 10, total_bytes / (kSms * 12 * 6));
   plan->total = 0;
   for (int i = 0; i < n; ++i) {
     const long long max_len = (long long)tiers[i].max_pages * ps;
     int chunk = split_tokens;
-    if (chunk == 0 && plan->fast) {
+    if (chunk == 0 && plan->kind != PLAN_GENERIC) {
       const size_t tok = item_bytes / token_bytes(tiers[i].cache);
-      chunk = (int)std::min<size_t>(gqa_max_chunk_tokens(), std::max<size_t>(ps, tok / ps * ps));
+      const size_t cap = plan->kind == PLAN_GQA ? (size_t)gqa_max_chunk_tokens() : (size_t)1 << 20;
+      chunk = (int)std::min<size_t>(cap, std::max<size_t>(ps, tok / ps * ps));
     } else if (chunk == 0) {
       // aim at ~16 CTAs per SM in total, chunks of 256 .. 4096 tokens
       const long long work = (long long)batch * hkv * max_len;
@@ -278,8 +286,10 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
   p.total_splits = plan.total;
   int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + need - 256);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool fast = plan.fast && aligned(q, 16);
-  cudaError_t e = fast ? launch_decode_gqa(p, counter, s) : launch_decode(p, d, num_q_heads / hkv, s);
+  cudaError_t e;
+  if (plan.kind == PLAN_GQA && aligned(q, 16)) e = launch_decode_gqa(p, counter, s);
+  else if (plan.kind == PLAN_CB) e = launch_decode_cb(p, d, counter, s);
+  else e = launch_decode(p, d, num_q_heads / hkv, s);
   if (e == cudaSuccess) e = launch_combine(p, d, s);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -388,14 +388,18 @@ cudaError_t launch_tier_fmt(const DecParams& p, int ti, cudaStream_t stream) {
   const DecTier& T = p.tier[ti];
   const int kf = T.k_fmt, vf = T.v_fmt;
   if (kf == KVQ_FMT_CODEBOOK && vf == KVQ_FMT_CODEBOOK) {
-    const int kb = T.k_bits, vb = T.v_bits;
-    if (kb == 4 && vb == 4) return launch_tier<D, G, Codebook<4>, Codebook<4>>(p, ti, stream);
-    if (kb == 4 && vb == 3) return launch_tier<D, G, Codebook<4>, Codebook<3>>(p, ti, stream);
-    if (kb == 4 && vb == 2) return launch_tier<D, G, Codebook<4>, Codebook<2>>(p, ti, stream);
-    if (kb == 3 && vb == 3) return launch_tier<D, G, Codebook<3>, Codebook<3>>(p, ti, stream);
-    if (kb == 3 && vb == 2) return launch_tier<D, G, Codebook<3>, Codebook<2>>(p, ti, stream);
-    if (kb == 2 && vb == 2) return launch_tier<D, G, Codebook<2>, Codebook<2>>(p, ti, stream);
-    return cudaErrorNotSupported;
+    switch (T.k_bits * 8 + T.v_bits) {
+      case 4 * 8 + 4: return launch_tier<D, G, Codebook<4>, Codebook<4>>(p, ti, stream);
+      case 4 * 8 + 3: return launch_tier<D, G, Codebook<4>, Codebook<3>>(p, ti, stream);
+      case 4 * 8 + 2: return launch_tier<D, G, Codebook<4>, Codebook<2>>(p, ti, stream);
+      case 3 * 8 + 4: return launch_tier<D, G, Codebook<3>, Codebook<4>>(p, ti, stream);
+      case 3 * 8 + 3: return launch_tier<D, G, Codebook<3>, Codebook<3>>(p, ti, stream);
+      case 3 * 8 + 2: return launch_tier<D, G, Codebook<3>, Codebook<2>>(p, ti, stream);
+      case 2 * 8 + 4: return launch_tier<D, G, Codebook<2>, Codebook<4>>(p, ti, stream);
+      case 2 * 8 + 3: return launch_tier<D, G, Codebook<2>, Codebook<3>>(p, ti, stream);
+      case 2 * 8 + 2: return launch_tier<D, G, Codebook<2>, Codebook<2>>(p, ti, stream);
+      default: return cudaErrorNotSupported;
+    }
   }
   if (kf == KVQ_FMT_FP16 && vf == KVQ_FMT_FP16) return launch_tier<D, G, Fp16, Fp16>(p, ti, stream);
   if (kf == KVQ_FMT_FP8_E4M3 && vf == KVQ_FMT_INT4_G32) return launch_tier<D, G, Fp8, Int4>(p, ti, stream);
@@ -423,8 +427,7 @@ cudaError_t launch_decode_d(const DecParams& p, int group, cudaStream_t stream) 
 
 bool decode_supports(int k_fmt, int k_bits, int v_fmt, int v_bits) {
   if (k_fmt == KVQ_FMT_CODEBOOK && v_fmt == KVQ_FMT_CODEBOOK)
-    return (k_bits == 4 && v_bits >= 2 && v_bits <= 4) || (k_bits == 3 && (v_bits == 3 || v_bits == 2)) ||
-           (k_bits == 2 && v_bits == 2);
+    return k_bits >= 2 && k_bits <= 4 && v_bits >= 2 && v_bits <= 4;
   if (k_fmt == KVQ_FMT_FP16 && v_fmt == KVQ_FMT_FP16) return true;
   if (k_fmt == KVQ_FMT_FP8_E4M3 && (v_fmt == KVQ_FMT_INT4_G32 || v_fmt == KVQ_FMT_FP16)) return true;
   return false;

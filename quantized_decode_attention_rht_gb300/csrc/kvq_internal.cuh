@@ -64,6 +64,12 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
 bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
 int gqa_max_chunk_tokens();
 cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t stream);
+// Fused tensor-core decode over codebook tiers (codebook K and V), head_dim 128 or 256,
+// 1, 2 or 4 query heads per kv head; one launch per tier.  `counters` is 64 ints (256 bytes)
+// of device scratch, cleared by the launcher: one work counter per tier, and at index 32 an
+// error word that a kernel sets when a wait for its own bulk copies gives up.
+bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
+cudaError_t launch_decode_cb(const DecParams& p, int head_dim, int* counters, cudaStream_t stream);
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream);
 
 // ------------------------------------------------------------------------ device helpers

@@ -69,6 +69,26 @@ def test_decode_edge_lengths_and_groups(group):
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
 
 
+CODE_WIDTHS = [(128, 1, 3, 3), (128, 4, 3, 3), (128, 2, 2, 4), (128, 1, 4, 2), (128, 4, 2, 3),
+               (256, 1, 3, 3), (256, 4, 4, 4), (256, 2, 2, 3), (256, 4, 3, 2), (256, 1, 2, 2)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d,group,kb,vb", CODE_WIDTHS)
+def test_decode_code_widths(d, group, kb, vb):
+    """Every head_dim, code width (the runs of packed bits a lane reads differ for each) and
+    group size of the codebook path, Lloyd-Max and uniform tables, ragged lengths."""
+    hkv = 2
+    codebook = "uniform" if (kb + vb) % 2 else "lloyd_max"
+    cfg = W.CONFIGS["llama7b"].scaled(batch=4, num_q_heads=hkv * group, num_kv_heads=hkv, head_dim=d,
+                                      tiers=(W.Tier("codebook", "codebook", k_bits=kb, v_bits=vb,
+                                                    codebook=codebook),))
+    lens = [1, 47, 300, 129]
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=96, shuffle=5)
+    assert np.all(np.isfinite(got))
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
 @pytest.mark.gpu
 def test_decode_two_tier_edge_lengths():
     cfg = W.CONFIGS["gqa32k"].scaled(batch=5, num_q_heads=8, num_kv_heads=2)
