@@ -161,22 +161,6 @@ def step_bytes(cfg, wl, kvq):
     return dec, quant
 
 
-def count_kernel_launches(torch, fn):
-    """Kernels (not memsets or copies) that one call of `fn` launches, read from the CUDA
-    activity trace of torch's profiler; None when the trace is unavailable."""
-    try:
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            fn()
-            torch.cuda.synchronize()
-        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
-    except Exception:  # noqa: BLE001 - a missing activity trace only loses the count
-        return None
-    ours = [n for n in names if not n.lower().startswith(("memset", "memcpy"))]
-    return {"per_step": len(ours), "kernels": sorted(set(n.split("(")[0].split("<")[0].split(" ")[-1]
-                                                         for n in ours))}
-
-
 def quantize_throughput(kvq, torch, reps=5):
     """Quantise-and-append of the append workload's prefill chunk: 4 sequences x 16384 tokens x
     16 kv heads x (K, V), head_dim 256, 4-bit Lloyd-Max, per-channel std log-uniform in
@@ -392,6 +376,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = kvq.kvq_kernel_launches()
     t0.record(stream)
     for i in range(args.steps):
         kvq.kvq_quantize_append(cache_last.struct, k_d, v_d, slots_d, stream)
@@ -399,6 +384,7 @@ def run_ours(args):
         kvq.kvq_decode_attention(views, q_d, out_d, ws_d, 0, stream)
         ev[i][1].record(stream)
     t1.record(stream)
+    launches = kvq.kvq_kernel_launches() - launches0
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop() if clocks else None
@@ -431,7 +417,6 @@ def run_ours(args):
     h2d = k_new.nbytes + v_new.nbytes + q_host.nbytes
     d2h = out_d.numel() * 4
 
-    launches = count_kernel_launches(torch, step)
     quant = quantize_throughput(kvq, torch) if rank == 0 else None
     barrier(ws)
     if rank != 0:
@@ -456,8 +441,7 @@ def run_ours(args):
                      "kernel": "decode call (split-K pass over every tier + combine), CUDA events per call"},
         "e2e": {"value": ws * (dec_bytes + quant_bytes) / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
-        "gpu_launches": None if launches is None else launches["per_step"] * args.steps,
-        "gpu_kernels": None if launches is None else launches["kernels"],
+        "gpu_launches": launches,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:

@@ -123,6 +123,12 @@ typedef struct kvq_tier_view {
 /* Human-readable name of a status.  Never NULL. */
 KVQ_API const char* kvq_status_string(kvq_status status);
 
+/* Number of GPU kernels this library has launched since it was loaded, over every device
+ * and stream (host-side count, incremented at each successful launch; memsets are not
+ * kernels and are not counted).  No counterpart in the pages: it lets a caller state how
+ * many kernels a timed region ran.  Thread-safe; never fails. */
+KVQ_API uint64_t kvq_kernel_launches(void);
+
 /* Bytes of one stored row and of its side data (host outputs) for a format, code bits
  * and head_dim.  Layouts are those of kvq_format above. */
 KVQ_API kvq_status kvq_row_bytes(int32_t format, int32_t bits, int32_t head_dim,

@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         h = ctypes.CDLL(LIB_PATH)
         h.kvq_status_string.restype = ctypes.c_char_p
         h.kvq_status_string.argtypes = [ctypes.c_int]
+        h.kvq_kernel_launches.restype = ctypes.c_uint64
+        h.kvq_kernel_launches.argtypes = []
         i32, vp, sz = ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
         dp, fp = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_float)
         szp = ctypes.POINTER(ctypes.c_size_t)
@@ -113,6 +115,11 @@ def _stream(stream) -> Optional[int]:
 
 def kvq_status_string(status: int) -> str:
     return lib().kvq_status_string(status).decode()
+
+
+def kvq_kernel_launches() -> int:
+    """Kernels this library has launched since it was loaded (all devices and streams)."""
+    return int(lib().kvq_kernel_launches())
 
 
 def kvq_row_bytes(fmt, bits: int, head_dim: int):

@@ -1,11 +1,15 @@
 // C ABI of libkvq.so: argument checks, split-K planning and kernel launches.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "kvq_internal.cuh"
 
 namespace kvq {
 bool decode_supports(int k_fmt, int k_bits, int v_fmt, int v_bits);
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }
 
 namespace {
@@ -166,6 +170,8 @@ KVQ_API const char* kvq_status_string(kvq_status s) {
   }
   return "KVQ_ERR_UNKNOWN";
 }
+
+KVQ_API uint64_t kvq_kernel_launches(void) { return kvq::g_launches.load(std::memory_order_relaxed); }
 
 KVQ_API kvq_status kvq_row_bytes(int32_t format, int32_t bits, int32_t head_dim, size_t* row_bytes,
                                  size_t* aux_bytes) {

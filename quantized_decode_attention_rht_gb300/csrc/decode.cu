@@ -8,7 +8,7 @@
 // units.  Per token it dequantises the K row in registers, forms the G scores, updates an
 // online softmax (running max / sum, one exp2 per score), and accumulates the value rows,
 // still in the rotated domain.  Partials (max, sum, acc[D]) go to the workspace.
-// Pass 2 (combine_kernel): one warp per (sequence, query head) merges the partials of every
+// Pass 2 (combine_kernel): one block per (sequence, query head) merges the partials of every
 // split of every tier, normalises, and undoes the V rotation, y = s_V * (H y~) / sqrt(D).
 //
 // Lane layout: LPT lanes share a token, each holding DPL = D/LPT consecutive coordinates
@@ -290,51 +290,75 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 }
 
 // ---------------------------------------------------------------- pass 2
-// One warp per (sequence, query head): lane l holds the D/32 consecutive coordinates
-// [l*D/32, (l+1)*D/32).  Merge the partials of every split of every tier (global max,
-// rescaled sums), normalise, then undo the V rotation with a Walsh-Hadamard transform
-// (in-register stages for the lane's coordinates, shuffles across lanes).
+// One block of kCombineWarps warps per (sequence, query head).  Warp w merges the splits
+// s = w, w + kCombineWarps, ... of every tier in one pass with a running max (each partial
+// is rescaled by exp2 of its max minus the running one), lane l holding the D/32 coordinates
+// [l*D/32, (l+1)*D/32).  Warp 0 then merges the warps' states, normalises, and undoes the V
+// rotation with a Walsh-Hadamard transform (in-register stages for the lane's coordinates,
+// shuffles across lanes).
+constexpr int kCombineWarps = 4;
+
 template <int D>
-__global__ void __launch_bounds__(128) combine_kernel(const DecParams p) {
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecParams p) {
   constexpr int PER = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (pair >= p.batch * p.hq) return;
+  __shared__ float s_acc[kCombineWarps][D];
+  __shared__ float s_ml[kCombineWarps][2];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = blockIdx.x;
   const int b = pair / p.hq, hq = pair % p.hq;
   const int hk = hq / (p.hq / p.hkv);
   const size_t base = ((size_t)b * p.hq + hq) * p.total_splits;
-  float mx = -INFINITY;
-  for (int ti = 0; ti < p.num_tiers; ++ti) {
-    const DecTier& T = p.tier[ti];
-    const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
-    for (int s = lane; s < n; s += 32) mx = fmaxf(mx, p.ws_ml[2 * (base + T.split_begin + s)]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   float acc[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  float lsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int ti = 0; ti < p.num_tiers; ++ti) {
-      const DecTier& T = p.tier[ti];
-      const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
-#pragma unroll 4
-      for (int s = 0; s < n; ++s) {
-        const size_t part = base + T.split_begin + s;
-        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * part);
-        const float f = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
-        lsum = fmaf(ml.y, f, lsum);
-        const float4* src = reinterpret_cast<const float4*>(p.ws_acc + part * D + lane * PER);
+  float m = -INFINITY, lsum = 0.f;
+  for (int ti = 0; ti < p.num_tiers; ++ti) {
+    const DecTier& T = p.tier[ti];
+    const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
+#pragma unroll 2
+    for (int s = warp; s < n; s += kCombineWarps) {
+      const size_t part = base + T.split_begin + s;
+      const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * part);
+      const float4* src = reinterpret_cast<const float4*>(p.ws_acc + part * D + lane * PER);
+      float4 v[PER / 4];
 #pragma unroll
-        for (int k = 0; k < PER / 4; ++k) {
-          const float4 v = src[k];
-          acc[4 * k] = fmaf(v.x, f, acc[4 * k]);
-          acc[4 * k + 1] = fmaf(v.y, f, acc[4 * k + 1]);
-          acc[4 * k + 2] = fmaf(v.z, f, acc[4 * k + 2]);
-          acc[4 * k + 3] = fmaf(v.w, f, acc[4 * k + 3]);
-        }
+      for (int k = 0; k < PER / 4; ++k) v[k] = src[k];
+      if (ml.x == -INFINITY) continue;  // a split that saw no token
+      const float mn = fmaxf(m, ml.x);
+      const float fo = exp2f(m - mn), fn = exp2f(ml.x - mn);  // m = -inf at first: fo = 0
+      lsum = lsum * fo + ml.y * fn;
+#pragma unroll
+      for (int k = 0; k < PER / 4; ++k) {
+        acc[4 * k] = fmaf(v[k].x, fn, acc[4 * k] * fo);
+        acc[4 * k + 1] = fmaf(v[k].y, fn, acc[4 * k + 1] * fo);
+        acc[4 * k + 2] = fmaf(v[k].z, fn, acc[4 * k + 2] * fo);
+        acc[4 * k + 3] = fmaf(v[k].w, fn, acc[4 * k + 3] * fo);
       }
+      m = mn;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) s_acc[warp][lane * PER + k] = acc[k];
+  if (lane == 0) {
+    s_ml[warp][0] = m;
+    s_ml[warp][1] = lsum;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) mx = fmaxf(mx, s_ml[w][0]);
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+  lsum = 0.f;
+  if (mx != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+      if (s_ml[w][0] == -INFINITY) continue;
+      const float f = exp2f(s_ml[w][0] - mx);
+      lsum = fmaf(s_ml[w][1], f, lsum);
+#pragma unroll
+      for (int k = 0; k < PER; ++k) acc[k] = fmaf(s_acc[w][lane * PER + k], f, acc[k]);
     }
   }
   const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
@@ -353,11 +377,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecParams p) {
     }
   }
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
+  for (int mm = 1; mm < 32; mm <<= 1) {
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      const float o = __shfl_xor_sync(0xFFFFFFFFu, acc[k], m);
-      acc[k] = (lane & m) ? (o - acc[k]) : (acc[k] + o);
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, acc[k], mm);
+      acc[k] = (lane & mm) ? (o - acc[k]) : (acc[k] + o);
     }
   }
   constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
@@ -380,7 +404,9 @@ cudaError_t launch_tier(const DecParams& p, int ti, cudaStream_t stream) {
   if (T.num_splits == 0) return cudaSuccess;
   dim3 grid(T.num_splits, p.hkv, p.batch);
   decode_tier_kernel<D, G, KF, VF><<<grid, kWarps * 32, 0, stream>>>(p, ti);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 template <int D, int G>
@@ -440,13 +466,14 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
 }
 
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
-  const int pairs = p.batch * p.hq;
-  const int blocks = (pairs + 3) / 4;
+  const int blocks = p.batch * p.hq;
   if (blocks == 0) return cudaSuccess;
-  if (head_dim == 128) combine_kernel<128><<<blocks, 128, 0, stream>>>(p);
-  else if (head_dim == 256) combine_kernel<256><<<blocks, 128, 0, stream>>>(p);
+  if (head_dim == 128) combine_kernel<128><<<blocks, kCombineWarps * 32, 0, stream>>>(p);
+  else if (head_dim == 256) combine_kernel<256><<<blocks, kCombineWarps * 32, 0, stream>>>(p);
   else return cudaErrorNotSupported;
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 }  // namespace kvq

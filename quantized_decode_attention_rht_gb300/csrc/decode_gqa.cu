@@ -638,7 +638,9 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
   e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
   if (e != cudaSuccess) return e;
   decode_gqa_kernel<<<ctas, kWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 }  // namespace kvq

@@ -11,6 +11,10 @@ namespace kvq {
 
 constexpr int kGroup = KVQ_INT4_GROUP;
 
+// Count of kernel launches made by this library (kvq_kernel_launches); every launcher calls
+// note_launch() after a launch that the runtime accepted.
+void note_launch();
+
 // ------------------------------------------------------------------------ quantize
 struct QuantSide {
   uint8_t* rows;

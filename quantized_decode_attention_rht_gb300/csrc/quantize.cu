@@ -328,7 +328,9 @@ cudaError_t launch_side(const QuantParams& p, int kind, int sms, cudaStream_t st
   const long long vpb = kThreads / TPV;
   const unsigned blocks = (unsigned)std::min<long long>((nvec + vpb - 1) / vpb, (long long)sms * 2);
   quantize_kernel<TPV, kCoords, FMT, BITS><<<blocks, kThreads, 0, stream>>>(p, kind);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 template <int TPV>

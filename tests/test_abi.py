@@ -39,6 +39,13 @@ def test_exports_match_header(kvq):
     assert exported == names
 
 
+def test_launch_counter_is_host_side(kvq):
+    n = kvq.kvq_kernel_launches()
+    assert isinstance(n, int) and n >= 0
+    assert kvq.kvq_quantize_append is not None  # argument checks below launch nothing
+    assert kvq.kvq_kernel_launches() == n
+
+
 def test_status_strings(kvq):
     for s, name in kvq.STATUS.items():
         assert kvq.kvq_status_string(s) == name
