@@ -45,6 +45,7 @@ extern "C" {
 #define KVQ_API __attribute__((visibility("default")))
 
 #define KVQ_MAX_TIERS 4  /* decode attends over at most this many tiers at once */
+#define KVQ_MAX_SPLITS 1024  /* split-K chunks per sequence, summed over the tiers */
 #define KVQ_INT4_GROUP 32 /* coordinates sharing one fp16 scale in KVQ_FMT_INT4_G32 */
 
 typedef enum kvq_status {
@@ -161,7 +162,9 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
 
 /* Workspace bytes kvq_decode_attention needs for these tiers and shapes (host output).
  * split_tokens: tokens per split-K chunk (a multiple of page_size), or 0 to let the
- * library choose; pass the same value to kvq_decode_attention. */
+ * library choose; pass the same value to kvq_decode_attention.  The chunks of the longest
+ * possible sequence (max_pages * page_size tokens per tier), summed over the tiers, may not
+ * exceed KVQ_MAX_SPLITS: a smaller split_tokens returns KVQ_ERR_UNSUPPORTED. */
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t num_tiers,
                                              int32_t batch, int32_t num_q_heads,
                                              int32_t split_tokens, size_t* bytes);

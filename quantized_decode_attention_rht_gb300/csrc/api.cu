@@ -89,6 +89,8 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
     // bulk copies of the norm runs need 16-byte aligned sources
     cb = cb && aligned(c->k_aux, 16) && aligned(c->v_aux, 16);
   }
+  // the fused fp16 / fp8 + INT4 kernel reads the sign vectors with 16-byte loads
+  gqa = gqa && aligned(c0->k_signs, 16) && aligned(c0->v_signs, 16);
   plan->kind = gqa ? PLAN_GQA : (cb ? PLAN_CB : PLAN_GENERIC);
   // fused kernels: items of about equal bytes, several per warp of a full GPU
   size_t total_bytes = 0;
@@ -117,6 +119,8 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
     plan->splits[i] = max_len == 0 ? 0 : (int)((max_len + chunk - 1) / chunk);
     plan->total += plan->splits[i];
   }
+  // the combine pass keeps the per-split weights of one output in shared memory
+  if (plan->total > KVQ_MAX_SPLITS) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 

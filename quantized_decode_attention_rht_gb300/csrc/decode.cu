@@ -290,76 +290,95 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 }
 
 // ---------------------------------------------------------------- pass 2
-// One block of kCombineWarps warps per (sequence, query head).  Warp w merges the splits
-// s = w, w + kCombineWarps, ... of every tier in one pass with a running max (each partial
-// is rescaled by exp2 of its max minus the running one), lane l holding the D/32 coordinates
-// [l*D/32, (l+1)*D/32).  Warp 0 then merges the warps' states, normalises, and undoes the V
-// rotation with a Walsh-Hadamard transform (in-register stages for the lane's coordinates,
-// shuffles across lanes).
+// One block of kCombineWarps warps per (sequence, query head).  First every thread reads
+// the (max, sum) pair of one split (all splits of every tier at once), and the block forms
+// the global max and each split's weight exp2(m_s - max); then warp w streams the
+// accumulators of splits w, w + kCombineWarps, ... with no dependence between splits (lane
+// l holds coordinates [l*D/32, (l+1)*D/32)).  Warp 0 sums the warps, normalises, and
+// undoes the V rotation with a Walsh-Hadamard transform (in-register stages for the lane's
+// coordinates, shuffles across lanes).  Launched as a programmatic dependent of the split-K
+// pass: it waits for that grid's completion before touching the partials.
 constexpr int kCombineWarps = 4;
+constexpr int kCombineMaxSplits = KVQ_MAX_SPLITS;  // the plan never makes more splits per output
 
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecParams p) {
   constexpr int PER = D / 32;
   __shared__ float s_acc[kCombineWarps][D];
-  __shared__ float s_ml[kCombineWarps][2];
+  __shared__ float s_w[kCombineMaxSplits];
+  __shared__ int s_part[kCombineMaxSplits];
+  __shared__ float s_red[kCombineWarps][2];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // partials of the split-K pass are complete
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = blockIdx.x;
   const int b = pair / p.hq, hq = pair % p.hq;
   const int hk = hq / (p.hq / p.hkv);
   const size_t base = ((size_t)b * p.hq + hq) * p.total_splits;
+  // ---- splits holding tokens, over every tier: partial indices and (max, sum)
+  int n = 0;
+  for (int ti = 0; ti < p.num_tiers; ++ti) {
+    const DecTier& T = p.tier[ti];
+    const int nt = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
+    for (int s = threadIdx.x; s < nt && n + s < kCombineMaxSplits; s += blockDim.x)
+      s_part[n + s] = T.split_begin + s;
+    n += nt;
+  }
+  n = min(n, kCombineMaxSplits);  // the plan refuses more splits than this
+  __syncthreads();
+  float mx = -INFINITY, lsum = 0.f;
+  for (int s = threadIdx.x; s < n; s += blockDim.x) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * (base + s_part[s]));
+    s_w[s] = ml.x;
+    mx = fmaxf(mx, ml.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if (lane == 0) s_red[warp][0] = mx;
+  __syncthreads();
+  mx = s_red[0][0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_red[w][0]);
+  __syncthreads();  // s_red is reused below
+  for (int s = threadIdx.x; s < n; s += blockDim.x) {
+    const float m = s_w[s];
+    const float f = m == -INFINITY ? 0.f : exp2f(m - mx);  // a split that saw no token: 0
+    lsum = fmaf(p.ws_ml[2 * (base + s_part[s]) + 1], f, lsum);
+    s_w[s] = f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+  if (lane == 0) s_red[warp][1] = lsum;
+  __syncthreads();
+  // ---- weighted sum of the accumulators
   float acc[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-  float m = -INFINITY, lsum = 0.f;
-  for (int ti = 0; ti < p.num_tiers; ++ti) {
-    const DecTier& T = p.tier[ti];
-    const int n = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
-#pragma unroll 2
-    for (int s = warp; s < n; s += kCombineWarps) {
-      const size_t part = base + T.split_begin + s;
-      const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * part);
-      const float4* src = reinterpret_cast<const float4*>(p.ws_acc + part * D + lane * PER);
-      float4 v[PER / 4];
+#pragma unroll 4
+  for (int s = warp; s < n; s += kCombineWarps) {
+    const float f = s_w[s];
+    const float4* src = reinterpret_cast<const float4*>(p.ws_acc + (base + s_part[s]) * D + lane * PER);
 #pragma unroll
-      for (int k = 0; k < PER / 4; ++k) v[k] = src[k];
-      if (ml.x == -INFINITY) continue;  // a split that saw no token
-      const float mn = fmaxf(m, ml.x);
-      const float fo = exp2f(m - mn), fn = exp2f(ml.x - mn);  // m = -inf at first: fo = 0
-      lsum = lsum * fo + ml.y * fn;
-#pragma unroll
-      for (int k = 0; k < PER / 4; ++k) {
-        acc[4 * k] = fmaf(v[k].x, fn, acc[4 * k] * fo);
-        acc[4 * k + 1] = fmaf(v[k].y, fn, acc[4 * k + 1] * fo);
-        acc[4 * k + 2] = fmaf(v[k].z, fn, acc[4 * k + 2] * fo);
-        acc[4 * k + 3] = fmaf(v[k].w, fn, acc[4 * k + 3] * fo);
-      }
-      m = mn;
+    for (int k = 0; k < PER / 4; ++k) {
+      const float4 v = src[k];
+      acc[4 * k] = fmaf(v.x, f, acc[4 * k]);
+      acc[4 * k + 1] = fmaf(v.y, f, acc[4 * k + 1]);
+      acc[4 * k + 2] = fmaf(v.z, f, acc[4 * k + 2]);
+      acc[4 * k + 3] = fmaf(v.w, f, acc[4 * k + 3]);
     }
   }
 #pragma unroll
   for (int k = 0; k < PER; ++k) s_acc[warp][lane * PER + k] = acc[k];
-  if (lane == 0) {
-    s_ml[warp][0] = m;
-    s_ml[warp][1] = lsum;
-  }
   __syncthreads();
   if (warp != 0) return;
-  float mx = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kCombineWarps; ++w) mx = fmaxf(mx, s_ml[w][0]);
-#pragma unroll
-  for (int k = 0; k < PER; ++k) acc[k] = 0.f;
   lsum = 0.f;
-  if (mx != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
-      if (s_ml[w][0] == -INFINITY) continue;
-      const float f = exp2f(s_ml[w][0] - mx);
-      lsum = fmaf(s_ml[w][1], f, lsum);
+  for (int w = 0; w < kCombineWarps; ++w) lsum += s_red[w][1];
 #pragma unroll
-      for (int k = 0; k < PER; ++k) acc[k] = fmaf(s_acc[w][lane * PER + k], f, acc[k]);
-    }
+  for (int k = 0; k < PER; ++k) {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) a += s_acc[w][lane * PER + k];
+    acc[k] = a;
   }
   const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
 #pragma unroll
@@ -468,12 +487,22 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
   const int blocks = p.batch * p.hq;
   if (blocks == 0) return cudaSuccess;
-  if (head_dim == 128) combine_kernel<128><<<blocks, kCombineWarps * 32, 0, stream>>>(p);
-  else if (head_dim == 256) combine_kernel<256><<<blocks, kCombineWarps * 32, 0, stream>>>(p);
-  else return cudaErrorNotSupported;
-  const cudaError_t e = cudaGetLastError();
+  if (head_dim != 128 && head_dim != 256) return cudaErrorNotSupported;
+  // programmatic dependent launch: the grid may be set up while the split-K pass drains
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
+                                        : cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
   if (e == cudaSuccess) note_launch();
-  return e;
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace kvq

@@ -145,6 +145,8 @@ def test_decode_argument_checks(kvq):
     assert _ws(kvq, [c, _fake_cache(kvq, k_signs=(1 << 40) + 4096 * 20)])[0] == 1  # tiers disagree on signs
     assert _ws(kvq, [c, _fake_cache(kvq, num_kv_heads=4)])[0] == 1
     assert _ws(kvq, [c], split=24)[0] == 1  # split not a multiple of the page size
+    assert _ws(kvq, [c], split=16, max_pages=2000)[0] == 2  # more than KVQ_MAX_SPLITS chunks
+    assert _ws(kvq, [c], split=32, max_pages=2000)[0] == 0
     assert _ws(kvq, [_fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_CODEBOOK)])[0] == 2
     # decode with too small a workspace fails before any launch
     L = kvq.lib()

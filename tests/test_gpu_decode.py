@@ -98,6 +98,18 @@ def test_decode_two_tier_edge_lengths():
 
 
 @pytest.mark.gpu
+def test_two_tier_many_splits():
+    """Split size 16 over long two-tier sequences (78 partials per sequence for the longest):
+    same result as the default split."""
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=3, num_q_heads=8, num_kv_heads=2)
+    lens = [1234, 700, 1]
+    got16, want, _, _ = run_exact(cfg, lens, split_tokens=16)
+    got0, _, _, _ = run_exact(cfg, lens)
+    assert np.abs(got16 - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+    np.testing.assert_allclose(got16, got0, rtol=0, atol=2e-6 * max(1.0, np.abs(got0).max()))
+
+
+@pytest.mark.gpu
 def test_split_invariance():
     """Split-K over 1, 2, 7 chunks and one chunk per page gives the same output."""
     cfg = W.CONFIGS["ragged"].scaled(batch=2, num_q_heads=8, num_kv_heads=2)

@@ -67,6 +67,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     views[0].cache = ctypes.pointer(s)
     views[0].block_table = 1 << 43
     views[0].seq_lens = 1 << 44
-    views[0].max_pages = 1 << 16  # 1M tokens with 16-token splits: far more scratch than it has
-    st = kvq.lib().kvq_decode_attention_noalloc(views, 1, 1 << 45, 64, 32, 16, 1 << 46, None)
+    views[0].max_pages = 1 << 16  # 1M tokens in 1024-token splits: 1024 splits per output,
+    # within the split limit but ~1 GB of partials, far more scratch than it has
+    st = kvq.lib().kvq_decode_attention_noalloc(views, 1, 1 << 45, 64, 32, 1024, 1 << 46, None)
     assert st == 3  # KVQ_ERR_WORKSPACE_TOO_SMALL
