@@ -11,9 +11,9 @@
 //      and "The Bit-Packing Problem"); fp16 / fp8 E4M3 / INT4-g32 formats: the rotated vector
 //      rounded to the format (FoveatedKV page, "The VR headset thing");
 //   3. store the row at its pool slot.
-// One launch per side (K, V), specialised to that side's format so the kernel holds a single
-// short path; a persistent grid walks the vectors; the decision table is built once per
-// block.
+// One launch for both sides (K and V blocks in grid rows 0 and 1), each row specialised to
+// its side's format so a block holds a single short path; a persistent grid walks the
+// vectors; the decision table is built once per block.
 // The kernel is HBM-bound: 2*D bytes read and one row (+ side data) written per vector.
 #include <algorithm>
 
@@ -169,182 +169,244 @@ __device__ __forceinline__ void encode_codebook(const Table& tb, const float (&y
 
 enum { F_CB = 0, F_F16 = 1, F_F8 = 2, F_I4 = 3 };
 
-// One side (K or V) of a quantise-and-append call.  TPV threads per vector, kE coordinates
-// each; FMT / BITS fix the storage format so the kernel holds one path only.
+// One vector's TPV lanes: sub-part `sub` holds coordinates [sub * kE, (sub + 1) * kE) of
+// the vector, read from src (fp16).  Rotates, encodes and stores it.
 template <int TPV, int kE, int FMT, int BITS>
-__global__ void __launch_bounds__(kThreads) quantize_kernel(const QuantParams p, int kind) {
+__device__ __forceinline__ void quantize_vector(const QuantParams& p, const QuantSide& side, const Table& table,
+                                                const uint16_t* src, int token, int h, int sub, unsigned gmask) {
   constexpr int D = kE * TPV;
-  const QuantSide& side = p.side[kind];
-  __shared__ Table table;
-  if constexpr (FMT == F_CB) build_table(table, side.bounds, (1 << BITS) - 1, D);
-  const int lane = threadIdx.x & 31;
-  const int sub = lane % TPV;  // which kE-coordinate part
-  const unsigned gmask = (TPV == 32 ? 0xFFFFFFFFu : ((1u << TPV) - 1u)) << (lane - sub);
-  const int nvec = p.num_tokens * p.hkv;
-  const int stride = gridDim.x * (kThreads / TPV);
-  const uint16_t* x = p.x[kind];
   constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
   constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
+  const int slot = p.slots[token];
+  const bool store = slot >= 0 && slot < p.num_slots;
 
-  for (int v = blockIdx.x * (kThreads / TPV) + threadIdx.x / TPV; v < nvec; v += stride) {
-    const int token = v / p.hkv, h = v - token * p.hkv;
-    const int slot = p.slots[token];
-    const bool store = slot >= 0 && slot < p.num_slots;
-
-    // ---- load kE fp16 coordinates and their signs; y = s * x
-    float y[kE];
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(x + ((size_t)token * p.hkv + h) * D + sub * kE);
-      const uint4* sg = reinterpret_cast<const uint4*>(side.signs + (size_t)h * D + sub * kE);
-      uint4 xs[kE / 8], ss[kE / 16];
+  // ---- kE fp16 coordinates and their signs; y = s * x
+  float y[kE];
+  {
+    const uint4* sg = reinterpret_cast<const uint4*>(side.signs + (size_t)h * D + sub * kE);
+    uint32_t xw[kE / 2];
+    uint4 ss[kE / 16];
 #pragma unroll
-      for (int i = 0; i < kE / 8; ++i) xs[i] = __ldg(src + i);
-#pragma unroll
-      for (int i = 0; i < kE / 16; ++i) ss[i] = __ldg(sg + i);
-      const uint32_t* xw = reinterpret_cast<const uint32_t*>(xs);
-      const uint32_t* sw = reinterpret_cast<const uint32_t*>(ss);
-#pragma unroll
-      for (int k = 0; k < kE / 2; ++k) {
-        // sign bytes 2k, 2k+1 (int8 +-1: bit 7 set for -1) -> fp16 sign bits 15, 31
-        const uint32_t m = __byte_perm(sw[k >> 1], 0, (k & 1) ? 0x3424 : 0x1404) & 0x80008000u;
-        const uint32_t xv = xw[k] ^ m;
-        const __half2 h2 = *reinterpret_cast<const __half2*>(&xv);
-        y[2 * k] = __low2float(h2);
-        y[2 * k + 1] = __high2float(h2);
-      }
+    for (int i = 0; i < kE / 8; ++i) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      xw[4 * i] = u.x;
+      xw[4 * i + 1] = u.y;
+      xw[4 * i + 2] = u.z;
+      xw[4 * i + 3] = u.w;
     }
-    // ---- Walsh-Hadamard: stage 1 in scalar, stages 2.. on f32x2 pairs, then across lanes
+#pragma unroll
+    for (int i = 0; i < kE / 16; ++i) ss[i] = __ldg(sg + i);
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(ss);
+#pragma unroll
+    for (int k = 0; k < kE / 2; ++k) {
+      // sign bytes 2k, 2k+1 (int8 +-1: bit 7 set for -1) -> fp16 sign bits 15, 31
+      const uint32_t m = __byte_perm(sw[k >> 1], 0, (k & 1) ? 0x3424 : 0x1404) & 0x80008000u;
+      const uint32_t xv = xw[k] ^ m;
+      const __half2 h2 = *reinterpret_cast<const __half2*>(&xv);
+      y[2 * k] = __low2float(h2);
+      y[2 * k + 1] = __high2float(h2);
+    }
+  }
+  // ---- Walsh-Hadamard: stage 1 in scalar, stages 2.. on f32x2 pairs, then across lanes
+#pragma unroll
+  for (int e = 0; e < kE; e += 2) {
+    const float a = y[e], c = y[e + 1];
+    y[e] = a + c;
+    y[e + 1] = a - c;
+  }
+#pragma unroll
+  for (int hs = 2; hs < kE; hs <<= 1) {
 #pragma unroll
     for (int e = 0; e < kE; e += 2) {
-      const float a = y[e], c = y[e + 1];
-      y[e] = a + c;
-      y[e + 1] = a - c;
-    }
-#pragma unroll
-    for (int hs = 2; hs < kE; hs <<= 1) {
-#pragma unroll
-      for (int e = 0; e < kE; e += 2) {
-        if ((e & hs) == 0) {
-          const u64 a = pk(y[e], y[e + 1]), c = pk(y[e + hs], y[e + hs + 1]);
-          upk(add2(a, c), y[e], y[e + 1]);
-          upk(sub2(a, c), y[e + hs], y[e + hs + 1]);
-        }
+      if ((e & hs) == 0) {
+        const u64 a = pk(y[e], y[e + 1]), c = pk(y[e + hs], y[e + hs + 1]);
+        upk(add2(a, c), y[e], y[e + 1]);
+        upk(sub2(a, c), y[e + hs], y[e + hs + 1]);
       }
     }
+  }
 #pragma unroll
-    for (int m = 1; m < TPV; m <<= 1) {
-      const float sgn = (sub & m) ? -1.0f : 1.0f;  // upper lane keeps partner - own
+  for (int m = 1; m < TPV; m <<= 1) {
+    const float sgn = (sub & m) ? -1.0f : 1.0f;  // upper lane keeps partner - own
 #pragma unroll
-      for (int e = 0; e < kE; ++e) y[e] = fmaf(sgn, y[e], __shfl_xor_sync(gmask, y[e], m, TPV));
-    }
-    // y = H s x (unnormalised); the rotated vector is x~ = y / sqrt(D)
-    const int slot_c = store ? slot : 0;
-    const size_t prow = ((size_t)(slot_c / p.page_size) * p.hkv + h) * p.page_size + (slot_c % p.page_size);
-    uint8_t* row = side.rows + prow * side.row_bytes;
+    for (int e = 0; e < kE; ++e) y[e] = fmaf(sgn, y[e], __shfl_xor_sync(gmask, y[e], m, TPV));
+  }
+  // y = H s x (unnormalised); the rotated vector is x~ = y / sqrt(D)
+  const int slot_c = store ? slot : 0;
+  const size_t prow = ((size_t)(slot_c / p.page_size) * p.hkv + h) * p.page_size + (slot_c % p.page_size);
+  uint8_t* row = side.rows + prow * side.row_bytes;
 
-    if constexpr (FMT == F_CB) {
-      u64 acc = pk(0.f, 0.f);
+  if constexpr (FMT == F_CB) {
+    u64 acc = pk(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < kE; e += 2) {
-        const u64 v2 = pk(y[e], y[e + 1]);
-        acc = fma2(v2, v2, acc);
-      }
-      float a0, a1;
-      upk(acc, a0, a1);
-      float ss = a0 + a1;
+    for (int e = 0; e < kE; e += 2) {
+      const u64 v2 = pk(y[e], y[e + 1]);
+      acc = fma2(v2, v2, acc);
+    }
+    float a0, a1;
+    upk(acc, a0, a1);
+    float ss = a0 + a1;
 #pragma unroll
-      for (int m = 1; m < TPV; m <<= 1) ss += __shfl_xor_sync(gmask, ss, m, TPV);
-      const float ny = sqrtf(ss);
-      const float inv = ny > 0.0f ? sqrt_d / ny : 0.0f;  // u = sqrt(D) y / ||y||
-      encode_codebook<BITS, kE>(table, y, inv * table.inv_w, row + sub * (kE * BITS / 8), store);
-      if (store && sub == 0) side.aux[prow] = __float2half_rn(ny * inv_sqrt_d);
-    } else if constexpr (FMT == F_F16) {
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(row) + sub * (kE / 8);
+    for (int m = 1; m < TPV; m <<= 1) ss += __shfl_xor_sync(gmask, ss, m, TPV);
+    const float ny = sqrtf(ss);
+    const float inv = ny > 0.0f ? sqrt_d / ny : 0.0f;  // u = sqrt(D) y / ||y||
+    encode_codebook<BITS, kE>(table, y, inv * table.inv_w, row + sub * (kE * BITS / 8), store);
+    if (store && sub == 0) side.aux[prow] = __float2half_rn(ny * inv_sqrt_d);
+  } else if constexpr (FMT == F_F16) {
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(row) + sub * (kE / 8);
 #pragma unroll
-        for (int k = 0; k < kE / 8; ++k) {
-          uint32_t w[4];
+      for (int k = 0; k < kE / 8; ++k) {
+        uint32_t w[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const __half2 h2 = __floats2half2_rn(y[8 * k + 2 * j] * inv_sqrt_d, y[8 * k + 2 * j + 1] * inv_sqrt_d);
-            w[j] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < 4; ++j) {
+          const __half2 h2 = __floats2half2_rn(y[8 * k + 2 * j] * inv_sqrt_d, y[8 * k + 2 * j + 1] * inv_sqrt_d);
+          w[j] = *reinterpret_cast<const uint32_t*>(&h2);
         }
+        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-    } else if constexpr (FMT == F_F8) {
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(row) + sub * (kE / 16);
+    }
+  } else if constexpr (FMT == F_F8) {
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(row) + sub * (kE / 16);
 #pragma unroll
-        for (int k = 0; k < kE / 16; ++k) {
-          uint32_t w[4];
+      for (int k = 0; k < kE / 16; ++k) {
+        uint32_t w[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int e = 16 * k + 4 * j;
-            const uint32_t a = float2_to_fp8x2(y[e] * inv_sqrt_d, y[e + 1] * inv_sqrt_d);
-            const uint32_t b = float2_to_fp8x2(y[e + 2] * inv_sqrt_d, y[e + 3] * inv_sqrt_d);
-            w[j] = a | (b << 16);
-          }
-          dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < 4; ++j) {
+          const int e = 16 * k + 4 * j;
+          const uint32_t a = float2_to_fp8x2(y[e] * inv_sqrt_d, y[e + 1] * inv_sqrt_d);
+          const uint32_t b = float2_to_fp8x2(y[e + 2] * inv_sqrt_d, y[e + 3] * inv_sqrt_d);
+          w[j] = a | (b << 16);
         }
+        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
       }
-    } else {  // F_I4: kE / 32 groups of 32 coordinates per thread
-      constexpr int NG = kE / kGroup;
-      uint32_t w[NG * 4];
+    }
+  } else {  // F_I4: kE / 32 groups of 32 coordinates per thread
+    constexpr int NG = kE / kGroup;
+    uint32_t w[NG * 4];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        float amax = 0.0f;
+    for (int g = 0; g < NG; ++g) {
+      float amax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(y[kGroup * g + e] * inv_sqrt_d));
-        const __half s16 = __float2half_rn(amax / 7.0f);
-        const float s = __half2float(s16);
-        const float r = s > 0.0f ? 1.0f / s : 0.0f;
+      for (int e = 0; e < kGroup; ++e) amax = fmaxf(amax, fabsf(y[kGroup * g + e] * inv_sqrt_d));
+      const __half s16 = __float2half_rn(amax / 7.0f);
+      const float s = __half2float(s16);
+      const float r = s > 0.0f ? 1.0f / s : 0.0f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) w[4 * g + k] = 0;
+      for (int k = 0; k < 4; ++k) w[4 * g + k] = 0;
 #pragma unroll
-        for (int e = 0; e < kGroup; ++e) {
-          const float xv = y[kGroup * g + e] * inv_sqrt_d;
-          // level = rint(x / s): x * (1/s) is within one ulp of the quotient; where that
-          // leaves the result next to a half-integer, divide exactly
-          float tq = xv * r;
-          if (s > 0.0f && fabsf(fabsf(tq - rintf(tq)) - 0.5f) < 1e-5f) tq = xv / s;
-          const float q = s > 0.0f ? fminf(fmaxf(rintf(tq), -7.0f), 7.0f) : 0.0f;
-          w[4 * g + e / 8] |= (uint32_t)((int)q + 8) << (4 * (e % 8));
-        }
-        if (store) side.aux[prow * (D / kGroup) + sub * NG + g] = s16;
+      for (int e = 0; e < kGroup; ++e) {
+        const float xv = y[kGroup * g + e] * inv_sqrt_d;
+        // level = rint(x / s): x * (1/s) is within one ulp of the quotient; where that
+        // leaves the result next to a half-integer, divide exactly
+        float tq = xv * r;
+        if (s > 0.0f && fabsf(fabsf(tq - rintf(tq)) - 0.5f) < 1e-5f) tq = xv / s;
+        const float q = s > 0.0f ? fminf(fmaxf(rintf(tq), -7.0f), 7.0f) : 0.0f;
+        w[4 * g + e / 8] |= (uint32_t)((int)q + 8) << (4 * (e % 8));
       }
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(row) + sub * NG;
+      if (store) side.aux[prow * (D / kGroup) + sub * NG + g] = s16;
+    }
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(row) + sub * NG;
 #pragma unroll
-        for (int k = 0; k < NG; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-      }
+      for (int k = 0; k < NG; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
     }
   }
 }
 
+constexpr long long kPairedMaxVectors = 1 << 16;  // per side
+
+// Every vector of one side (kind) that falls to this block (grid-stride over vectors).
 template <int TPV, int FMT, int BITS>
-cudaError_t launch_side(const QuantParams& p, int kind, int sms, cudaStream_t stream) {
+__device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Table& table) {
+  constexpr int kE = kCoords, D = kE * TPV, VPB = kThreads / TPV;
+  const QuantSide& side = p.side[kind];
+  if constexpr (FMT == F_CB) build_table(table, side.bounds, (1 << BITS) - 1, D);
+  const int lane = threadIdx.x & 31, sub = lane % TPV;
+  const unsigned gmask = (TPV == 32 ? 0xFFFFFFFFu : ((1u << TPV) - 1u)) << (lane - sub);
+  const int nvec = p.num_tokens * p.hkv;
+  const int stride = gridDim.x * VPB;
+  const uint16_t* x = p.x[kind];
+  for (int v = blockIdx.x * VPB + threadIdx.x / TPV; v < nvec; v += stride) {
+    const int token = v / p.hkv, h = v - token * p.hkv;
+    quantize_vector<TPV, kE, FMT, BITS>(p, side, table, x + (size_t)v * D + sub * kE, token, h, sub, gmask);
+  }
+}
+
+// Side slot blockIdx.y: (F0, B0) for slot 0, (F1, B1) for slot 1; kind = kind_first + slot.
+template <int TPV, int F0, int B0, int F1, int B1>
+__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantParams p) {
+  __shared__ Table table;
+  if (blockIdx.y == 0) quantize_side<TPV, F0, B0>(p, p.kind_first, table);
+  else quantize_side<TPV, F1, B1>(p, p.kind_first + 1, table);
+}
+
+template <int TPV, int F0, int B0, int F1, int B1>
+cudaError_t launch_q(const QuantParams& p, int sides, int sms, cudaStream_t stream) {
+  constexpr int VPB = kThreads / TPV;
   const long long nvec = (long long)p.num_tokens * p.hkv;
-  const long long vpb = kThreads / TPV;
-  const unsigned blocks = (unsigned)std::min<long long>((nvec + vpb - 1) / vpb, (long long)sms * 2);
-  quantize_kernel<TPV, kCoords, FMT, BITS><<<blocks, kThreads, 0, stream>>>(p, kind);
+  const long long need = (nvec + VPB - 1) / VPB;
+  const unsigned blocks = (unsigned)std::max<long long>(1, std::min<long long>(need, (long long)sms * 2 / sides));
+  quantize_kernel<TPV, F0, B0, F1, B1><<<dim3(blocks, sides), kThreads, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }
 
-template <int TPV>
-cudaError_t launch_tpv(const QuantParams& p, int kind, int sms, cudaStream_t stream) {
-  const QuantSide& s = p.side[kind];
-  switch (s.fmt) {
+// A format / code width as a (F, B) template pair.
+template <int TPV, int F0, int B0>
+cudaError_t launch_second(const QuantParams& p, const QuantSide& s1, int sms, cudaStream_t stream) {
+  switch (s1.fmt) {
     case KVQ_FMT_CODEBOOK:
-      if (s.bits == 4) return launch_side<TPV, F_CB, 4>(p, kind, sms, stream);
-      if (s.bits == 3) return launch_side<TPV, F_CB, 3>(p, kind, sms, stream);
-      return launch_side<TPV, F_CB, 2>(p, kind, sms, stream);
-    case KVQ_FMT_FP16: return launch_side<TPV, F_F16, 0>(p, kind, sms, stream);
-    case KVQ_FMT_FP8_E4M3: return launch_side<TPV, F_F8, 0>(p, kind, sms, stream);
-    default: return launch_side<TPV, F_I4, 0>(p, kind, sms, stream);
+      if (s1.bits == 4) return launch_q<TPV, F0, B0, F_CB, 4>(p, 2, sms, stream);
+      if (s1.bits == 3) return launch_q<TPV, F0, B0, F_CB, 3>(p, 2, sms, stream);
+      return launch_q<TPV, F0, B0, F_CB, 2>(p, 2, sms, stream);
+    default: return cudaErrorNotSupported;
   }
+}
+
+template <int TPV, int F0, int B0>
+cudaError_t launch_single(const QuantParams& p, int sms, cudaStream_t stream) {
+  return launch_q<TPV, F0, B0, F0, B0>(p, 1, sms, stream);
+}
+
+template <int TPV>
+cudaError_t launch_tpv(const QuantParams& p, int sms, cudaStream_t stream) {
+  const QuantSide& s0 = p.side[p.kind_first];
+  const QuantSide& s1 = p.side[1];
+  // Small appends (a decode step's one token per sequence) are bound by launch latency:
+  // both sides go in one launch, for the pairs the caches use.  Large ones launch per side,
+  // so every SM runs a single side's code path (the paths are long; two of them on one SM
+  // compete for the instruction cache).
+  const bool both = p.num_kinds == 2 && (long long)p.num_tokens * p.hkv <= kPairedMaxVectors;
+  if (both && s0.fmt == KVQ_FMT_CODEBOOK && s1.fmt == KVQ_FMT_CODEBOOK) {
+    if (s0.bits == 4) return launch_second<TPV, F_CB, 4>(p, s1, sms, stream);
+    if (s0.bits == 3) return launch_second<TPV, F_CB, 3>(p, s1, sms, stream);
+    return launch_second<TPV, F_CB, 2>(p, s1, sms, stream);
+  }
+  if (both && s0.fmt == KVQ_FMT_FP16 && s1.fmt == KVQ_FMT_FP16) return launch_q<TPV, F_F16, 0, F_F16, 0>(p, 2, sms, stream);
+  if (both && s0.fmt == KVQ_FMT_FP8_E4M3 && s1.fmt == KVQ_FMT_INT4_G32)
+    return launch_q<TPV, F_F8, 0, F_I4, 0>(p, 2, sms, stream);
+  for (int kind = p.kind_first; kind < p.kind_first + p.num_kinds; ++kind) {
+    QuantParams q = p;
+    q.kind_first = kind;
+    q.num_kinds = 1;
+    const QuantSide& s = p.side[kind];
+    cudaError_t e;
+    switch (s.fmt) {
+      case KVQ_FMT_CODEBOOK:
+        e = s.bits == 4 ? launch_single<TPV, F_CB, 4>(q, sms, stream)
+                        : (s.bits == 3 ? launch_single<TPV, F_CB, 3>(q, sms, stream)
+                                       : launch_single<TPV, F_CB, 2>(q, sms, stream));
+        break;
+      case KVQ_FMT_FP16: e = launch_single<TPV, F_F16, 0>(q, sms, stream); break;
+      case KVQ_FMT_FP8_E4M3: e = launch_single<TPV, F_F8, 0>(q, sms, stream); break;
+      default: e = launch_single<TPV, F_I4, 0>(q, sms, stream); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -356,13 +418,9 @@ cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t str
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  for (int kind = p.kind_first; kind < p.kind_first + p.num_kinds; ++kind) {
-    // kCoords coordinates per thread: 2 lanes per vector for head_dim 128, 4 for 256
-    e = head_dim == 128 ? launch_tpv<2>(p, kind, sms, stream)
-                        : (head_dim == 256 ? launch_tpv<4>(p, kind, sms, stream) : cudaErrorInvalidValue);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  // kCoords coordinates per thread: 2 lanes per vector for head_dim 128, 4 for 256
+  return head_dim == 128 ? launch_tpv<2>(p, sms, stream)
+                         : (head_dim == 256 ? launch_tpv<4>(p, sms, stream) : cudaErrorInvalidValue);
 }
 
 }  // namespace kvq
