@@ -15,6 +15,10 @@ Steps, in this order, all in float64:
   3. for every query head of the group (query head h reads kv head h // (Hq/Hkv)),
      plain softmax(q K^T / sqrt(d)) V over all tokens of all tiers.
 
+Keys stored with a residual sketch (codebook_qjl, VeloxQuant-MLX page "Stage 3"): the
+score of such a key is the page's corrected inner product, <q, k^> plus the sketch's
+estimate of <q, r> (cache.qjl_correction, taken with the rotated query q~ = R q).
+
 Readings taken: decode attends to the whole cache (no causal or window mask: the
 query is the newest token); the output is float32; a sequence with no cached
 token gives a zero output.  The oracle does not use the rotated-domain scores, a
@@ -30,6 +34,7 @@ from typing import List, Sequence
 import numpy as np
 
 from . import cache
+from .rotation import rotate
 
 
 @dataclasses.dataclass
@@ -58,10 +63,32 @@ def dequantised_kv(tiers: Sequence[TierState], b: int, g: int):
     return np.concatenate(ks, axis=0), np.concatenate(vs, axis=0)
 
 
-def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray) -> np.ndarray:
-    """softmax(q K^T / sqrt(d)) V for one query vector q [d] (float64)."""
+def sketch_terms(tiers: Sequence[TierState], b: int, g: int, q: np.ndarray) -> np.ndarray:
+    """Per token of sequence b, kv head g (tier order, as dequantised_kv): the residual
+    sketch's estimate of <q, r> for keys stored with one, else 0."""
+    out = []
+    for t in tiers:
+        n = int(t.lens[b])
+        if n == 0:
+            continue
+        if t.k.fmt != cache.CODEBOOK_QJL:
+            out.append(np.zeros(n))
+            continue
+        rows, aux = cache.gather(t.k, t.block_table[b], n, g, t.page_size)
+        q_rot = rotate(np.asarray(q, dtype=np.float64), t.k.signs[g])
+        d = q.shape[-1]
+        out.append(cache.qjl_correction(rows, aux, q_rot, t.k.proj, d, t.k.bits))
+    return np.concatenate(out) if out else np.zeros(0)
+
+
+def attend(q: np.ndarray, keys: np.ndarray, values: np.ndarray, extra=None) -> np.ndarray:
+    """softmax(q K^T / sqrt(d)) V for one query vector q [d] (float64); `extra` [L] adds
+    to each q.k before the 1/sqrt(d) scaling (the residual sketch's term)."""
     d = q.shape[-1]
-    scores = keys @ np.asarray(q, dtype=np.float64) / math.sqrt(d)
+    dots = keys @ np.asarray(q, dtype=np.float64)
+    if extra is not None:
+        dots = dots + extra
+    scores = dots / math.sqrt(d)
     w = np.exp(scores - np.max(scores))  # the shift cancels in the normalisation
     w = w / np.sum(w)
     return w @ values
@@ -84,6 +111,8 @@ def decode_attention(q16: np.ndarray, tiers: Sequence[TierState],
             keys, values = dequantised_kv(tiers, b, g)
             if keys is None:
                 continue
+            sketched = any(t.k.fmt == cache.CODEBOOK_QJL for t in tiers)
             for h in todo:
-                out[b, h] = attend(q16[b, h].astype(np.float64), keys, values)
+                q = q16[b, h].astype(np.float64)
+                out[b, h] = attend(q, keys, values, sketch_terms(tiers, b, g, q) if sketched else None)
     return out.astype(np.float32)

@@ -8,6 +8,11 @@ Sources:
     token and head the record is the packed indices plus the fp16 norm.
   * FoveatedKV page, section "The VR headset thing": near tier fp16, far tier fp8
     E4M3 keys and INT4 values; every token still contributes to attention.
+  * VeloxQuant-MLX page, section "Stage 3: QJL Residual Correction" (TurboQuantProd):
+    the residual r = k - k^ of the codebook encode is not stored; only the signs
+    z = sign(S r) of a random Johnson-Lindenstrauss projection (m = 128 rows) and the
+    residual norm ||r|| as fp16; its "Memory Layout" table: for d = 128 and 3-bit codes
+    48 B of codes + 16 B of signs + 2 B residual norm + 2 B norm = 68 B per key.
 
 Readings taken:
   * unit-norm coordinates of a d-dimensional rotated vector are about N(0, 1/d),
@@ -21,7 +26,13 @@ Readings taken:
   * pool layout: rows[page][kv_head][slot_in_page][row_bytes], side data
     (fp16 norm or fp16 group scales) aux[page][kv_head][slot_in_page][...]; a token
     of sequence b at position t lives in page block_table[b][t // page_size] at slot
-    t % page_size.
+    t % page_size;
+  * residual sketch: taken in the rotated domain, z = sign(S r~) with r~ = x~ - x^~
+    (x^~ the dequantised rotated vector, exactly what the decoder reconstructs) and S
+    an m x d matrix of iid N(0,1) entries -- equal in distribution to sketching the
+    unrotated residual, since the rotation is orthogonal; sign(0) = +1; the m sign
+    bits follow the codes in the row, LSB-first like the codes; side data is
+    (fp16 norm, fp16 ||r~||).
 """
 from __future__ import annotations
 
@@ -35,15 +46,31 @@ from . import formats
 from .rotation import rotate, unrotate
 
 CODEBOOK, FP16, FP8_E4M3, INT4_G32 = "codebook", "fp16", "fp8_e4m3", "int4_g32"
+CODEBOOK_QJL = "codebook_qjl"
+QJL_DIM = formats.QJL_DIM
 
 
 def encode(x16: np.ndarray, s: np.ndarray, fmt: str, bits: int = 0,
-           bounds32: Optional[np.ndarray] = None):
+           bounds32: Optional[np.ndarray] = None, centroids32: Optional[np.ndarray] = None,
+           proj: Optional[np.ndarray] = None):
     """Encode fp16 vectors x16 [..., d] rotated with signs s [d] (broadcastable).
     Returns (rows uint8 [..., row_bytes], aux or None):
-      codebook: aux = fp16 norms [...];  int4_g32: aux = fp16 scales [..., d/32]."""
+      codebook: aux = fp16 norms [...];  int4_g32: aux = fp16 scales [..., d/32];
+      codebook_qjl: aux = fp16 [..., 2] (norm, residual norm); needs centroids32 and
+      the projection proj [m, d] (float32)."""
     d = x16.shape[-1]
     xr = rotate(np.asarray(x16, dtype=np.float64), s)
+    if fmt == CODEBOOK_QJL:
+        # 1. the codebook encode of x~ (codes of `bits` bits, fp16 norm)
+        codes, norm16 = encode(x16, s, CODEBOOK, bits, bounds32)
+        # 2. the residual against what the decoder reconstructs
+        r = xr - decode_rotated(codes, norm16, CODEBOOK, d, bits, centroids32)
+        rnorm16 = formats.to_f16(np.sqrt(np.sum(r * r, axis=-1)))
+        # 3. signs of the projection, decided on the float32 value: z_j = 1 <=> (S r)_j >= 0
+        sr = formats.to_f32(r @ np.asarray(proj, dtype=np.float32).astype(np.float64).T)
+        zbits = (sr >= 0).astype(np.int64)
+        rows = np.concatenate([codes, formats.pack_bits(zbits, 1)], axis=-1)
+        return rows, np.stack([norm16, rnorm16], axis=-1)
     if fmt == CODEBOOK:
         n = np.sqrt(np.sum(xr * xr, axis=-1))
         norm16 = formats.to_f16(n)
@@ -66,6 +93,9 @@ def decode_rotated(rows: np.ndarray, aux, fmt: str, d: int, bits: int = 0,
                    centroids32: Optional[np.ndarray] = None) -> np.ndarray:
     """Stored rows -> the dequantised vector in the rotated domain (float64 [..., d])."""
     rows = np.asarray(rows, dtype=np.uint8)
+    if fmt == CODEBOOK_QJL:  # the codebook part; qjl_correction() adds the sketch's term
+        nb = (d * bits + 7) // 8
+        return decode_rotated(rows[..., :nb], np.asarray(aux)[..., 0], CODEBOOK, d, bits, centroids32)
     if fmt == CODEBOOK:
         idx = formats.unpack_bits(rows, bits, d)
         c = np.asarray(centroids32, dtype=np.float32).astype(np.float64)
@@ -77,6 +107,21 @@ def decode_rotated(rows: np.ndarray, aux, fmt: str, d: int, bits: int = 0,
     if fmt == INT4_G32:
         return formats.int4_g32_decode(formats.unpack_bits(rows, 4, d), aux)
     raise ValueError(fmt)
+
+
+def qjl_correction(rows: np.ndarray, aux, q_rot: np.ndarray, proj: np.ndarray, d: int, bits: int) -> np.ndarray:
+    """The sketch's estimate of <q~, r~> for stored codebook_qjl rows [..., row_bytes] and a
+    rotated query q_rot [d]:  ||r~|| * sqrt(pi/2) / m * sum_j z_j <S_j, q~>,  z_j = +-1.
+
+    VeloxQuant-MLX page, "Stage 3": the correction is unbiased.  For S_j ~ N(0, I),
+    E[sign(<S_j, r>) <S_j, q>] = sqrt(2/pi) <q, r> / ||r||, so this is the unbiased
+    estimator of that construction (the page's printed factor reads pi/(2m) and puts a
+    sign on <S_j, q>; that form is neither unbiased nor proportional to ||q||)."""
+    nb = (d * bits + 7) // 8
+    z = 2.0 * formats.unpack_bits(np.asarray(rows, dtype=np.uint8)[..., nb:], 1, QJL_DIM).astype(np.float64) - 1.0
+    sq = np.asarray(proj, dtype=np.float32).astype(np.float64) @ np.asarray(q_rot, dtype=np.float64)
+    rnorm = np.asarray(aux, dtype=np.float64)[..., 1]
+    return rnorm * math.sqrt(math.pi / 2.0) / QJL_DIM * (z @ sq)
 
 
 def decode(rows, aux, fmt, s, d, bits=0, centroids32=None) -> np.ndarray:
@@ -94,18 +139,21 @@ class Side:
     bounds32: Optional[np.ndarray]
     signs: np.ndarray  # int8 [Hkv, d]
     rows: np.ndarray  # uint8 [num_pages, Hkv, page_size, row_bytes]
-    aux: Optional[np.ndarray]  # fp16 [num_pages, Hkv, page_size(, d/32)]
+    aux: Optional[np.ndarray]  # fp16 [num_pages, Hkv, page_size(, d/32 | 2)]
+    proj: Optional[np.ndarray] = None  # float32 [m, d], codebook_qjl keys only
 
 
-def new_side(fmt, bits, centroids32, bounds32, signs, num_pages, num_kv_heads, page_size, d) -> Side:
+def new_side(fmt, bits, centroids32, bounds32, signs, num_pages, num_kv_heads, page_size, d, proj=None) -> Side:
     rb = formats.row_bytes(fmt, bits, d)
     rows = np.zeros((num_pages, num_kv_heads, page_size, rb), dtype=np.uint8)
     aux = None
     if fmt == CODEBOOK:
         aux = np.zeros((num_pages, num_kv_heads, page_size), dtype=np.float16)
+    elif fmt == CODEBOOK_QJL:
+        aux = np.zeros((num_pages, num_kv_heads, page_size, 2), dtype=np.float16)
     elif fmt == INT4_G32:
         aux = np.zeros((num_pages, num_kv_heads, page_size, d // formats.GROUP), dtype=np.float16)
-    return Side(fmt, bits, centroids32, bounds32, signs, rows, aux)
+    return Side(fmt, bits, centroids32, bounds32, signs, rows, aux, proj)
 
 
 def write(side: Side, slots: np.ndarray, x16: np.ndarray, page_size: int) -> None:
@@ -115,7 +163,8 @@ def write(side: Side, slots: np.ndarray, x16: np.ndarray, page_size: int) -> Non
     keep = slots >= 0
     page, off = slots[keep] // page_size, slots[keep] % page_size
     for h in range(x16.shape[1]):
-        rows, aux = encode(x16[keep, h, :], side.signs[h], side.fmt, side.bits, side.bounds32)
+        rows, aux = encode(x16[keep, h, :], side.signs[h], side.fmt, side.bits, side.bounds32, side.centroids32,
+                           side.proj)
         side.rows[page, h, off] = rows
         if side.aux is not None:
             side.aux[page, h, off] = aux

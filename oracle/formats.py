@@ -136,10 +136,15 @@ def unpack_bits(rows: np.ndarray, bits: int, n: int) -> np.ndarray:
     return np.sum(stream << np.arange(bits), axis=-1)
 
 
+QJL_DIM = 128  # sign-sketch dimensions m of the residual correction
+
+
 def row_bytes(fmt: str, bits: int, d: int) -> int:
     """Bytes of one packed row (one token's vector) in the given format."""
     if fmt == "codebook":
         return (d * bits + 7) // 8
+    if fmt == "codebook_qjl":  # codes, then the m sign bits of the residual sketch
+        return (d * bits + 7) // 8 + QJL_DIM // 8
     if fmt == "fp16":
         return 2 * d
     if fmt == "fp8_e4m3":
@@ -150,9 +155,12 @@ def row_bytes(fmt: str, bits: int, d: int) -> int:
 
 
 def aux_bytes(fmt: str, d: int) -> int:
-    """Bytes of per-row side data: fp16 norm (codebook), fp16 scale per 32-group (INT4)."""
+    """Bytes of per-row side data: fp16 norm (codebook), fp16 norm + fp16 residual norm
+    (codebook with residual sketch), fp16 scale per 32-group (INT4)."""
     if fmt == "codebook":
         return 2
+    if fmt == "codebook_qjl":  # fp16 norm, fp16 residual norm
+        return 4
     if fmt == "int4_g32":
         return 2 * (d // GROUP)
     return 0
