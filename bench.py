@@ -245,12 +245,13 @@ def cpu_oracle_run(config: str, steps: int, warmup: int, out_json: str | None = 
     tiers = []
     dec_bytes = 0
     for t, tier in enumerate(cfg.tiers):
-        kt = ocb.tables(tier.codebook, tier.k_bits) if tier.k_format == "codebook" else (None, None)
+        kt = ocb.tables(tier.codebook, tier.k_bits) if tier.k_format.startswith("codebook") else (None, None)
         vt = ocb.tables(tier.codebook, tier.v_bits) if tier.v_format == "codebook" else (None, None)
         tl = np.array([W.tier_lens(cfg, int(n))[t] for n in lens])
         pm = W.page_map(cfg.scaled(batch=nb), tl, tier=t)
         k_side = ocache.new_side(tier.k_format, tier.k_bits, kt[0], kt[1], ks, pm.num_pages, cfg.num_kv_heads,
-                                 cfg.page_size, cfg.head_dim)
+                                 cfg.page_size, cfg.head_dim,
+                                 W.qjl_projection(cfg) if tier.k_format == "codebook_qjl" else None)
         v_side = ocache.new_side(tier.v_format, tier.v_bits, vt[0], vt[1], vs, pm.num_pages, cfg.num_kv_heads,
                                  cfg.page_size, cfg.head_dim)
         tiers.append(oatt.TierState(k_side, v_side, pm.block_table, tl, cfg.page_size))

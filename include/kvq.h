@@ -47,6 +47,7 @@ extern "C" {
 #define KVQ_MAX_TIERS 4  /* decode attends over at most this many tiers at once */
 #define KVQ_MAX_SPLITS 1024  /* split-K chunks per sequence, summed over the tiers */
 #define KVQ_INT4_GROUP 32 /* coordinates sharing one fp16 scale in KVQ_FMT_INT4_G32 */
+#define KVQ_QJL_DIM 128   /* rows m of the residual sketch's projection (KVQ_FMT_CODEBOOK_QJL) */
 
 typedef enum kvq_status {
   KVQ_OK = 0,
@@ -70,12 +71,21 @@ typedef enum kvq_status {
  *                      q = clamp(rint(x~ / s), -7, 7) stored as the nibble q + 8
  *                      (even coordinate in the low nibble); side data: the fp16 scales
  *                      (far-tier values).
+ *   KVQ_FMT_CODEBOOK_QJL (keys only; VeloxQuant-MLX page, "Stage 3: QJL Residual
+ *                      Correction" -- TurboQuantProd): the KVQ_FMT_CODEBOOK row, then
+ *                      KVQ_QJL_DIM sign bits z_j = [ (S r~)_j >= 0 ] of the residual
+ *                      r~ = x~ - (the decoded x~) under the cache's projection S
+ *                      (k_qjl), LSB-first; side data: fp16 [2] = (||x~||, ||r~||).
+ *                      Decode adds ||r~|| sqrt(pi/2) / KVQ_QJL_DIM * sum_j (2 z_j - 1)
+ *                      <S_j, q~> to the key's inner product with the rotated query q~
+ *                      (the unbiased estimator of <q~, r~>).
  * Rounding decisions are taken on float32 values. */
 typedef enum kvq_format {
   KVQ_FMT_CODEBOOK = 0,
   KVQ_FMT_FP16 = 1,
   KVQ_FMT_FP8_E4M3 = 2,
-  KVQ_FMT_INT4_G32 = 3
+  KVQ_FMT_INT4_G32 = 3,
+  KVQ_FMT_CODEBOOK_QJL = 4
 } kvq_format;
 
 /* One tier of a paged cache.  A token of a sequence at position t lives in physical
@@ -83,6 +93,8 @@ typedef enum kvq_format {
  * offset addresses the pool directly.
  *   rows : uint8 [num_pages][num_kv_heads][page_size][row_bytes], 16-byte aligned
  *   aux  : fp16  [num_pages][num_kv_heads][page_size]          (codebook: norms)
+ *          fp16  [num_pages][num_kv_heads][page_size][2]        (codebook + sketch:
+ *                                                                norm, residual norm)
  *          fp16  [num_pages][num_kv_heads][page_size][D/32]     (INT4: group scales)
  *          unused (may be NULL) for fp16 / fp8.
  * row_bytes / aux bytes per row come from kvq_row_bytes().  Codebook tables are fp32:
@@ -97,7 +109,7 @@ typedef struct kvq_cache {
   int32_t num_pages;    /* pages in the pool */
   int32_t k_format;     /* kvq_format of keys   */
   int32_t v_format;     /* kvq_format of values */
-  int32_t k_bits;       /* 2, 3 or 4 when k_format == KVQ_FMT_CODEBOOK, else ignored */
+  int32_t k_bits;       /* 2, 3 or 4 when k_format is a codebook format, else ignored */
   int32_t v_bits;
   void* k_rows;
   void* v_rows;
@@ -109,6 +121,9 @@ typedef struct kvq_cache {
   const float* v_bounds;
   const int8_t* k_signs;
   const int8_t* v_signs;
+  const float* k_qjl;       /* KVQ_FMT_CODEBOOK_QJL keys only: the projection S, fp32
+                               [KVQ_QJL_DIM][head_dim] (iid N(0,1) entries), 16-byte
+                               aligned; the same for every tier attended together */
 } kvq_cache;
 
 /* One tier as seen by a decode call: the cache plus each sequence's pages and length.
@@ -174,7 +189,9 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
  * codebook path -- then a combine pass):
  *   out[b][h] = softmax_t( q[b][h] . K[t] / sqrt(D) ) V[t]
  * over every cached token t < seq_lens[b] of every tier of kv head h / (Hq / Hkv), where
- * K[t], V[t] are the dequantised cache rows with the rotation undone.  The query is
+ * K[t], V[t] are the dequantised cache rows with the rotation undone; keys stored as
+ * KVQ_FMT_CODEBOOK_QJL add their sketch's estimate of <q, r> to q . K[t] (one more small
+ * launch per call projects every query once).  The query is
  * rotated with the K signs inside the kernel and the result is rotated back with the V
  * signs, so the cache is never expanded.  A sequence with no cached token gives zeros.
  *   tiers : host array [num_tiers], 1..KVQ_MAX_TIERS, same head_dim / num_kv_heads

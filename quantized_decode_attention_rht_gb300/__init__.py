@@ -20,8 +20,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
-FMT_CODEBOOK, FMT_FP16, FMT_FP8_E4M3, FMT_INT4_G32 = 0, 1, 2, 3
-FORMATS = {"codebook": FMT_CODEBOOK, "fp16": FMT_FP16, "fp8_e4m3": FMT_FP8_E4M3, "int4_g32": FMT_INT4_G32}
+FMT_CODEBOOK, FMT_FP16, FMT_FP8_E4M3, FMT_INT4_G32, FMT_CODEBOOK_QJL = 0, 1, 2, 3, 4
+FORMATS = {"codebook": FMT_CODEBOOK, "fp16": FMT_FP16, "fp8_e4m3": FMT_FP8_E4M3, "int4_g32": FMT_INT4_G32,
+           "codebook_qjl": FMT_CODEBOOK_QJL}
+QJL_DIM = 128
 MAX_TIERS = 4
 INT4_GROUP = 32
 
@@ -48,6 +50,7 @@ class KvqCache(ctypes.Structure):
         ("k_centroids", ctypes.c_void_p), ("k_bounds", ctypes.c_void_p),
         ("v_centroids", ctypes.c_void_p), ("v_bounds", ctypes.c_void_p),
         ("k_signs", ctypes.c_void_p), ("v_signs", ctypes.c_void_p),
+        ("k_qjl", ctypes.c_void_p),
     ]
 
 
@@ -213,12 +216,14 @@ def kvq_decode_attention_noalloc(tiers, q, out, split_tokens: int = 0, stream=No
 class PagedCache:
     """Owns the device buffers of one tier (torch allocations) and its ``KvqCache`` struct.
 
-    k_format / v_format: "codebook" | "fp16" | "fp8_e4m3" | "int4_g32"; codebook tiers take
-    `k_bits` / `v_bits` and a codebook kind ("lloyd_max" or "uniform") computed by the library.
-    k_signs / v_signs: int8 [Hkv, D] tensors or arrays of +1/-1 (shared by every tier)."""
+    k_format / v_format: "codebook" | "fp16" | "fp8_e4m3" | "int4_g32", and for keys also
+    "codebook_qjl" (codes + residual sign sketch); codebook tiers take `k_bits` / `v_bits` and
+    a codebook kind ("lloyd_max" or "uniform") computed by the library.
+    k_signs / v_signs: int8 [Hkv, D] tensors or arrays of +1/-1 (shared by every tier).
+    k_qjl: float32 [QJL_DIM, D] projection (tensor or array) for "codebook_qjl" keys."""
 
     def __init__(self, head_dim, num_kv_heads, num_pages, k_format, v_format, k_bits=0, v_bits=0,
-                 k_signs=None, v_signs=None, page_size=16, codebook="lloyd_max", device="cuda"):
+                 k_signs=None, v_signs=None, page_size=16, codebook="lloyd_max", device="cuda", k_qjl=None):
         import torch
         self.head_dim, self.num_kv_heads, self.num_pages, self.page_size = head_dim, num_kv_heads, num_pages, page_size
         self.k_format, self.v_format = FORMATS.get(k_format, k_format), FORMATS.get(v_format, v_format)
@@ -232,7 +237,7 @@ class PagedCache:
             if aux:
                 a = torch.zeros((num_pages, num_kv_heads, page_size, aux // 2), dtype=torch.float16, device=dev)
             cent = bnd = None
-            if fmt == FMT_CODEBOOK:
+            if fmt in (FMT_CODEBOOK, FMT_CODEBOOK_QJL):
                 c = (kvq_lloyd_max_codebook if codebook == "lloyd_max" else kvq_uniform_codebook)(bits)[0]
                 c32, b32 = kvq_codebook_tables(bits, c)
                 cent = torch.from_numpy(c32).to(dev)
@@ -243,6 +248,10 @@ class PagedCache:
         self.v_rows, self.v_aux, self.v_centroids, self.v_bounds = side(self.v_format, v_bits)
         self.k_signs = torch.as_tensor(np.asarray(k_signs, dtype=np.int8)).to(dev) if not hasattr(k_signs, "data_ptr") else k_signs
         self.v_signs = torch.as_tensor(np.asarray(v_signs, dtype=np.int8)).to(dev) if not hasattr(v_signs, "data_ptr") else v_signs
+        self.k_qjl = None
+        if k_qjl is not None:
+            self.k_qjl = (k_qjl if hasattr(k_qjl, "data_ptr")
+                          else torch.as_tensor(np.asarray(k_qjl, dtype=np.float32)).to(dev)).contiguous()
         s = KvqCache()
         s.head_dim, s.num_kv_heads, s.page_size, s.num_pages = head_dim, num_kv_heads, page_size, num_pages
         s.k_format, s.v_format, s.k_bits, s.v_bits = self.k_format, self.v_format, k_bits, v_bits
@@ -251,6 +260,7 @@ class PagedCache:
         s.k_centroids, s.k_bounds = _ptr(self.k_centroids), _ptr(self.k_bounds)
         s.v_centroids, s.v_bounds = _ptr(self.v_centroids), _ptr(self.v_bounds)
         s.k_signs, s.v_signs = _ptr(self.k_signs), _ptr(self.v_signs)
+        s.k_qjl = _ptr(self.k_qjl)
         self.struct = s
 
     def append(self, k, v, slot_mapping, stream=None) -> None:

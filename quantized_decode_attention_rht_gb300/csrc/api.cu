@@ -28,6 +28,11 @@ kvq_status side_bytes(int fmt, int bits, int d, size_t* row, size_t* aux) {
       *row = (size_t)d * bits / 8;
       *aux = 2;
       return KVQ_OK;
+    case KVQ_FMT_CODEBOOK_QJL:  // codes, then the sketch's sign bits; norm + residual norm
+      if (bits < 2 || bits > 4) return KVQ_ERR_UNSUPPORTED;
+      *row = (size_t)d * bits / 8 + KVQ_QJL_DIM / 8;
+      *aux = 4;
+      return KVQ_OK;
     case KVQ_FMT_FP16: *row = 2 * (size_t)d; *aux = 0; return KVQ_OK;
     case KVQ_FMT_FP8_E4M3: *row = d; *aux = 0; return KVQ_OK;
     case KVQ_FMT_INT4_G32: *row = d / 2; *aux = 2 * (size_t)(d / KVQ_INT4_GROUP); return KVQ_OK;
@@ -35,14 +40,21 @@ kvq_status side_bytes(int fmt, int bits, int d, size_t* row, size_t* aux) {
   }
 }
 
+bool is_codebook(int fmt) { return fmt == KVQ_FMT_CODEBOOK || fmt == KVQ_FMT_CODEBOOK_QJL; }
+
+// One side of a cache; is_key: the side holds keys (only keys may carry a residual sketch).
 kvq_status check_side(const kvq_cache* c, int fmt, int bits, const void* rows, const void* aux,
-                      const float* cent, const float* bounds, const int8_t* signs, bool need_bounds) {
+                      const float* cent, const float* bounds, const int8_t* signs, bool need_bounds,
+                      bool is_key) {
   size_t rb, ab;
   kvq_status st = side_bytes(fmt, bits, c->head_dim, &rb, &ab);
   if (st != KVQ_OK) return st;
   if (!rows || !aligned(rows, 16) || !signs) return KVQ_ERR_INVALID_ARGUMENT;
   if (ab && (!aux || !aligned(aux, 2))) return KVQ_ERR_INVALID_ARGUMENT;
-  if (fmt == KVQ_FMT_CODEBOOK && (!cent || (need_bounds && !bounds))) return KVQ_ERR_INVALID_ARGUMENT;
+  if (is_codebook(fmt) && (!cent || (need_bounds && !bounds))) return KVQ_ERR_INVALID_ARGUMENT;
+  if (fmt == KVQ_FMT_CODEBOOK_QJL &&
+      (!is_key || !c->k_qjl || !aligned(c->k_qjl, 16) || !aligned(aux, 16)))
+    return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;
 }
 
@@ -144,20 +156,44 @@ kvq_status check_tiers(const kvq_tier_view* tiers, int n, int batch, int hq) {
       return KVQ_ERR_INVALID_ARGUMENT;
     if (!tiers[i].seq_lens) return KVQ_ERR_INVALID_ARGUMENT;
     if ((st = check_side(c, c->k_format, c->k_bits, c->k_rows, c->k_aux, c->k_centroids, c->k_bounds,
-                         c->k_signs, false)) != KVQ_OK)
+                         c->k_signs, false, true)) != KVQ_OK)
       return st;
     if ((st = check_side(c, c->v_format, c->v_bits, c->v_rows, c->v_aux, c->v_centroids, c->v_bounds,
-                         c->v_signs, false)) != KVQ_OK)
+                         c->v_signs, false, false)) != KVQ_OK)
       return st;
-    if (!decode_supports(c->k_format, c->k_bits, c->v_format, c->v_bits)) return KVQ_ERR_UNSUPPORTED;
+    if (c->k_format == KVQ_FMT_CODEBOOK_QJL) {
+      for (int j = 0; j < n; ++j)
+        if (tiers[j].cache->k_format == KVQ_FMT_CODEBOOK_QJL && tiers[j].cache->k_qjl != c->k_qjl)
+          return KVQ_ERR_INVALID_ARGUMENT;  // one projection for every tier attended together
+    } else if (!decode_supports(c->k_format, c->k_bits, c->v_format, c->v_bits)) {
+      return KVQ_ERR_UNSUPPORTED;
+    }
   }
+  // keys with a residual sketch run on the fused codebook kernel only: every tier attended
+  // with them must qualify for it
+  bool sketch = false, all_cb = c0->page_size == 16;
+  for (int i = 0; i < n; ++i) {
+    const kvq_cache* c = tiers[i].cache;
+    sketch = sketch || c->k_format == KVQ_FMT_CODEBOOK_QJL;
+    all_cb = all_cb && cb_fast_supported(c->head_dim, g, c->k_format, c->v_format) && aligned(c->k_aux, 16) &&
+             aligned(c->v_aux, 16);
+  }
+  if (sketch && !all_cb) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
-// Workspace: partial accumulators [B][Hq][S][D], (max, sum) [B][Hq][S][2], work counter.
-size_t workspace_bytes(int batch, int hq, int d, int total_splits) {
+bool has_sketch(const kvq_tier_view* tiers, int n) {
+  for (int i = 0; i < n; ++i)
+    if (tiers[i].cache->k_format == KVQ_FMT_CODEBOOK_QJL) return true;
+  return false;
+}
+
+// Workspace: partial accumulators [B][Hq][S][D], (max, sum) [B][Hq][S][2], with keys that
+// carry a sketch the projected queries [B][Hq][KVQ_QJL_DIM], then the work counters.
+size_t workspace_bytes(int batch, int hq, int d, int total_splits, bool sketch) {
   const size_t parts = (size_t)batch * hq * total_splits;
-  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256) + 256;
+  const size_t pq = sketch ? align_up((size_t)batch * hq * KVQ_QJL_DIM * sizeof(float), 256) : 0;
+  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256) + pq + 256;
 }
 
 }  // namespace
@@ -193,10 +229,10 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
   if ((k && !aligned(k, 16)) || (v && !aligned(v, 16))) return KVQ_ERR_INVALID_ARGUMENT;
   const kvq_cache* c = cache;
   if (k && (st = check_side(c, c->k_format, c->k_bits, c->k_rows, c->k_aux, c->k_centroids, c->k_bounds,
-                            c->k_signs, true)) != KVQ_OK)
+                            c->k_signs, true, true)) != KVQ_OK)
     return st;
   if (v && (st = check_side(c, c->v_format, c->v_bits, c->v_rows, c->v_aux, c->v_centroids, c->v_bounds,
-                            c->v_signs, true)) != KVQ_OK)
+                            c->v_signs, true, false)) != KVQ_OK)
     return st;
   QuantParams p;
   memset(&p, 0, sizeof(p));
@@ -206,11 +242,14 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
   void* rows[2] = {c->k_rows, c->v_rows};
   void* aux[2] = {c->k_aux, c->v_aux};
   const float* bnd[2] = {c->k_bounds, c->v_bounds};
+  const float* cnt[2] = {c->k_centroids, c->v_centroids};
   const int8_t* sg[2] = {c->k_signs, c->v_signs};
   for (int i = 0; i < 2; ++i) {
     p.side[i].rows = static_cast<uint8_t*>(rows[i]);
     p.side[i].aux = static_cast<__half*>(aux[i]);
     p.side[i].bounds = bnd[i];
+    p.side[i].centroids = cnt[i];
+    p.side[i].qjl = i == 0 ? c->k_qjl : nullptr;
     p.side[i].signs = sg[i];
     p.side[i].fmt = fmts[i];
     p.side[i].bits = bits[i];
@@ -236,7 +275,7 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
   if (st != KVQ_OK) return st;
   Plan plan;
   if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, &plan)) != KVQ_OK) return st;
-  *bytes = workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total);
+  *bytes = workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total, has_sketch(tiers, num_tiers));
   return KVQ_OK;
 }
 
@@ -251,7 +290,8 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
   const int d = c0->head_dim, hkv = c0->num_kv_heads;
   Plan plan;
   if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, &plan)) != KVQ_OK) return st;
-  const size_t need = workspace_bytes(batch, num_q_heads, d, plan.total);
+  const bool sketch = has_sketch(tiers, num_tiers);
+  const size_t need = workspace_bytes(batch, num_q_heads, d, plan.total, sketch);
   if (need > 0 && (!workspace || !aligned(workspace, 256))) return KVQ_ERR_INVALID_ARGUMENT;
   if (ws_bytes < need) return KVQ_ERR_WORKSPACE_TOO_SMALL;
 
@@ -267,6 +307,7 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
     t.k_aux = static_cast<const __half*>(c->k_aux);
     t.v_aux = static_cast<const __half*>(c->v_aux);
     t.k_cent = c->k_centroids;
+    t.k_qjl = c->k_qjl;
     t.v_cent = c->v_centroids;
     t.block_table = tiers[i].block_table;
     t.seq_lens = tiers[i].seq_lens;
@@ -289,6 +330,8 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
   const size_t parts = (size_t)batch * num_q_heads * plan.total;
   p.ws_acc = static_cast<float*>(workspace);
   p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(parts * d * sizeof(float), 256));
+  p.ws_pq = sketch ? reinterpret_cast<float*>(reinterpret_cast<char*>(p.ws_ml) + align_up(parts * 2 * sizeof(float), 256))
+                   : nullptr;
   p.batch = batch;
   p.hq = num_q_heads;
   p.hkv = hkv;

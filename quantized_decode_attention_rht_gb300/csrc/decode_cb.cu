@@ -1,845 +1,14 @@
-// Fused decode attention over codebook tiers (b-bit Lloyd-Max or uniform codes + fp16 norm
-// for keys and values), head_dim 128 or 256, 1, 2 or 4 query heads per kv head.
-//
-// The score of a key row is q'.k~ with k~_j = (norm / sqrt(D)) C[idx_j] (TurboQuant page,
-// the dequantisation step; AdapTQ page, "Engineering the Hot Path": the rotated query meets
-// the stored codes directly, through a table of centroids).  Values accumulate in the
-// rotated domain the same way and the combine pass undoes the rotation once.
-//
-// Work: items of (sequence, kv head, chunk of pages), handed to warps from an atomic
-// counter; every warp is independent and writes one split-K partial per item.
-//
-// Pages reach shared memory through a per-warp ring of STAGES slots filled by TMA bulk
-// copies (cp.async.bulk, completion counted in bytes on one mbarrier per slot): one lane
-// issues the four copies of a page block (16 key rows, 16 value rows, their 16 key norms and
-// 16 value norms) into the slot the warp has just read, STAGES pages ahead of their use, and
-// the stream of pages runs on from one item into the next.  Every wait on a slot is bounded.
-//
-// Codes become numbers through tables in shared memory indexed by a pair field (2b bits =
-// two codes, the first code in the low bits).  K and V entries interleave in one region (K
-// at byte 0, V at byte 128 of each 256-byte entry) with 16 lane copies each: a 64-bit shared
-// load is served half a warp at a time, so lanes l and l + 16 can share a copy while the 16
-// lanes of a half-warp always hit 16 different bank pairs.  The region sits at a shared
-// address aligned to its size, so the lookup address of lane l is
-// (field << 8) | ((l & 15) << 3) | base (+128 for V): one byte permute (byte fields) or one
-// shift and one logic op from the packed word.
-//
-// Two paths share that machinery:
-//  * G = 1 (Path1): a matrix-vector product, kept on the FMA pipes.  Lane (t, c) takes
-//    tokens t and t+8 of the page and coordinates [c D/4, (c+1) D/4); a table entry is the
-//    fp32 pair (C[first], C[second]) and feeds one packed fma.rn.f32x2 -- exact fp32
-//    products.  Scores: packed partial dot products summed over the 4 lanes of a token.
-//    Values: packed accumulators per coordinate pair, summed over the 8 lanes of a
-//    coordinate block once per item (a reduce-scatter: each lane ends with D/32 coords).
-//  * G = 2, 4 (PathM): the G heads make a real contraction, done with mma.sync.m16n8k16
-//    (fp16 inputs, fp32 accumulation):
-//        scores  S[16 tokens x 8]  = K~[16 tokens x D] . Q[D x 8]
-//        values  O[16 dims x 8]   += V~^T[16 dims x 16 tokens] . W[16 tokens x 8]
-//    The 8 columns are (head, hi/lo); columns of heads >= G are zero.  Table entries hold
-//    fp16 of 256 C and fp16 of the remainder, so each code pair feeds two mma (hi, lo); the
-//    query and the weights are split the same way, and the products keep ~22 bits.  The
-//    dot product does not care in which order its terms are summed, so lane (g, c) of the
-//    key mma takes the pair slots [c D/8, (c+1) D/8) of rows g and g+8 and the query
-//    fragments follow that order; the value mma maps its A rows g and g+8 of m-tile mt to
-//    the two coordinates of pair slot g D/16 + mt, so one lookup gives both rows and the
-//    lane's output coordinates come out contiguous.  Value fragments pair two tokens per
-//    register, the table pairs two coordinates of one token: two byte permutes per
-//    register pair swap them.
-#include <algorithm>
-#include <cstring>
-
-#include "kvq_internal.cuh"
+// Fused codebook decode: host-side dispatch and the instances for plain codebook keys (the
+// kernels are in decode_cb.cuh; keys with a residual sketch are instantiated in
+// decode_cb_qjl.cu).
+#include "decode_cb.cuh"
 
 namespace kvq {
-namespace {
-
-constexpr int PS = 16;
-constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kCScale = 256.0f;  // fp16 table entries hold 2^8 C
-constexpr float kQScale = 64.0f;   // the rotated queries hold 2^6 q'
-constexpr float kWScale = 8.0f;    // weight fragments hold 2^3 p norm / sqrt(D); with p <= 1
-                                   // every fp16 norm stays below the fp16 maximum
-constexpr int kSpinLimit = 1 << 22;  // try_wait rounds before a slot counts as lost
-constexpr int kErrorWord = 32;       // index of the error word in the counter block
-typedef unsigned long long u64;
-
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-// Table lookups.  Not volatile: once the tables are built a lookup is a plain function of
-// its address, which leaves the compiler free to overlap lookups with arithmetic.  Every
-// lookup address derives from a value pin()ned after the barrier that ends the build.
-__device__ __forceinline__ uint2 lut64(uint32_t a) {
-  uint2 v;
-  asm("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ u64 lut64x(uint32_t a) {
-  u64 v;
-  asm("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ uint32_t pin(uint32_t x) {
-  asm volatile("" : "+r"(x));
-  return x;
-}
-__device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
-  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-// fp16 pair holding either the rounded values (hl = 0) or the rounding remainders (hl = 1)
-__device__ __forceinline__ uint32_t split_pair(float x, float y, float hl) {
-  const uint32_t h = pack_f16x2(x, y);
-  const __half2 hh = *reinterpret_cast<const __half2*>(&h);
-  const float rx = fmaf(-hl, __low2float(hh), x);
-  const float ry = fmaf(-hl, __high2float(hh), y);
-  return pack_f16x2(rx, ry);
-}
-__device__ __forceinline__ u64 pk2(float a, float b) {
-  u64 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void upk2(u64 r, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r)); }
-__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
-  u64 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
-  u64 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ void mbar_init(uint32_t a, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(a), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(mbar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// NBYTES of packed bits at shared address a (4-byte aligned) into words.
-template <int NBYTES>
-__device__ __forceinline__ void lds_run(uint32_t a, uint32_t* w) {
-  if constexpr (NBYTES == 32 || NBYTES == 16) {
-#pragma unroll
-    for (int h = 0; h < NBYTES / 16; ++h)
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(w[4 * h]), "=r"(w[4 * h + 1]), "=r"(w[4 * h + 2]), "=r"(w[4 * h + 3])
-                   : "r"(a + 16 * h));
-  } else if constexpr (NBYTES == 24 || NBYTES == 8) {
-#pragma unroll
-    for (int h = 0; h < NBYTES / 8; ++h)
-      asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(w[2 * h]), "=r"(w[2 * h + 1]) : "r"(a + 8 * h));
-  } else {
-    static_assert(NBYTES == 12 || NBYTES == 4, "unsupported run length");
-#pragma unroll
-    for (int h = 0; h < NBYTES / 4; ++h) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[h]) : "r"(a + 4 * h));
-  }
-}
-__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-
-// ---------------------------------------------------------------- parameters
-struct CbTier {
-  const uint8_t* k_rows;
-  const uint8_t* v_rows;
-  const __half* k_norm;
-  const __half* v_norm;
-  const int32_t* block_table;
-  const int32_t* seq_lens;
-  int max_pages, chunk, nchunks, split_begin;
-};
-
-struct CbParams {
-  CbTier t;
-  const __half* q;
-  const int8_t* k_signs;
-  const float* k_cent;
-  const float* v_cent;
-  float* ws_acc;
-  float* ws_ml;
-  int* counter;  // this launch's work counter
-  int* err;      // error word: set when a wait for a bulk copy gives up
-  int hq, hkv, total_splits, total_items, smem_bytes;
-};
-
-// Shared-memory plan common to both paths: table region (aligned to its size), then per
-// warp a ring of STAGES page slots, a rotated-query buffer and the slot barriers.
-template <int D, int G, int KB, int VB, int WARPS_>
-struct Layout {
-  static constexpr int KROW = D * KB / 8, VROW = D * VB / 8;
-  static constexpr int KBLK = PS * KROW, VBLK = PS * VROW;
-  static constexpr int STAGE = KBLK + VBLK + 64;  // + 16 fp16 key norms + 16 value norms
-  static constexpr int STAGES = 3;
-  static constexpr int WARPS = WARPS_;
-  static constexpr int TABLE = (1 << (2 * (KB > VB ? KB : VB))) * 256;
-  static constexpr int QBUF = G * D * 4;
-  static constexpr int QLINES = G * D * 2 / 128;  // fp16 query rows of the group, in lines
-  static constexpr int WSM = STAGES * STAGE + QBUF + 16 * ((8 * STAGES + 15) / 16);
-  // the table's alignment may leave up to TABLE - 1 bytes before it; warp areas fill that gap
-  // first, so the worst case wastes under one area
-  static constexpr int SMEM = (TABLE + WARPS * WSM + WSM > 2 * TABLE) ? TABLE + WARPS * WSM + WSM : 2 * TABLE;
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
-};
-
-// ---------------------------------------------------------------- bit fields
-
-// Lookup address of the pair field that starts at bit o of the lane's words.  Every call
-// sits in a fully unrolled loop, so o is a constant and the branches fold away.
-template <int BITS2, int NW>
-__device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int o, uint32_t lanebase) {
-  const int i = o / 32, r = o % 32;
-  constexpr uint32_t mask = ((1u << BITS2) - 1u) << 8;
-  if (BITS2 == 8) {
-    // byte r/8 of word i into byte 1; bytes 0, 2, 3 from lanebase (its byte 1 is zero)
-    return __byte_perm(w[i], lanebase, 0x7604 | ((r / 8) << 4));
-  } else if (r + BITS2 <= 32) {
-    const uint32_t x = r >= 8 ? (w[i] >> (r - 8)) : (w[i] << (8 - r));
-    return (x & mask) | lanebase;
-  } else {
-    const uint32_t x = __funnelshift_r(w[i], w[i + 1 < NW ? i + 1 : i], r - 8);
-    return (x & mask) | lanebase;
-  }
-}
-
-// ---------------------------------------------------------------- query rotation
-
-// q' = H (s_K * q) * log2(e) / D * 2^6 for the G heads of kv head hk into qbuf[G][D].
-// Lane l holds coordinates [l*D/32, (l+1)*D/32) of one head at a time: in-register
-// butterfly stages, then five across lanes.
-template <int D, int G>
-__device__ __forceinline__ void rotate_query(const CbParams& p, int b, int hk, float* qbuf, int lane) {
-  constexpr int E = D / 32;
-  const int d0 = lane * E;
-  const int8_t* sg = p.k_signs + hk * D + d0;
-  int8_t s[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) s[e] = sg[e];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const __half* qs = p.q + ((size_t)b * p.hq + hk * G + h) * D + d0;
-    float y[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const float v = __half2float(qs[e]);
-      y[e] = s[e] < 0 ? -v : v;
-    }
-#pragma unroll
-    for (int hs = 1; hs < E; hs <<= 1) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        if ((e & hs) == 0) {
-          const float a = y[e], c = y[e + hs];
-          y[e] = a + c;
-          y[e + hs] = a - c;
-        }
-      }
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float o = __shfl_xor_sync(kFull, y[e], m);
-        y[e] = (lane & m) ? (o - y[e]) : (y[e] + o);
-      }
-    }
-    constexpr float scale = kLog2e / (float)D * kQScale;
-#pragma unroll
-    for (int e = 0; e < E; ++e) qbuf[h * D + d0 + e] = y[e] * scale;
-  }
-}
-
-// ---------------------------------------------------------------- work items, page stream
-
-// A work item: chunk `chunk` of sequence b, kv head hk.  `len` is loaded one item ahead and
-// `btw` holds the block-table entry of page t0/16 + lane of the item.
-struct Item {
-  int b, hk, chunk, t0, len;
-  uint32_t btw;
-};
-
-__device__ __forceinline__ Item fetch_item(const CbParams& p, int item, int lane) {
-  const CbTier& T = p.t;
-  Item it;
-  it.chunk = item % T.nchunks;
-  const int rem = item / T.nchunks;
-  it.hk = rem % p.hkv;
-  it.b = rem / p.hkv;
-  it.t0 = it.chunk * T.chunk;
-  it.len = __ldg(T.seq_lens + it.b);
-  const int pg = it.t0 / PS + lane;
-  it.btw = pg < T.max_pages ? (uint32_t)__ldg(T.block_table + (size_t)it.b * T.max_pages + pg) : 0u;
-  return it;
-}
-
-__device__ __forceinline__ int item_pages(const CbTier& T, const Item& it) {
-  const int t1 = min(it.len, it.t0 + T.chunk);
-  return t1 > it.t0 ? (t1 + PS - 1) / PS - it.t0 / PS : 0;
-}
-
-// A warp's page stream: ring slots, their barriers, and how far it has issued and consumed.
-struct Ring {
-  uint32_t slots, bars;  // shared addresses
-  int issued, consumed;  // stream positions (pages)
-  bool lost;             // a slot wait gave up
-};
-
-template <class L>
-__device__ __forceinline__ void ring_issue(const CbTier& T, int hkv, Ring& rg, uint32_t phys, int hk, int lane) {
-  const int slot = rg.issued % L::STAGES;
-  if (lane == 0) {
-    const uint32_t dst = rg.slots + slot * L::STAGE, bar = rg.bars + 8 * slot;
-    const size_t blk = (size_t)phys * hkv + hk;
-    fence_proxy_async();  // the slot's previous page was read through the generic proxy
-    mbar_expect_tx(bar, L::STAGE);
-    bulk_g2s(dst, T.k_rows + blk * L::KBLK, L::KBLK, bar);
-    bulk_g2s(dst + L::KBLK, T.v_rows + blk * L::VBLK, L::VBLK, bar);
-    bulk_g2s(dst + L::KBLK + L::VBLK, T.k_norm + blk * PS, 32, bar);
-    bulk_g2s(dst + L::KBLK + L::VBLK + 32, T.v_norm + blk * PS, 32, bar);
-  }
-  ++rg.issued;
-}
-
-// Wait until the next page of the stream has landed; returns its slot address.
-template <class L>
-__device__ __forceinline__ uint32_t ring_wait(Ring& rg, int* err) {
-  const int slot = rg.consumed % L::STAGES;
-  const uint32_t parity = (rg.consumed / L::STAGES) & 1;
-  int n = 0;
-  while (!mbar_try_wait(rg.bars + 8 * slot, parity)) {
-    if (++n >= kSpinLimit) {
-      rg.lost = true;
-      atomicExch(err, 1);
-      break;
-    }
-  }
-  return rg.slots + slot * L::STAGE;
-}
-
-// Feeds the pages of an item (and the first pages of the next one) into the ring, STAGES
-// ahead of consumption.  Block-table entries of pages [wbase, wbase + 32) and
-// [wbase + 32, wbase + 64) of the item live one per lane.
-template <class L>
-struct Feeder {
-  const CbTier* T;
-  const int32_t* bt;
-  const Item* nx;
-  uint32_t btw0, btw1;
-  int wbase, start, npg, n_next, hk, hkv, lane;
-
-  __device__ __forceinline__ void init(const CbParams& p, const Item& it, const Item& nxt, int n_pages, int n_nxt,
-                                       const Ring& rg, int ln) {
-    T = &p.t;
-    nx = &nxt;
-    lane = ln;
-    hk = it.hk;
-    hkv = p.hkv;
-    npg = n_pages;
-    n_next = n_nxt;
-    start = rg.consumed;
-    const int pg0 = it.t0 / PS;
-    bt = T->block_table + (size_t)it.b * T->max_pages + pg0;
-    btw0 = it.btw;
-    btw1 = 0u;
-    wbase = 0;
-    if (npg > 32 && pg0 + 32 + lane < T->max_pages) btw1 = (uint32_t)__ldg(bt + 32 + lane);
-  }
-  __device__ __forceinline__ void top_up(Ring& rg) {
-    while (rg.issued < rg.consumed + L::STAGES && rg.issued - start < npg + n_next) {
-      const int o = rg.issued - start;
-      if (o < npg) {
-        if (o - wbase >= 32) {  // slide the window by 32 pages
-          btw0 = btw1;
-          wbase += 32;
-          btw1 = (wbase + 32 + lane < npg) ? (uint32_t)__ldg(bt + wbase + 32 + lane) : 0u;
-        }
-        ring_issue<L>(*T, hkv, rg, __shfl_sync(kFull, btw0, o - wbase), hk, lane);
-      } else {
-        ring_issue<L>(*T, hkv, rg, __shfl_sync(kFull, nx->btw, o - npg), nx->hk, lane);
-      }
-    }
-  }
-};
-
-// ================================================================ G = 1: FMA path
-template <int D, int KB, int VB>
-struct Path1 {
-  using L = Layout<D, 1, KB, VB, D == 128 ? 16 : 8>;
-  static constexpr int kD = D, kG = 1;
-  static constexpr int DL = D / 4;  // coordinates per lane and token
-  static constexpr int NP = DL / 2;  // pair slots per lane and token
-  static constexpr int KBYTES = DL * KB / 8, VBYTES = DL * VB / 8;
-  static constexpr int KW = KBYTES / 4, VW = VBYTES / 4;
-  static constexpr float kInvD = D == 128 ? 0.08838834764831845f : 0.0625f;
-
-  // K and V fp32 pair tables: entry e, lane copy l at base + e*256 + l*8 (K) and +128 (V).
-  __device__ static void build_tables(const float* kc, const float* vc, uint32_t base) {
-    constexpr int NK = 1 << (2 * KB), NV = 1 << (2 * VB), N = NK > NV ? NK : NV;
-    for (int i = threadIdx.x; i < N * 32; i += blockDim.x) {
-      const int e = i >> 5, half = (i >> 4) & 1, ln = i & 15;
-      const int bits = half ? VB : KB;
-      if (e >= (half ? NV : NK)) continue;
-      const float* cent = half ? vc : kc;
-      const int mask = (1 << bits) - 1;
-      sts64(base + e * 256 + half * 128 + ln * 8, __float_as_uint(__ldg(cent + (e & mask))),
-            __float_as_uint(__ldg(cent + (e >> bits))));
-    }
-  }
-
-  __device__ static void run_item(const CbParams& p, const Item& it, bool has_next, const Item& nx, float* qbuf,
-                                  Ring& rg, uint32_t klane, uint32_t vlane, int lane) {
-    const CbTier& T = p.t;
-    const int b = it.b, hk = it.hk;
-    const int t1 = min(it.len, it.t0 + T.chunk);
-    const int pg0 = it.t0 / PS, npg = item_pages(T, it);
-    const int t = lane >> 2, c = lane & 3;
-    Feeder<L> fd;
-    fd.init(p, it, nx, npg, has_next ? item_pages(T, nx) : 0, rg, lane);
-    fd.top_up(rg);
-    rotate_query<D, 1>(p, b, hk, qbuf, lane);
-    __syncwarp();
-    u64 q2[NP], acc[NP];
-    {
-      const uint32_t base = smem_addr(qbuf + DL * c);
-#pragma unroll
-      for (int j = 0; j < NP; j += 2) {
-        const uint4 v = lds128(base + 8 * j);
-        q2[j] = pk2(__uint_as_float(v.x), __uint_as_float(v.y));
-        q2[j + 1] = pk2(__uint_as_float(v.z), __uint_as_float(v.w));
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NP; ++j) acc[j] = 0ull;
-    float m = -INFINITY, l = 0.f;
-    constexpr float sscale = kInvD / kQScale;
-#pragma unroll 1
-    for (int i = 0; i < npg; ++i) {
-      const uint32_t st = ring_wait<L>(rg, p.err);
-      if (rg.lost) return;
-      uint32_t k[2][KW], v[2][VW];
-      lds_run<KBYTES>(st + t * L::KROW + c * KBYTES, k[0]);
-      lds_run<KBYTES>(st + (t + 8) * L::KROW + c * KBYTES, k[1]);
-      lds_run<VBYTES>(st + L::KBLK + t * L::VROW + c * VBYTES, v[0]);
-      lds_run<VBYTES>(st + L::KBLK + (t + 8) * L::VROW + c * VBYTES, v[1]);
-      const uint32_t nrm = st + L::KBLK + L::VBLK + 2 * t;
-      const uint32_t nk0 = lds_u16(nrm), nk1 = lds_u16(nrm + 16), nv0 = lds_u16(nrm + 32), nv1 = lds_u16(nrm + 48);
-      __syncwarp();  // every lane holds its words: the slot may be refilled
-      ++rg.consumed;
-      fd.top_up(rg);
-      const int tok0 = (pg0 + i) * PS;
-      const bool v0 = tok0 + t < t1, v1 = tok0 + t + 8 < t1;
-      // ---- scores of tokens t and t+8
-      u64 s[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int j = 0; j < NP; ++j) {
-        s[j & 1] = fma2(q2[j], lut64x(field_addr<2 * KB>(k[0], 2 * KB * j, klane)), s[j & 1]);
-        s[2 + (j & 1)] = fma2(q2[j], lut64x(field_addr<2 * KB>(k[1], 2 * KB * j, klane)), s[2 + (j & 1)]);
-      }
-      float a0, b0, a1, b1, e0, f0, e1, f1;
-      upk2(s[0], a0, b0);
-      upk2(s[1], e0, f0);
-      upk2(s[2], a1, b1);
-      upk2(s[3], e1, f1);
-      float x0 = (a0 + b0) + (e0 + f0), x1 = (a1 + b1) + (e1 + f1);
-      x0 += __shfl_xor_sync(kFull, x0, 1);
-      x1 += __shfl_xor_sync(kFull, x1, 1);
-      x0 += __shfl_xor_sync(kFull, x0, 2);
-      x1 += __shfl_xor_sync(kFull, x1, 2);
-      x0 = v0 ? x0 * (__half2float(__ushort_as_half((uint16_t)nk0)) * sscale) : -INFINITY;
-      x1 = v1 ? x1 * (__half2float(__ushort_as_half((uint16_t)nk1)) * sscale) : -INFINITY;
-      // ---- online softmax over the 16 tokens
-      float mt = fmaxf(x0, x1);
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
-      if (mt > m) {
-        const float f = exp2f(m - mt);  // m = -inf at first: f = 0
-        l *= f;
-        const u64 f2 = pk2(f, f);
-#pragma unroll
-        for (int j = 0; j < NP; ++j) acc[j] = mul2(acc[j], f2);
-        m = mt;
-      }
-      const float p0 = v0 ? exp2f(x0 - m) : 0.f;
-      const float p1 = v1 ? exp2f(x1 - m) : 0.f;
-      l += p0 + p1;
-      const float w0 = v0 ? p0 * (__half2float(__ushort_as_half((uint16_t)nv0)) * kInvD) : 0.f;
-      const float w1 = v1 ? p1 * (__half2float(__ushort_as_half((uint16_t)nv1)) * kInvD) : 0.f;
-      const u64 W0 = pk2(w0, w0), W1 = pk2(w1, w1);
-      // ---- values of tokens t and t+8
-#pragma unroll
-      for (int j = 0; j < NP; ++j) acc[j] = fma2(W0, lut64x(field_addr<2 * VB>(v[0], 2 * VB * j, vlane)), acc[j]);
-#pragma unroll
-      for (int j = 0; j < NP; ++j) acc[j] = fma2(W1, lut64x(field_addr<2 * VB>(v[1], 2 * VB * j, vlane)), acc[j]);
-    }
-    // ---- sums over the 8 token lanes of a coordinate block: reduce-scatter on lane bits 4, 3, 2
-    float a[DL];
-#pragma unroll
-    for (int j = 0; j < NP; ++j) upk2(acc[j], a[2 * j], a[2 * j + 1]);
-#pragma unroll
-    for (int s2 = 0; s2 < 3; ++s2) {
-      const int msk = 16 >> s2, n = DL >> s2;
-      const bool up = lane & msk;
-#pragma unroll
-      for (int k = 0; k < n / 2; ++k) {
-        const float send = up ? a[k] : a[k + n / 2];
-        const float keep = up ? a[k + n / 2] : a[k];
-        a[k] = keep + __shfl_xor_sync(kFull, send, msk);
-      }
-    }
-    l += __shfl_xor_sync(kFull, l, 4);
-    l += __shfl_xor_sync(kFull, l, 8);
-    l += __shfl_xor_sync(kFull, l, 16);
-    const size_t part = ((size_t)b * p.hq + hk) * p.total_splits + T.split_begin + it.chunk;
-    const int off = DL * c + ((lane >> 4) & 1) * (DL / 2) + ((lane >> 3) & 1) * (DL / 4) + ((lane >> 2) & 1) * (DL / 8);
-    float4* dst = reinterpret_cast<float4*>(p.ws_acc + part * D + off);
-#pragma unroll
-    for (int k = 0; k < DL / 8; k += 4) dst[k / 4] = make_float4(a[k], a[k + 1], a[k + 2], a[k + 3]);
-    if (lane == 0) {
-      p.ws_ml[2 * part] = m;
-      p.ws_ml[2 * part + 1] = l;
-    }
-  }
-};
-
-// ================================================================ G = 2, 4: tensor-core path
-template <int D, int G, int KB, int VB>
-struct PathM {
-  using L = Layout<D, G, KB, VB, D == 128 ? 12 : 8>;
-  static constexpr int kD = D, kG = G;
-  static constexpr int KS = D / 16;            // key mma k-steps; also value m-tiles
-  static constexpr int PPT = D / 8;            // key pair slots per lane (index c)
-  static constexpr int QPT = D / 16;           // value pair slots per lane (index g)
-  static constexpr int KBYTES = PPT * KB / 4;  // key bits of one lane, in bytes
-  static constexpr int VBYTES = QPT * VB / 4;
-  static constexpr int KW = KBYTES / 4;
-  static constexpr bool VODD = (VBYTES % 4) != 0;  // 3-bit values at D = 128: 6 bytes at 6g
-  static constexpr int VW = VODD ? 2 : VBYTES / 4;
-
-  // fp16 hi / remainder tables of 256 C: entry e, lane copy l at base + e*256 + l*8 (K) and
-  // +128 (V) = {fp16x2 hi(256 C[e & mask], 256 C[e >> bits]), fp16x2 remainders}.
-  __device__ static void build_tables(const float* kc, const float* vc, uint32_t base) {
-    constexpr int NK = 1 << (2 * KB), NV = 1 << (2 * VB), N = NK > NV ? NK : NV;
-    for (int i = threadIdx.x; i < N * 32; i += blockDim.x) {
-      const int e = i >> 5, half = (i >> 4) & 1, ln = i & 15;
-      const int bits = half ? VB : KB;
-      if (e >= (half ? NV : NK)) continue;
-      const float* cent = half ? vc : kc;
-      const int mask = (1 << bits) - 1;
-      const float c0 = __ldg(cent + (e & mask)) * kCScale, c1 = __ldg(cent + (e >> bits)) * kCScale;
-      sts64(base + e * 256 + half * 128 + ln * 8, split_pair(c0, c1, 0.f), split_pair(c0, c1, 1.f));
-    }
-  }
-
-  __device__ static void run_item(const CbParams& p, const Item& it, bool has_next, const Item& nx, float* qbuf,
-                                  Ring& rg, uint32_t klane, uint32_t vlane, int lane) {
-    const CbTier& T = p.t;
-    const int b = it.b, hk = it.hk;
-    const int t1 = min(it.len, it.t0 + T.chunk);
-    const int pg0 = it.t0 / PS, npg = item_pages(T, it);
-    const int g = lane >> 2, c = lane & 3;
-    Feeder<L> fd;
-    fd.init(p, it, nx, npg, has_next ? item_pages(T, nx) : 0, rg, lane);
-    fd.top_up(rg);
-    rotate_query<D, G>(p, b, hk, qbuf, lane);
-    __syncwarp();
-    // query B fragments: column g = (head g/2, part g%2); pair slots c*PPT + 2ks (+1)
-    uint32_t qf[KS][2];
-    const int hB = g >> 1;
-    if (hB < G) {
-      const float hl = (float)(g & 1);
-      const uint32_t base = smem_addr(qbuf + hB * D + 2 * PPT * c);
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint4 v = lds128(base + 16 * ks);
-        qf[ks][0] = split_pair(__uint_as_float(v.x), __uint_as_float(v.y), hl);
-        qf[ks][1] = split_pair(__uint_as_float(v.z), __uint_as_float(v.w), hl);
-      }
-    } else {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) qf[ks][0] = qf[ks][1] = 0u;
-    }
-    float acc[KS][4];
-#pragma unroll
-    for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    constexpr float kInvD = D == 128 ? 0.08838834764831845f : 0.0625f;
-    constexpr float sscale = kInvD / (kQScale * kCScale);
-    constexpr float wscale = kWScale * kInvD;
-    const int srcA = 4 * (2 * c) + hB, srcB = srcA + 4;
-    const bool lo_part = g & 1, live_col = hB < G;
-#pragma unroll 1
-    for (int i = 0; i < npg; ++i) {
-      const uint32_t st = ring_wait<L>(rg, p.err);
-      if (rg.lost) return;
-      uint32_t k[2][KW], v[4][VW];
-      lds_run<KBYTES>(st + g * L::KROW + c * KBYTES, k[0]);
-      lds_run<KBYTES>(st + (g + 8) * L::KROW + c * KBYTES, k[1]);
-      const int tok[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-      if constexpr (!VODD) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) lds_run<VBYTES>(st + L::KBLK + tok[r] * L::VROW + g * VBYTES, v[r]);
-      } else {
-        // 6-byte runs at 6g lie in the two 4-byte aligned words from (6g & ~3), inside the
-        // row (a is only 4-byte aligned: two 32-bit loads); shift them down by 16 bits when
-        // g is odd
-        const int off = g * VBYTES, a = off & ~3, sh = 8 * (off - a);
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          uint32_t w[2];
-          lds_run<4>(st + L::KBLK + tok[r] * L::VROW + a, w);
-          lds_run<4>(st + L::KBLK + tok[r] * L::VROW + a + 4, w + 1);
-          v[r][0] = __funnelshift_r(w[0], w[1], sh);
-          v[r][1] = __funnelshift_r(w[1], 0u, sh);
-        }
-      }
-      const uint32_t nrm = st + L::KBLK + L::VBLK + 2 * g;
-      const uint32_t nk0 = lds_u16(nrm), nk1 = lds_u16(nrm + 16), nv0 = lds_u16(nrm + 32), nv1 = lds_u16(nrm + 48);
-      __syncwarp();  // every lane holds its words: the slot may be refilled
-      ++rg.consumed;
-      fd.top_up(rg);
-      // ---- scores of tokens g and g+8 for head c
-      float sa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint2 e0 = lut64(field_addr<2 * KB>(k[0], 2 * KB * (2 * ks), klane));
-        const uint2 e1 = lut64(field_addr<2 * KB>(k[1], 2 * KB * (2 * ks), klane));
-        const uint2 e2 = lut64(field_addr<2 * KB>(k[0], 2 * KB * (2 * ks + 1), klane));
-        const uint2 e3 = lut64(field_addr<2 * KB>(k[1], 2 * KB * (2 * ks + 1), klane));
-        const uint32_t ah[4] = {e0.x, e1.x, e2.x, e3.x}, al[4] = {e0.y, e1.y, e2.y, e3.y};
-        mma16816(sa[0], ah, qf[ks][0], qf[ks][1]);
-        mma16816(sa[1], al, qf[ks][0], qf[ks][1]);
-      }
-      const int tok0 = (pg0 + i) * PS;
-      const bool v0 = tok0 + g < t1, v1 = tok0 + g + 8 < t1;
-      float x0 = ((sa[0][0] + sa[0][1]) + (sa[1][0] + sa[1][1])) *
-                 (__half2float(__ushort_as_half((uint16_t)nk0)) * sscale);
-      float x1 = ((sa[0][2] + sa[0][3]) + (sa[1][2] + sa[1][3])) *
-                 (__half2float(__ushort_as_half((uint16_t)nk1)) * sscale);
-      x0 = v0 ? x0 : -INFINITY;
-      x1 = v1 ? x1 : -INFINITY;
-      // ---- online softmax of head c over the 16 tokens
-      float mt = fmaxf(x0, x1);
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
-      if (mt > m) {
-        const float f = exp2f(m - mt);  // m = -inf at first: f = 0
-        l *= f;
-#pragma unroll
-        for (int a = 0; a < KS; ++a)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) acc[a][kk] *= f;
-        m = mt;
-      }
-      const float p0 = v0 ? exp2f(x0 - m) : 0.f;
-      const float p1 = v1 ? exp2f(x1 - m) : 0.f;
-      l += p0 + p1;
-      // ---- weight B fragments: column g = (head g/2, part g%2), tokens 2c, 2c+1 | 2c+8, 2c+9
-      const float w0 = v0 ? p0 * (__half2float(__ushort_as_half((uint16_t)nv0)) * wscale) : 0.f;
-      const float w1 = v1 ? p1 * (__half2float(__ushort_as_half((uint16_t)nv1)) * wscale) : 0.f;
-      const uint32_t hi = pack_f16x2(w0, w1);
-      const __half2 hh = *reinterpret_cast<const __half2*>(&hi);
-      const uint32_t lo = pack_f16x2(w0 - __low2float(hh), w1 - __high2float(hh));
-      const uint32_t ah = __shfl_sync(kFull, hi, srcA), al = __shfl_sync(kFull, lo, srcA);
-      const uint32_t bh = __shfl_sync(kFull, hi, srcB), bl = __shfl_sync(kFull, lo, srcB);
-      const uint32_t A = lo_part ? al : ah, B = lo_part ? bl : bh;
-      const uint32_t b0 = live_col ? __byte_perm(A, B, 0x5410) : 0u;
-      const uint32_t b1 = live_col ? __byte_perm(A, B, 0x7632) : 0u;
-      // ---- values: m-tile mt covers pair slot g*QPT + mt of the four tokens
-#pragma unroll
-      for (int mt2 = 0; mt2 < KS; ++mt2) {
-        const uint2 r0 = lut64(field_addr<2 * VB>(v[0], 2 * VB * mt2, vlane));
-        const uint2 r1 = lut64(field_addr<2 * VB>(v[1], 2 * VB * mt2, vlane));
-        const uint2 r2 = lut64(field_addr<2 * VB>(v[2], 2 * VB * mt2, vlane));
-        const uint2 r3 = lut64(field_addr<2 * VB>(v[3], 2 * VB * mt2, vlane));
-        const uint32_t ah4[4] = {__byte_perm(r0.x, r1.x, 0x5410), __byte_perm(r0.x, r1.x, 0x7632),
-                                 __byte_perm(r2.x, r3.x, 0x5410), __byte_perm(r2.x, r3.x, 0x7632)};
-        const uint32_t al4[4] = {__byte_perm(r0.y, r1.y, 0x5410), __byte_perm(r0.y, r1.y, 0x7632),
-                                 __byte_perm(r2.y, r3.y, 0x5410), __byte_perm(r2.y, r3.y, 0x7632)};
-        mma16816(acc[mt2], ah4, b0, b1);
-        mma16816(acc[mt2], al4, b0, b1);
-      }
-    }
-    // ---- partial of head c: sum over the 8 lanes of the head, coordinates 2*QPT*g ..
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(kFull, l, o);
-    if (c < G) {
-      const size_t part = ((size_t)b * p.hq + hk * G + c) * p.total_splits + T.split_begin + it.chunk;
-      constexpr float unw = 1.0f / (kWScale * kCScale);
-      float4* dst = reinterpret_cast<float4*>(p.ws_acc + part * D + 2 * QPT * g);
-#pragma unroll
-      for (int a = 0; a < KS; a += 2)
-        dst[a / 2] = make_float4((acc[a][0] + acc[a][1]) * unw, (acc[a][2] + acc[a][3]) * unw,
-                                 (acc[a + 1][0] + acc[a + 1][1]) * unw, (acc[a + 1][2] + acc[a + 1][3]) * unw);
-      if (g == 0) {
-        p.ws_ml[2 * part] = m;
-        p.ws_ml[2 * part + 1] = l;
-      }
-    }
-  }
-};
-
-// ================================================================ the kernel
-template <class P>
-__global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __grid_constant__ CbParams p) {
-  using L = typename P::L;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  // the table sits at a shared address that is a multiple of its size; warp areas fill the
-  // space before it first, then follow it
-  const uint32_t base = smem_addr(smem);
-  const uint32_t a_t = (base + L::TABLE - 1) & ~(uint32_t)(L::TABLE - 1);
-  const int nfit = min(L::WARPS, (int)((a_t - base) / L::WSM));
-  const uint32_t end = nfit == L::WARPS ? a_t + L::TABLE : a_t + L::TABLE + (L::WARPS - nfit) * L::WSM;
-  if (end > base + (uint32_t)p.smem_bytes) return;  // the launcher sizes smem for any base
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t area = warp < nfit ? base + warp * L::WSM : a_t + L::TABLE + (warp - nfit) * L::WSM;
-  Ring rg;
-  rg.slots = area;
-  rg.bars = area + L::STAGES * L::STAGE + L::QBUF;
-  rg.issued = rg.consumed = 0;
-  rg.lost = false;
-  float* qbuf = reinterpret_cast<float*>(smem + (area + L::STAGES * L::STAGE - base));
-  if (lane == 0) {
-    for (int s = 0; s < L::STAGES; ++s) mbar_init(rg.bars + 8 * s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  P::build_tables(p.k_cent, p.v_cent, a_t);
-  __syncthreads();
-  const uint32_t klane = pin(a_t | ((lane & 15) << 3)), vlane = pin(a_t | 128 | ((lane & 15) << 3));
-  // items: the one in hand, the next (its metadata and queries fetched while this one
-  // runs), and the one after (its counter ticket in flight)
-  int item = 0, next = 0;
-  if (lane == 0) {
-    item = atomicAdd(p.counter, 1);
-    next = atomicAdd(p.counter, 1);
-  }
-  item = __shfl_sync(kFull, item, 0);
-  next = __shfl_sync(kFull, next, 0);
-  Item cur = fetch_item(p, item < p.total_items ? item : 0, lane);
-  while (item < p.total_items && !rg.lost) {
-    int after = 0;
-    if (lane == 0) after = atomicAdd(p.counter, 1);
-    const bool has_next = next < p.total_items;
-    Item nx = cur;
-    if (has_next) {
-      nx = fetch_item(p, next, lane);
-      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q + ((size_t)nx.b * p.hq + nx.hk * P::kG) * P::kD);
-      if (lane < L::QLINES) prefetch_l2(qrow + 128 * lane);
-    }
-    if (cur.len > cur.t0) P::run_item(p, cur, has_next, nx, qbuf, rg, klane, vlane, lane);
-    item = next;
-    next = __shfl_sync(kFull, after, 0);
-    cur = nx;
-  }
-  // a warp that gave up on a slot waits (bounded) for whatever it still has in flight
-  if (rg.lost) {
-    for (; rg.consumed < rg.issued; ++rg.consumed) {
-      const int slot = rg.consumed % L::STAGES;
-      const uint32_t parity = (rg.consumed / L::STAGES) & 1;
-      for (int n = 0; n < kSpinLimit && !mbar_try_wait(rg.bars + 8 * slot, parity); ++n) {
-      }
-    }
-  }
-}
-
-template <class P>
-cudaError_t launch_path(const CbParams& p, int sms, cudaStream_t stream) {
-  using L = typename P::L;
-  auto kern = decode_cb_kernel<P>;
-  CbParams q = p;
-  q.smem_bytes = L::SMEM;
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
-  const int ctas = std::max(1, std::min(sms, (p.total_items + 2 * L::WARPS - 1) / (2 * L::WARPS)));
-  kern<<<ctas, L::WARPS * 32, L::SMEM, stream>>>(q);
-  e = cudaGetLastError();
-  if (e == cudaSuccess) note_launch();
-  return e;
-}
-
-template <int D, int G, int KB, int VB>
-cudaError_t launch_bits(const CbParams& p, int sms, cudaStream_t s) {
-  if constexpr (G == 1) return launch_path<Path1<D, KB, VB>>(p, sms, s);
-  else return launch_path<PathM<D, G, KB, VB>>(p, sms, s);
-}
-
-template <int D, int G, int KB>
-cudaError_t launch_vb(const CbParams& p, int vb, int sms, cudaStream_t s) {
-  switch (vb) {
-    case 2: return launch_bits<D, G, KB, 2>(p, sms, s);
-    case 3: return launch_bits<D, G, KB, 3>(p, sms, s);
-    default: return launch_bits<D, G, KB, 4>(p, sms, s);
-  }
-}
-
-template <int D, int G>
-cudaError_t launch_kb(const CbParams& p, int kb, int vb, int sms, cudaStream_t s) {
-  switch (kb) {
-    case 2: return launch_vb<D, G, 2>(p, vb, sms, s);
-    case 3: return launch_vb<D, G, 3>(p, vb, sms, s);
-    default: return launch_vb<D, G, 4>(p, vb, sms, s);
-  }
-}
-
-template <int D>
-cudaError_t launch_g(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s) {
-  switch (g) {
-    case 1: return launch_kb<D, 1>(p, kb, vb, sms, s);
-    case 2: return launch_kb<D, 2>(p, kb, vb, sms, s);
-    default: return launch_kb<D, 4>(p, kb, vb, sms, s);
-  }
-}
-
-}  // namespace
 
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
   return (head_dim == 128 || head_dim == 256) && (group == 1 || group == 2 || group == 4) &&
-         k_fmt == KVQ_FMT_CODEBOOK && v_fmt == KVQ_FMT_CODEBOOK;
+         v_fmt == KVQ_FMT_CODEBOOK &&
+         (k_fmt == KVQ_FMT_CODEBOOK || (k_fmt == KVQ_FMT_CODEBOOK_QJL && head_dim == 128));
 }
 
 cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, cudaStream_t stream) {
@@ -850,13 +19,15 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
   e = cudaMemsetAsync(counters, 0, 64 * sizeof(int), stream);  // work counters and the error word
   if (e != cudaSuccess) return e;
   const int group = dp.hq / dp.hkv;
+  bool projected = false;  // every sketched tier shares the projection and the queries
   for (int i = 0; i < dp.num_tiers; ++i) {
     const DecTier& t = dp.tier[i];
-    CbParams p;
+    cbk::CbParams p;
     memset(&p, 0, sizeof(p));
     p.t.k_rows = t.k_rows;
     p.t.v_rows = t.v_rows;
     p.t.k_norm = t.k_aux;
+    p.t.qjl = t.k_qjl;
     p.t.v_norm = t.v_aux;
     p.t.block_table = t.block_table;
     p.t.seq_lens = t.seq_lens;
@@ -870,15 +41,21 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.v_cent = t.v_cent;
     p.ws_acc = dp.ws_acc;
     p.ws_ml = dp.ws_ml;
+    p.pq = dp.ws_pq;
     p.counter = counters + i;
-    p.err = counters + kErrorWord;
+    p.err = counters + cbk::kErrorWord;
     p.hq = dp.hq;
     p.hkv = dp.hkv;
     p.total_splits = dp.total_splits;
     p.total_items = dp.batch * dp.hkv * t.num_splits;
     if (p.total_items == 0) continue;
-    e = head_dim == 128 ? launch_g<128>(p, group, t.k_bits, t.v_bits, sms, stream)
-                        : launch_g<256>(p, group, t.k_bits, t.v_bits, sms, stream);
+    if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL && !projected) {
+      if ((e = cbk::launch_project_qjl(p, group, dp.batch, stream)) != cudaSuccess) return e;
+      projected = true;
+    }
+    if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL) e = cbk::launch_cb_qjl(p, group, t.k_bits, t.v_bits, sms, stream);
+    else if (head_dim == 128) e = cbk::launch_g<128, false>(p, group, t.k_bits, t.v_bits, sms, stream);
+    else e = cbk::launch_g<256, false>(p, group, t.k_bits, t.v_bits, sms, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

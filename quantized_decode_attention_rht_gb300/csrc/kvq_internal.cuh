@@ -20,7 +20,9 @@ struct QuantSide {
   uint8_t* rows;
   __half* aux;
   const float* bounds;
+  const float* centroids;
   const int8_t* signs;
+  const float* qjl;  // KVQ_FMT_CODEBOOK_QJL: projection [KVQ_QJL_DIM][D]
   int fmt, bits, row_bytes;
 };
 
@@ -43,6 +45,7 @@ struct DecTier {
   const __half* v_aux;
   const float* k_cent;
   const float* v_cent;
+  const float* k_qjl;  // KVQ_FMT_CODEBOOK_QJL keys: projection [KVQ_QJL_DIM][D]
   const int32_t* block_table;
   const int32_t* seq_lens;
   int k_fmt, v_fmt, k_bits, v_bits, k_row_bytes, v_row_bytes;
@@ -58,6 +61,7 @@ struct DecParams {
   float* out;
   float* ws_acc;  // [B][Hq][S][D]
   float* ws_ml;   // [B][Hq][S][2]  (running max in log2 units, sum of exp2)
+  float* ws_pq;   // [B][Hq][KVQ_QJL_DIM] projected queries when a tier's keys carry a sketch
   int batch, hq, hkv, page_size, total_splits;
 };
 
@@ -69,7 +73,8 @@ bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
 int gqa_max_chunk_tokens();
 cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t stream);
 // Fused tensor-core decode over codebook tiers (codebook K and V), head_dim 128 or 256,
-// 1, 2 or 4 query heads per kv head; one launch per tier.  `counters` is 64 ints (256 bytes)
+// 1, 2 or 4 query heads per kv head; one launch per tier (after one projection launch when
+// a tier's keys carry a sketch).  `counters` is 64 ints (256 bytes)
 // of device scratch, cleared by the launcher: one work counter per tier, and at index 32 an
 // error word that a kernel sets when a wait for its own bulk copies gives up.
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);

@@ -1,0 +1,275 @@
+// Quantise-and-append for small appends (a decode step's new token of every sequence): one
+// warp per vector, D / 32 neighbouring coordinates per lane.
+//
+// The per-thread kernel of quantize.cuh keeps 64 coordinates of a vector in one thread's
+// registers, which is what a prefill chunk of millions of vectors wants; a few hundred
+// vectors then occupy a handful of SMs whose warps wait on one long, cold instruction
+// stream (and, for keys with a residual sketch, on 16 K multiply-adds per thread).  Here a
+// vector's work is spread over a warp: the rotation takes log2(D / 32) register stages and
+// five shuffle stages, the norms are warp sums, the codes are packed through a per-warp
+// shared buffer, and the residual sketch is a coalesced pass over the projection rows with
+// a reduce-scatter.  Same steps, same stored bytes, and the same float32 decisions as the
+// per-thread kernel (VeloxQuant-MLX page, "Stage 1", "Stage 2", "Stage 3" and "The
+// Bit-Packing Problem"; FoveatedKV page, "The VR headset thing").
+#include "quantize.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 8;  // warps (vectors in flight) per block
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, m);
+  return x;  // fp32 addition commutes: every lane ends with the same value
+}
+
+// y = H (s * x) (unnormalised) for the lane's coordinates [lane * E, lane * E + E).
+template <int E>
+__device__ __forceinline__ void load_rotate(const uint16_t* src, const int8_t* sg, int lane, float (&y)[E]) {
+  uint32_t xw[E / 2], sw[E / 4];
+  if constexpr (E == 4) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src) + lane);
+    xw[0] = u.x;
+    xw[1] = u.y;
+    sw[0] = __ldg(reinterpret_cast<const uint32_t*>(sg) + lane);
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+    xw[0] = u.x;
+    xw[1] = u.y;
+    xw[2] = u.z;
+    xw[3] = u.w;
+    const uint2 s2 = __ldg(reinterpret_cast<const uint2*>(sg) + lane);
+    sw[0] = s2.x;
+    sw[1] = s2.y;
+  }
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) {
+    // sign bytes 2k, 2k+1 (int8 +-1: bit 7 set for -1) -> fp16 sign bits 15, 31
+    const uint32_t m = __byte_perm(sw[k >> 1], 0, (k & 1) ? 0x3424 : 0x1404) & 0x80008000u;
+    const uint32_t xv = xw[k] ^ m;
+    const __half2 h2 = *reinterpret_cast<const __half2*>(&xv);
+    y[2 * k] = __low2float(h2);
+    y[2 * k + 1] = __high2float(h2);
+  }
+#pragma unroll
+  for (int hs = 1; hs < E; hs <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & hs) == 0) {
+        const float a = y[e], c = y[e + hs];
+        y[e] = a + c;
+        y[e + hs] = a - c;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;  // upper lane keeps partner - own
+#pragma unroll
+    for (int e = 0; e < E; ++e) y[e] = fmaf(sgn, y[e], __shfl_xor_sync(0xFFFFFFFFu, y[e], m));
+  }
+}
+
+// The lane's E fields of `bits` bits each (coordinate order) into the row's little-endian
+// bit stream; `buf` is the warp's shared staging area (D * bits / 32 words).
+template <int D, int E, int BITS>
+__device__ __forceinline__ void store_fields(uint32_t* buf, uint32_t fields, uint8_t* row, int lane) {
+  constexpr int W = D * BITS / 32;
+  __syncwarp();  // the previous vector's words have been read
+  if (lane < W) buf[lane] = 0u;
+  __syncwarp();
+  const int off = lane * E * BITS, w0 = off / 32, sh = off % 32;
+  atomicOr(buf + w0, fields << sh);
+  if (sh + E * BITS > 32) atomicOr(buf + w0 + 1, fields >> (32 - sh));
+  __syncwarp();
+  static_assert(W % 4 == 0, "rows are whole 16-byte units");
+  if (lane < W / 4) reinterpret_cast<uint4*>(row)[lane] = reinterpret_cast<const uint4*>(buf)[lane];
+}
+
+// Residual sign sketch: z_j = [ (S r)_j >= 0 ], j < KVQ_QJL_DIM, as four 32-bit words.  The
+// lane's partial dot products of 32 rows at a time are reduce-scattered over the warp so
+// lane l ends with row 32k + l, and a ballot gathers the signs.
+template <int D, int E>
+__device__ __forceinline__ uint4 sketch_words(const float* __restrict__ proj, const float (&r)[E], int lane) {
+  uint32_t zw[KVQ_QJL_DIM / 32];
+#pragma unroll 1
+  for (int k = 0; k < KVQ_QJL_DIM / 32; ++k) {
+    float a[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const float4* srow = reinterpret_cast<const float4*>(proj + (size_t)(32 * k + t) * D + lane * E);
+      float s = 0.f;
+#pragma unroll
+      for (int q = 0; q < E / 4; ++q) {
+        const float4 v = __ldg(srow + q);
+        s = fmaf(v.x, r[4 * q], s);
+        s = fmaf(v.y, r[4 * q + 1], s);
+        s = fmaf(v.z, r[4 * q + 2], s);
+        s = fmaf(v.w, r[4 * q + 3], s);
+      }
+      a[t] = s;
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < 5; ++s2) {
+      const int msk = 16 >> s2, n = 32 >> s2;
+      const bool up = lane & msk;
+#pragma unroll
+      for (int q = 0; q < n / 2; ++q) {
+        const float send = up ? a[q] : a[q + n / 2];
+        const float keep = up ? a[q + n / 2] : a[q];
+        a[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, msk);
+      }
+    }
+    zw[k] = __ballot_sync(0xFFFFFFFFu, a[0] >= 0.f);
+  }
+  return make_uint4(zw[0], zw[1], zw[2], zw[3]);
+}
+
+template <int D, int FMT, int BITS>
+__device__ __forceinline__ void append_side(const QuantParams& p, const QuantSide& side, const uint16_t* x,
+                                            uint32_t* buf) {
+  constexpr int E = D / 32;
+  constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
+  constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
+  constexpr int NB = (FMT == F_CB || FMT == F_CBQ) ? (1 << BITS) - 1 : 1;
+  const int lane = threadIdx.x & 31;
+  float bnd[NB];
+  if constexpr (FMT == F_CB || FMT == F_CBQ) {
+#pragma unroll
+    for (int i = 0; i < NB; ++i) bnd[i] = __ldg(side.bounds + i);
+  }
+  const int nvec = p.num_tokens * p.hkv;
+  for (int v = blockIdx.x * kWarps + (threadIdx.x >> 5); v < nvec; v += gridDim.x * kWarps) {
+    const int token = v / p.hkv, h = v - token * p.hkv;
+    const int slot = p.slots[token];
+    if (slot < 0 || slot >= p.num_slots) continue;  // warp-uniform
+    float y[E];
+    load_rotate<E>(x + (size_t)v * D, side.signs + (size_t)h * D, lane, y);
+    const size_t prow = ((size_t)(slot / p.page_size) * p.hkv + h) * p.page_size + (slot % p.page_size);
+    uint8_t* row = side.rows + prow * side.row_bytes;
+    if constexpr (FMT == F_CB || FMT == F_CBQ) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss = fmaf(y[e], y[e], ss);
+      const float ny = sqrtf(warp_sum(ss));
+      const float inv = ny > 0.0f ? sqrt_d / ny : 0.0f;  // u = sqrt(D) y / ||y||
+      const __half norm16 = __float2half_rn(ny * inv_sqrt_d);
+      uint32_t fields = 0u;
+      int idx[E];
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float u = y[e] * inv;
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < NB; ++i) c += u > bnd[i] ? 1 : 0;
+        idx[e] = c;
+        fields |= (uint32_t)c << (e * BITS);
+      }
+      store_fields<D, E, BITS>(buf, fields, row, lane);
+      if constexpr (FMT == F_CB) {
+        if (lane == 0) side.aux[prow] = norm16;
+      } else {
+        // y <- the rotated residual x~ - x^~ against the decoded vector (stored fp16 norm)
+        const float dscale = __half2float(norm16) * inv_sqrt_d;
+        float rs = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          y[e] = fmaf(-dscale, __ldg(side.centroids + idx[e]), y[e] * inv_sqrt_d);
+          rs = fmaf(y[e], y[e], rs);
+        }
+        const float rn = sqrtf(warp_sum(rs));
+        const uint4 z = sketch_words<D, E>(side.qjl, y, lane);
+        if (lane == 0) {
+          *reinterpret_cast<uint4*>(row + D * BITS / 8) = z;
+          reinterpret_cast<__half2*>(side.aux)[prow] = __halves2half2(norm16, __float2half_rn(rn));
+        }
+      }
+    } else if constexpr (FMT == F_F16) {
+      uint32_t w[E / 2];
+#pragma unroll
+      for (int k = 0; k < E / 2; ++k) {
+        const __half2 h2 = __floats2half2_rn(y[2 * k] * inv_sqrt_d, y[2 * k + 1] * inv_sqrt_d);
+        w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      if constexpr (E == 4) reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
+      else reinterpret_cast<uint4*>(row)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (FMT == F_F8) {
+      uint32_t w[E / 4];
+#pragma unroll
+      for (int k = 0; k < E / 4; ++k) {
+        const int e = 4 * k;
+        w[k] = float2_to_fp8x2(y[e] * inv_sqrt_d, y[e + 1] * inv_sqrt_d) |
+               (float2_to_fp8x2(y[e + 2] * inv_sqrt_d, y[e + 3] * inv_sqrt_d) << 16);
+      }
+      if constexpr (E == 4) reinterpret_cast<uint32_t*>(row)[lane] = w[0];
+      else reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
+    } else {  // F_I4: a group of 32 coordinates spans 32 / E neighbouring lanes
+      constexpr int LG = kGroup / E;
+      float amax = 0.0f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e] * inv_sqrt_d));
+#pragma unroll
+      for (int m = 1; m < LG; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
+      const __half s16 = __float2half_rn(amax / 7.0f);
+      const float s = __half2float(s16);
+      const float rcp = s > 0.0f ? 1.0f / s : 0.0f;
+      uint32_t nib = 0u;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float xv = y[e] * inv_sqrt_d;
+        // level = rint(x / s): x * (1/s) is within one ulp of the quotient; where that
+        // leaves the result next to a half-integer, divide exactly
+        float tq = xv * rcp;
+        if (s > 0.0f && fabsf(fabsf(tq - rintf(tq)) - 0.5f) < 1e-5f) tq = xv / s;
+        const float q = s > 0.0f ? fminf(fmaxf(rintf(tq), -7.0f), 7.0f) : 0.0f;
+        nib |= (uint32_t)((int)q + 8) << (4 * e);
+      }
+      if constexpr (E == 4) reinterpret_cast<uint16_t*>(row)[lane] = (uint16_t)nib;
+      else reinterpret_cast<uint32_t*>(row)[lane] = nib;
+      if (lane % LG == 0) side.aux[prow * (D / kGroup) + lane / LG] = s16;
+    }
+  }
+}
+
+template <int D, int FMT>
+__device__ __forceinline__ void append_bits(const QuantParams& p, const QuantSide& side, const uint16_t* x,
+                                            uint32_t* buf) {
+  if (side.bits == 4) append_side<D, FMT, 4>(p, side, x, buf);
+  else if (side.bits == 3) append_side<D, FMT, 3>(p, side, x, buf);
+  else append_side<D, FMT, 2>(p, side, x, buf);
+}
+
+// Grid row blockIdx.y = side kind_first + y; the format is a warp-uniform branch (only the
+// taken path's instructions are fetched).
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) append_kernel(const QuantParams p) {
+  __shared__ __align__(16) uint32_t words[kWarps][32];
+  const int kind = p.kind_first + blockIdx.y;  // 0 or 1
+  const QuantSide side = kind ? p.side[1] : p.side[0];
+  const uint16_t* x = kind ? p.x[1] : p.x[0];
+  uint32_t* buf = words[threadIdx.x >> 5];
+  switch (side.fmt) {
+    case KVQ_FMT_CODEBOOK: append_bits<D, F_CB>(p, side, x, buf); break;
+    case KVQ_FMT_CODEBOOK_QJL: append_bits<D, F_CBQ>(p, side, x, buf); break;
+    case KVQ_FMT_FP16: append_side<D, F_F16, 0>(p, side, x, buf); break;
+    case KVQ_FMT_FP8_E4M3: append_side<D, F_F8, 0>(p, side, x, buf); break;
+    default: append_side<D, F_I4, 0>(p, side, x, buf); break;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_small(const QuantParams& p, int head_dim, int sms, cudaStream_t stream) {
+  const long long nvec = (long long)p.num_tokens * p.hkv;
+  const unsigned blocks =
+      (unsigned)std::max<long long>(1, std::min<long long>((nvec + kWarps - 1) / kWarps, (long long)sms * 8));
+  const dim3 grid(blocks, p.num_kinds);
+  if (head_dim == 128) append_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
+  else append_kernel<256><<<grid, kWarps * 32, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
+}  // namespace kvq

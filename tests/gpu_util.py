@@ -105,6 +105,40 @@ def check_codebook_codes(x16, signs, bits, rows_gpu, norms_gpu, kind="lloyd_max"
     return int(np.sum(bad)), int(np.sum(near)), idx_o.size, int(np.sum(diff))
 
 
+def check_qjl_rows(x16, signs, bits, proj, rows_gpu, aux_gpu, kind="lloyd_max"):
+    """Keys with a residual sign sketch: x16 [T, d] of one head, proj float32 [m, d];
+    rows_gpu [T, row_bytes]; aux_gpu fp16 [T, 2].
+
+    The codes and the norm follow the codebook criteria.  Where both agree with the
+    oracle, the residual is the same vector up to float32 rounding, so the residual norm
+    may differ by at most one fp16 ulp and a sign bit only where |<S_j, r~>| lies within
+    the float32 error of the kernel's residual and dot product:
+    1e-5 * sum_i |S_ji| (|r~_i| + |x~_i|), far above (log2 d + 4) 2^-24 of that sum.
+    Rows whose codes or norm differ carry a different residual and are checked only for
+    their codes.  Returns (rows compared, sign bits differing, residual norms differing)."""
+    c32, b32 = tables(kind, bits)
+    d = x16.shape[-1]
+    nb = d * bits // 8
+    aux_gpu = np.asarray(aux_gpu, dtype=np.float16)
+    check_codebook_codes(x16, signs, bits, rows_gpu[:, :nb], aux_gpu[:, 0], kind)
+    rows_o, aux_o = ocache.encode(x16, signs, "codebook_qjl", bits, b32, c32, proj)
+    same = np.all(rows_gpu[:, :nb] == rows_o[:, :nb], axis=-1) & (aux_gpu[:, 0] == aux_o[:, 0])
+    xr = orot.rotate(x16.astype(np.float64), signs)
+    r = xr - ocache.decode_rotated(rows_o, aux_o, "codebook_qjl", d, bits, c32)
+    s64 = np.asarray(proj, dtype=np.float32).astype(np.float64)
+    sr = r @ s64.T
+    tol = 1e-5 * (np.abs(r) + np.abs(xr)) @ np.abs(s64).T
+    z_o = ofmt.unpack_bits(rows_o[:, nb:], 1, ocache.QJL_DIM)
+    z_g = ofmt.unpack_bits(rows_gpu[:, nb:], 1, ocache.QJL_DIM)
+    bad = (z_o != z_g) & same[:, None]
+    assert not np.any(bad & (np.abs(sr) > tol)), "sign bits differ away from zero"
+    ug = aux_gpu[:, 1].view(np.uint16).astype(np.int64)
+    uo = np.asarray(aux_o[:, 1], dtype=np.float16).view(np.uint16).astype(np.int64)
+    rdiff = (ug != uo) & same
+    assert np.all(np.abs(ug - uo)[rdiff] == 1), "residual norms differ by more than one fp16 ulp"
+    return int(np.sum(same)), int(np.sum(bad)), int(np.sum(rdiff))
+
+
 def check_float_rows(x16, signs, fmt, rows_gpu):
     """fp16 / fp8 rows: every stored value must be the format's rounding of SOME value within
     the kernel's rotation error tau of the exact rotated coordinate, i.e. lie between the
@@ -169,7 +203,7 @@ class Built:
         self.ora, self.gpu, self.views, self.k_signs, self.v_signs = ora_tiers, gpu_caches, views, k_signs, v_signs
 
 
-def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16, shuffle_seed=None):
+def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16, shuffle_seed=None, k_qjl=None):
     """tier_specs: list of workloads.Tier; tier_kv: per tier, per sequence, (k [L, Hkv, D], v)
     fp16.  The ORACLE encodes every row into numpy pools; those bytes are uploaded into the
     GPU caches unchanged.  Returns Built."""
@@ -190,9 +224,10 @@ def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16,
         for b, n in enumerate(per):
             bt[b, :n] = phys[at: at + n]
             at += n
-        kc = tables(spec.codebook, spec.k_bits) if spec.k_format == "codebook" else (None, None)
+        kc = tables(spec.codebook, spec.k_bits) if spec.k_format in ("codebook", "codebook_qjl") else (None, None)
         vc = tables(spec.codebook, spec.v_bits) if spec.v_format == "codebook" else (None, None)
-        ks = ocache.new_side(spec.k_format, spec.k_bits, kc[0], kc[1], k_signs, num_pages, hkv, page_size, d)
+        proj = k_qjl if spec.k_format == "codebook_qjl" else None
+        ks = ocache.new_side(spec.k_format, spec.k_bits, kc[0], kc[1], k_signs, num_pages, hkv, page_size, d, proj)
         vs = ocache.new_side(spec.v_format, spec.v_bits, vc[0], vc[1], v_signs, num_pages, hkv, page_size, d)
         for b, (k, v) in enumerate(seqs):
             t = np.arange(k.shape[0])
@@ -201,7 +236,7 @@ def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16,
             ocache.write(vs, slots, v, page_size)
         ora_tiers.append(oatt.TierState(ks, vs, bt, lens, page_size))
         c = kvq.PagedCache(d, hkv, num_pages, spec.k_format, spec.v_format, spec.k_bits, spec.v_bits,
-                           ks_dev, vs_dev, page_size, spec.codebook)
+                           ks_dev, vs_dev, page_size, spec.codebook, k_qjl=proj)
         c.k_rows.copy_(torch.from_numpy(ks.rows))
         c.v_rows.copy_(torch.from_numpy(vs.rows))
         if ks.aux is not None:

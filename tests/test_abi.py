@@ -54,8 +54,8 @@ def test_status_strings(kvq):
 
 @pytest.mark.parametrize("d", [128, 256])
 def test_row_bytes_match_oracle(kvq, d):
-    for fmt in ("codebook", "fp16", "fp8_e4m3", "int4_g32"):
-        for bits in ((2, 3, 4) if fmt == "codebook" else (0,)):
+    for fmt in ("codebook", "codebook_qjl", "fp16", "fp8_e4m3", "int4_g32"):
+        for bits in ((2, 3, 4) if fmt.startswith("codebook") else (0,)):
             assert kvq.kvq_row_bytes(fmt, bits, d) == (ofmt.row_bytes(fmt, bits, d), ofmt.aux_bytes(fmt, d))
     with pytest.raises(kvq.KvqError):
         kvq.kvq_row_bytes("codebook", 5, d)
@@ -162,3 +162,30 @@ def test_workspace_size_formula(kvq):
     # partial accumulators + (max, sum) pairs, each rounded up to 256 B, + 256 B work counter
     want = -(-parts * 128 * 4 // 256) * 256 + -(-parts * 2 * 4 // 256) * 256 + 256
     assert st == 0 and n == want
+
+
+def _qjl_cache(kvq, **kw):
+    args = dict(k_format=kvq.FMT_CODEBOOK_QJL, k_qjl=(1 << 40) + 4096 * 30)
+    args.update(kw)
+    return _fake_cache(kvq, **args)
+
+
+def test_qjl_key_checks(kvq):
+    """Keys with a residual sketch need the projection (16-byte aligned) and 16-byte
+    aligned (norm, residual norm) pairs; values may not carry a sketch."""
+    assert kvq.kvq_row_bytes("codebook_qjl", 3, 128) == (128 * 3 // 8 + 16, 4)
+    assert _quant(kvq, _qjl_cache(kvq), n=0) == 0  # arguments accepted (nothing to launch)
+    assert _quant(kvq, _qjl_cache(kvq, k_qjl=None)) == 1
+    assert _quant(kvq, _qjl_cache(kvq, k_qjl=(1 << 40) + 4096 * 30 + 4)) == 1
+    assert _quant(kvq, _qjl_cache(kvq, k_aux=(1 << 40) + 4096 * 2 + 2)) == 1
+    assert _quant(kvq, _qjl_cache(kvq, v_format=kvq.FMT_CODEBOOK_QJL)) == 1
+    assert _ws(kvq, [_qjl_cache(kvq)])[0] == 0
+    assert _ws(kvq, [_qjl_cache(kvq)], hq=4 * 2)[0] == 0  # 4 query heads per kv head
+    assert _ws(kvq, [_qjl_cache(kvq, head_dim=256)])[0] == 2  # the sketched decode is built for D=128
+    assert _ws(kvq, [_qjl_cache(kvq, v_format=kvq.FMT_FP16, v_bits=0)])[0] == 2
+    assert _ws(kvq, [_qjl_cache(kvq), _fake_cache(kvq)])[0] == 0  # with a plain codebook tier
+    assert _ws(kvq, [_qjl_cache(kvq), _fake_cache(kvq, k_format=kvq.FMT_FP8_E4M3, k_bits=0,
+                                                    v_format=kvq.FMT_INT4_G32, v_bits=0)])[0] == 2
+    assert _ws(kvq, [_qjl_cache(kvq), _qjl_cache(kvq, k_qjl=(1 << 40) + 4096 * 31)])[0] == 1
+    assert _ws(kvq, [_qjl_cache(kvq, page_size=32)])[0] == 2
+    assert _ws(kvq, [_qjl_cache(kvq)], hq=2 * 8)[0] == 2  # 8 query heads per kv head

@@ -25,7 +25,7 @@ def run_exact(cfg, lens, split_tokens=0, shuffle=None, q=None):
     kvq = gu.kvq_module()
     tiers_kv = seqs_for(cfg, lens)
     built = gu.build_exact(kvq, torch, list(cfg.tiers), tiers_kv, W.signs(cfg, 0), W.signs(cfg, 1),
-                           cfg.page_size, shuffle)
+                           cfg.page_size, shuffle, k_qjl=W.qjl_projection(cfg))
     if q is None:
         q = W.queries(cfg.scaled(batch=len(lens)))
     got = gu.gpu_decode(kvq, torch, built.views, q, split_tokens)
@@ -86,6 +86,43 @@ def test_decode_code_widths(d, group, kb, vb):
     lens = [1, 47, 300, 129]
     got, want, _, _ = run_exact(cfg, lens, split_tokens=96, shuffle=5)
     assert np.all(np.isfinite(got))
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
+QJL_WIDTHS = [(1, 3, 4), (1, 2, 2), (2, 2, 3), (2, 4, 4), (4, 4, 4), (4, 3, 2)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("group,kb,vb", QJL_WIDTHS)
+def test_decode_qjl_keys(group, kb, vb):
+    """Keys with a residual sign sketch (head_dim 128): the scores carry the sketch's
+    correction ||r~|| sqrt(pi/2)/m sum_j z_j <S_j, q~>; both the one-query-head path and
+    the grouped path, ragged lengths, several splits."""
+    hkv = 2
+    cfg = W.CONFIGS["llama7b"].scaled(batch=4, num_q_heads=hkv * group, num_kv_heads=hkv,
+                                      tiers=(W.Tier("codebook_qjl", "codebook", k_bits=kb, v_bits=vb),))
+    lens = [1, 47, 300, 129]
+    got, want, built, q = run_exact(cfg, lens, split_tokens=96, shuffle=5)
+    assert np.all(np.isfinite(got))
+    err = np.abs(got - want).max()
+    assert err <= 1e-4 * max(1.0, np.abs(want).max())
+    # the correction is not negligible: leaving it out moves the output far past the error
+    plain = np.zeros_like(want)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            keys, values = oatt.dequantised_kv(built.ora, b, h // group)
+            plain[b, h] = oatt.attend(q[b, h].astype(np.float64), keys, values)
+    assert np.abs(plain - want).max() > 100 * max(err, 1e-6)
+
+
+@pytest.mark.gpu
+def test_decode_qjl_near_tier_with_codebook_far_tier():
+    """Two tiers in one call: sketched 4-bit keys (near) and plain 2-bit codebook (far)."""
+    cfg = W.CONFIGS["llama7b"].scaled(batch=3, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                                      tiers=(W.Tier("codebook_qjl", "codebook", k_bits=4, v_bits=4, fraction=0.25),
+                                             W.Tier("codebook", "codebook", k_bits=2, v_bits=2)))
+    lens = [5, 400, 1111]
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=64, shuffle=2)
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
 
 
@@ -172,7 +209,7 @@ def pool_index(torch, wl, t, b, n):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["tiny", "llama7b", "gqa32k", "ragged", "append"])
+@pytest.mark.parametrize("name", ["tiny", "llama7b", "llama7b_prod", "gqa32k", "ragged", "append"])
 def test_full_size_sampled_heads(name):
     """Every workload at its full size, built on the GPU by kvq_quantize_append and decoded with
     the split plan the benchmark uses.  For sampled (sequence, kv head) pairs:
@@ -181,6 +218,7 @@ def test_full_size_sampled_heads(name):
          those heads, and the GPU outputs of their query heads must match the oracle's
          dequantise-then-attend within 2e-3."""
     from oracle import cache as ocache
+    from oracle import rotation as orot
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
     cfg = W.CONFIGS[name]
@@ -196,11 +234,12 @@ def test_full_size_sampled_heads(name):
     picks = [(int(rng.integers(cfg.batch)), int(rng.integers(cfg.num_q_heads))) for _ in range(3)]
     picks.append((cfg.batch - 1, cfg.num_q_heads - 1))
     ks_all, vs_all = W.signs(cfg, 0), W.signs(cfg, 1)
-    kv_ref = {}
+    proj = W.qjl_projection(cfg)
+    kv_ref, sketch_rows = {}, {}
     near = total_el = 0
     for b, g in sorted({(b, h // cfg.group) for b, h in picks}):
         parts = head_tokens(cfg, b, g, int(wl.lens[b]), bool(cfg.prefill_chunk))
-        K, V = [], []
+        K, V, SK = [], [], []
         for t, tier in enumerate(cfg.tiers):
             cache = wl.caches[t]
             n = int(wl.tier_len[t][b])
@@ -212,28 +251,41 @@ def test_full_size_sampled_heads(name):
                 rows_t, aux_t = getattr(cache, f"{side}_rows"), getattr(cache, f"{side}_aux")
                 rows_g = rows_t[pages, g, offs].cpu().numpy()
                 aux_g = None if aux_t is None else aux_t[pages, g, offs].cpu().numpy()
-                tab = gu.tables(tier.codebook, bits) if fmt == "codebook" else (None, None)
-                if fmt == "codebook":
+                tab = gu.tables(tier.codebook, bits) if fmt.startswith("codebook") else (None, None)
+                if fmt == "codebook_qjl":
+                    gu.check_qjl_rows(x, sg, bits, proj, rows_g, aux_g, kind=tier.codebook)
+                elif fmt == "codebook":
                     st = gu.check_codebook_codes(x, sg, bits, rows_g, aux_g[:, 0], kind=tier.codebook)
                     near, total_el = near + st[1], total_el + st[2]
                 elif fmt == "int4_g32":
                     gu.check_int4_rows(x, sg, rows_g, aux_g)
                 else:
                     gu.check_float_rows(x, sg, fmt, rows_g)
-                rows_o, aux_o = ocache.encode(x, sg, fmt, bits, tab[1])
+                rows_o, aux_o = ocache.encode(x, sg, fmt, bits, tab[1], tab[0], proj)
+                if side == "k":
+                    SK.append((rows_o, aux_o) if fmt == "codebook_qjl" else n)
                 rows_t[pages, g, offs] = torch.from_numpy(rows_o).cuda()
                 if aux_t is not None:
                     aux_t[pages, g, offs] = torch.from_numpy(np.asarray(aux_o).reshape(n, -1)).cuda()
                 dec = ocache.decode(rows_o, aux_o, fmt, sg, cfg.head_dim, bits, tab[0])
                 (K if side == "k" else V).append(dec)
         kv_ref[(b, g)] = (np.concatenate(K), np.concatenate(V))
+        sketch_rows[(b, g)] = SK
     if total_el:
         assert near < gu.MAX_BOUNDARY_FRACTION * total_el, (near, total_el)
     q = W.queries(cfg)
     got = gu.gpu_decode(kvq, torch, wl.views(), q)
     for b, h in picks:
         K, V = kv_ref[(b, h // cfg.group)]
-        want = oatt.attend(q[b, h].astype(np.float64), K, V)
+        qh = q[b, h].astype(np.float64)
+        extra = None
+        if any(t.k_format == "codebook_qjl" for t in cfg.tiers):
+            q_rot = orot.rotate(qh, ks_all[h // cfg.group])
+            extra = np.concatenate([np.zeros(e) if isinstance(e, int) else
+                                    ocache.qjl_correction(e[0], e[1], q_rot, proj, cfg.head_dim,
+                                                          cfg.tiers[t].k_bits)
+                                    for t, e in enumerate(sketch_rows[(b, h // cfg.group)])])
+        want = oatt.attend(qh, K, V, extra)
         err = np.abs(got[b, h] - want).max()
         print(f"{name} b={b} h={h}: max-abs {err:.3e} (|out| max {np.abs(want).max():.2f})")
         assert err <= gu.ATOL_OUT

@@ -30,7 +30,8 @@ def make_inputs(n, hkv, d, seed):
     return x.astype(np.float16)
 
 
-def run_append(kvq, torch, fmt, bits, d, n=203, hkv=3, ps=16, seed=0, codebook="lloyd_max", k_only=False):
+def run_append(kvq, torch, fmt, bits, d, n=203, hkv=3, ps=16, seed=0, codebook="lloyd_max", k_only=False,
+               v_fmt=None, k_qjl=None):
     rng = np.random.default_rng(seed + 100)
     k = make_inputs(n, hkv, d, seed)
     v = make_inputs(n, hkv, d, seed + 1)
@@ -40,20 +41,27 @@ def run_append(kvq, torch, fmt, bits, d, n=203, hkv=3, ps=16, seed=0, codebook="
     slots = rng.permutation(num_pages * ps)[:n].astype(np.int32)
     slots[7] = -1  # skipped
     slots[11] = num_pages * ps + 5  # out of range: skipped
-    cache = kvq.PagedCache(d, hkv, num_pages, fmt, fmt, bits, bits, ks, vs, ps, codebook)
+    cache = kvq.PagedCache(d, hkv, num_pages, fmt, v_fmt or fmt, bits, bits, ks, vs, ps, codebook, k_qjl=k_qjl)
     cache.append(torch.from_numpy(k).cuda(), None if k_only else torch.from_numpy(v).cuda(),
                  torch.from_numpy(slots).cuda())
     torch.cuda.synchronize()
     return k, v, ks, vs, slots, cache
 
 
+# The library takes appends of at most 16384 vectors per side with one warp per vector
+# (decode steps) and larger ones with the per-thread kernel (prefill chunks): 203 tokens x 3
+# heads and 5600 x 3 cover both.
+SIZES = [203, 5600]
+
+
 @pytest.mark.gpu
+@pytest.mark.parametrize("n", SIZES)
 @pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("fmt,bits", FORMATS)
-def test_quantize_matches_oracle(fmt, bits, d):
+def test_quantize_matches_oracle(fmt, bits, d, n):
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
-    k, v, ks, vs, slots, cache = run_append(kvq, torch, fmt, bits, d, seed=d + bits)
+    k, v, ks, vs, slots, cache = run_append(kvq, torch, fmt, bits, d, n=n, seed=d + bits)
     keep = np.flatnonzero((slots >= 0) & (slots < cache.num_pages * cache.page_size))
     assert np.all(keep[:DEGENERATE] == np.arange(DEGENERATE))
     stats = []
@@ -84,10 +92,12 @@ def test_quantize_matches_oracle(fmt, bits, d):
 
 
 @pytest.mark.gpu
-def test_quantize_uniform_codebook_and_k_only():
+@pytest.mark.parametrize("n", SIZES)
+def test_quantize_uniform_codebook_and_k_only(n):
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
-    k, v, ks, vs, slots, cache = run_append(kvq, torch, "codebook", 4, 128, seed=5, codebook="uniform", k_only=True)
+    k, v, ks, vs, slots, cache = run_append(kvq, torch, "codebook", 4, 128, n=n, seed=5, codebook="uniform",
+                                            k_only=True)
     keep = np.flatnonzero((slots >= 0) & (slots < cache.num_pages * cache.page_size))
     rows = gu.pool_rows(cache.k_rows, slots[keep])
     aux = gu.pool_rows(cache.k_aux, slots[keep])
@@ -120,3 +130,33 @@ def test_quantize_codes_on_a_large_sample():
         bad, near, total = bad + b_, near + n_, total + t_
     assert near < gu.MAX_BOUNDARY_FRACTION * total
     print(f"codes differing: {bad} of {total}; within 1e-6 of a boundary: {near}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("d,bits", [(128, 2), (128, 3), (128, 4), (256, 3)])
+def test_quantize_qjl_keys_match_oracle(d, bits, n):
+    """Keys with a residual sign sketch (codes, norm, residual norm, 128 sign bits) next to
+    codebook values, on the degenerate and outlier rows of make_inputs."""
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_module()
+    proj = np.random.default_rng(d * 7 + bits).standard_normal((128, d)).astype(np.float32)
+    k, v, ks, vs, slots, cache = run_append(kvq, torch, "codebook_qjl", bits, d, n=n, seed=d + bits,
+                                            v_fmt="codebook", k_qjl=proj)
+    keep = np.flatnonzero((slots >= 0) & (slots < cache.num_pages * cache.page_size))
+    assert cache.k_rows.shape[-1] == d * bits // 8 + 16 and cache.k_aux.shape[-1] == 2
+    rows = gu.pool_rows(cache.k_rows, slots[keep])
+    aux = gu.pool_rows(cache.k_aux, slots[keep])
+    vrows = gu.pool_rows(cache.v_rows, slots[keep])
+    vaux = gu.pool_rows(cache.v_aux, slots[keep])
+    compared = bits_bad = rn_bad = 0
+    for h in range(k.shape[1]):
+        c, sb, rb = gu.check_qjl_rows(k[keep, h], ks[h], bits, proj, rows[:, h], aux[:, h])
+        compared, bits_bad, rn_bad = compared + c, bits_bad + sb, rn_bad + rb
+        gu.check_codebook_codes(v[keep, h], vs[h], bits, vrows[:, h], vaux[:, h, 0])
+    assert compared >= 0.95 * len(keep) * k.shape[1]
+    assert bits_bad <= 1e-3 * compared * 128 + 1
+    # the zero vector: zero residual, every projection 0 -> every sign bit set
+    z0 = rows[0, :, d * bits // 8:]
+    assert np.all(z0 == 0xFF) and np.all(aux[0, :, 1] == 0)
+    print(f"rows compared {compared}, sign bits differing {bits_bad}, residual norms differing {rn_bad}")

@@ -31,10 +31,12 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import numpy as np
 
 # Stream ids: one independent PCG64 stream family per kind of draw.
-S_K, S_V, S_Q, S_OUTLIER, S_TIER, S_LENS, S_PAGES, S_SIGNS, S_SIGMA, S_NEWTOK = range(10)
+S_K, S_V, S_Q, S_OUTLIER, S_TIER, S_LENS, S_PAGES, S_SIGNS, S_SIGMA, S_NEWTOK, S_PROJ = range(11)
 
 # Storage format names (the same four the C header enumerates).
 CODEBOOK, FP16, FP8_E4M3, INT4_G32 = "codebook", "fp16", "fp8_e4m3", "int4_g32"
+CODEBOOK_QJL = "codebook_qjl"  # keys: codebook codes + residual sign sketch
+QJL_DIM = 128
 
 
 @dataclasses.dataclass(frozen=True)
@@ -86,6 +88,10 @@ CONFIGS: Dict[str, Config] = {
     # Llama-7B-shaped layer: B8, 32/32 heads, D128, ctx 8192, 1% outlier channels x50, 4-bit LM
     "llama7b": Config("llama7b", 8, 32, 32, 128, 8192, (LM4,), seed=1,
                       outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
+    # the same layer with product-quantised keys: 3-bit LM codes + 128-bit residual sign
+    # sketch (4 bits per coordinate), 4-bit LM values
+    "llama7b_prod": Config("llama7b_prod", 8, 32, 32, 128, 8192, (Tier(CODEBOOK_QJL, CODEBOOK, 3, 4),), seed=1,
+                           outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
     # GQA long-context: B32, 32/8 heads, D128, ctx 32768; top 10% fp16, rest fp8 K + INT4-g32 V
     "gqa32k": Config("gqa32k", 32, 32, 8, 128, 32768,
                      (Tier(FP16, FP16, fraction=0.1), Tier(FP8_E4M3, INT4_G32, fraction=0.9)),
@@ -182,6 +188,12 @@ def signs(cfg: Config, which: int, layer: int = 0) -> np.ndarray:
     r = rng(cfg, S_SIGNS, layer, which)
     return np.where(r.integers(0, 2, size=(cfg.num_kv_heads, cfg.head_dim)) == 0,
                     1, -1).astype(np.int8)
+
+
+def qjl_projection(cfg: Config, layer: int = 0) -> np.ndarray:
+    """float32 [QJL_DIM, D] projection of the residual sign sketch, iid N(0,1) entries, one
+    per layer.  Like the signs, it is an input of the method."""
+    return rng(cfg, S_PROJ, layer).standard_normal((QJL_DIM, cfg.head_dim)).astype(np.float32)
 
 
 def tier_members(cfg: Config, b: int, h: int, total: int) -> List[np.ndarray]:
@@ -317,11 +329,14 @@ class GpuWorkload:
         ks, vs = signs(cfg, 0), signs(cfg, 1)
         self.k_signs = torch.from_numpy(ks).to(device)
         self.v_signs = torch.from_numpy(vs).to(device)
+        self.k_qjl = (torch.from_numpy(qjl_projection(cfg)).to(device)
+                      if any(t.k_format == CODEBOOK_QJL for t in cfg.tiers) else None)
         self.caches = []
         for t, tier in enumerate(cfg.tiers):
             self.caches.append(kvq.PagedCache(cfg.head_dim, cfg.num_kv_heads, self.maps[t].num_pages,
                                               tier.k_format, tier.v_format, tier.k_bits, tier.v_bits,
-                                              self.k_signs, self.v_signs, cfg.page_size, tier.codebook, device))
+                                              self.k_signs, self.v_signs, cfg.page_size, tier.codebook, device,
+                                              k_qjl=self.k_qjl if tier.k_format == CODEBOOK_QJL else None))
         self.block_tables = [torch.from_numpy(np.maximum(m.block_table, 0)).to(device) for m in self.maps]
         self.seq_lens_dev = [torch.from_numpy(l.astype(np.int32)).to(device) for l in self.tier_len]
         self.device = device
