@@ -21,7 +21,8 @@ estimate of <q, r> (cache.qjl_correction, taken with the rotated query q~ = R q)
 
 Readings taken: decode attends to the whole cache (no causal or window mask: the
 query is the newest token); the output is float32; a sequence with no cached
-token gives a zero output.  The oracle does not use the rotated-domain scores, a
+token gives a zero output.  Score gating and spike flags (FoveatedKV "Making it
+fast"): see the last section of this file.  The oracle does not use the rotated-domain scores, a
 lookup table, split-K or an online softmax; that those give the same result is
 what the GPU tests check.
 """
@@ -116,3 +117,86 @@ def decode_attention(q16: np.ndarray, tiers: Sequence[TierState],
                 q = q16[b, h].astype(np.float64)
                 out[b, h] = attend(q, keys, values, sketch_terms(tiers, b, g, q) if sketched else None)
     return out.astype(np.float32)
+
+
+# ----------------------------------------------------------------------------- FoveatedKV
+# Two kernel features of the FoveatedKV page, section "Making it fast": score-gated value
+# loading (a token whose softmax weight is below exp(-16) of the largest contributes
+# essentially nothing, so its value need not be dequantised) and spike detection (a
+# far-tier token that scores above near-tier tokens), which the page reads off the softmax
+# bookkeeping.  Tier 0 is the near tier; tiers 1.. are far.
+
+SCORE_GATE_NATS = 16.0
+
+
+def tier_scores(q: np.ndarray, tiers: Sequence[TierState], b: int, g: int) -> List[np.ndarray]:
+    """Per tier, the scores (q.k + sketch term) / sqrt(d) of sequence b's tokens at kv head g
+    (float64, natural-log units; empty arrays for empty tiers)."""
+    d = q.shape[-1]
+    out = []
+    for i, t in enumerate(tiers):
+        n = int(t.lens[b])
+        if n == 0:
+            out.append(np.zeros(0))
+            continue
+        keys = cache.read(t.k, t.block_table[b], n, g, t.page_size)
+        dots = keys @ np.asarray(q, dtype=np.float64)
+        if t.k.fmt == cache.CODEBOOK_QJL:
+            rows, aux = cache.gather(t.k, t.block_table[b], n, g, t.page_size)
+            q_rot = rotate(np.asarray(q, dtype=np.float64), t.k.signs[g])
+            dots = dots + cache.qjl_correction(rows, aux, q_rot, t.k.proj, d, t.k.bits)
+        out.append(dots / math.sqrt(d))
+    return out
+
+
+def spike_flags(q16: np.ndarray, tiers: Sequence[TierState]) -> np.ndarray:
+    """int32 [B, Hq]: 1 where the highest score among the tokens of tiers 1.. exceeds the
+    lowest score among the tokens of tier 0 (a far token outranks a near one), else 0; 0
+    when tier 0 or the later tiers hold no token of the sequence.  Also returns the margin
+    max_far - min_near (float64 [B, Hq], nan where undefined), which tells how close a
+    decision was."""
+    bsz, hq, _ = q16.shape
+    hkv = tiers[0].k.signs.shape[0]
+    grp = hq // hkv
+    flags = np.zeros((bsz, hq), dtype=np.int32)
+    margin = np.full((bsz, hq), np.nan)
+    for b in range(bsz):
+        for h in range(hq):
+            s = tier_scores(q16[b, h].astype(np.float64), tiers, b, h // grp)
+            near = s[0]
+            far = np.concatenate(s[1:]) if len(s) > 1 else np.zeros(0)
+            if near.size == 0 or far.size == 0:
+                continue
+            margin[b, h] = far.max() - near.min()
+            flags[b, h] = int(far.max() > near.min())
+    return flags, margin
+
+
+def gated_attention(q16: np.ndarray, tiers: Sequence[TierState], gate_nats: float = SCORE_GATE_NATS):
+    """Score-gated decode attention, with the gate taken against the largest score of the
+    whole sequence: a token scoring more than gate_nats below it adds nothing to the value
+    sum but still counts in the softmax denominator.  Returns (gated, exact, bound), each
+    float64 [B, Hq, d]: bound[b, h, i] = sum over the gated tokens of w_t |v_t[i]| with the
+    exact softmax weights w_t.  Any implementation that drops the value of a subset of
+    the gated tokens -- for instance gating against a running maximum, which never
+    exceeds the final one -- lies within `bound` of both `exact` and `gated`."""
+    bsz, hq, d = q16.shape
+    hkv = tiers[0].k.signs.shape[0]
+    grp = hq // hkv
+    gated = np.zeros((bsz, hq, d))
+    exact = np.zeros((bsz, hq, d))
+    bound = np.zeros((bsz, hq, d))
+    for b in range(bsz):
+        for g in range(hkv):
+            keys, values = dequantised_kv(tiers, b, g)
+            if keys is None:
+                continue
+            for h in range(g * grp, (g + 1) * grp):
+                s = np.concatenate(tier_scores(q16[b, h].astype(np.float64), tiers, b, g))
+                w = np.exp(s - s.max())
+                w = w / w.sum()
+                drop = s < s.max() - gate_nats
+                exact[b, h] = w @ values
+                gated[b, h] = (w * ~drop) @ values
+                bound[b, h] = (w * drop) @ np.abs(values)
+    return gated, exact, bound
