@@ -204,6 +204,37 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
                                         float* out, void* workspace,
                                         size_t workspace_bytes, void* stream);
 
+/* Options of kvq_decode_attention_ex: two features of the FoveatedKV page's fused kernel
+ * ("Making it fast").  All zero is the plain computation of kvq_decode_attention. */
+#define KVQ_SCORE_GATE_NATS 16.0f
+typedef struct kvq_decode_options {
+  /* Nonzero: score-gated value loading.  A token whose score is more than
+   * KVQ_SCORE_GATE_NATS below the running maximum of its split-K chunk (natural-log
+   * units: its softmax weight is below exp(-16) of that maximum's) may leave out its value:
+   * it still counts in the softmax denominator, but adds nothing to the value sum.  The
+   * fused kernels leave out the value work of a 16-token page when every token of it, for
+   * every query head of the kv head, qualifies; the generic kernel judges token by token
+   * and skips the value row's load.  A running maximum never exceeds the final one, so the
+   * output differs from the exact one by at most sum_t w_t |v_t| over the tokens scoring
+   * more than 16 nats below the sequence's best (w_t the exact softmax weights). */
+  int32_t score_gate;
+  /* Optional device int32 [batch][num_q_heads] (4-byte aligned), written when non-NULL:
+   * 1 where the best score among the tokens of tiers 1..num_tiers-1 exceeds the worst
+   * score among the tokens of tier 0 (a far-tier token outranks a near-tier one -- the
+   * page's spike detection), else 0; 0 when tier 0 or the later tiers hold no token of the
+   * sequence.  Scores are compared as the kernels compute them (float32). */
+  int32_t* spike_flags;
+} kvq_decode_options;
+
+/* kvq_decode_attention with options (NULL options: identical to kvq_decode_attention).
+ * Same arguments, workspace and errors, plus: a misaligned spike_flags buffer returns
+ * KVQ_ERR_INVALID_ARGUMENT. */
+KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t num_tiers,
+                                           const uint16_t* q, int32_t batch,
+                                           int32_t num_q_heads, int32_t split_tokens,
+                                           float* out, void* workspace, size_t workspace_bytes,
+                                           const kvq_decode_options* options, void* stream);
+
 /* Decode attention for callers that cannot allocate device memory.
  *
  * Same computation, arguments and results as kvq_decode_attention, without the workspace

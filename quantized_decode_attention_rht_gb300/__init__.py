@@ -61,6 +61,14 @@ class KvqTierView(ctypes.Structure):
                 ("seq_lens", ctypes.c_void_p), ("max_pages", ctypes.c_int32)]
 
 
+class KvqDecodeOptions(ctypes.Structure):
+    """Mirror of ``struct kvq_decode_options``."""
+
+    _fields_ = [("score_gate", ctypes.c_int32), ("spike_flags", ctypes.c_void_p)]
+
+
+SCORE_GATE_NATS = 16.0
+
 _lib_handle = None
 
 
@@ -87,6 +95,8 @@ def lib() -> ctypes.CDLL:
             "kvq_quantize_append": [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp],
             "kvq_decode_workspace_size": [ctypes.POINTER(KvqTierView), i32, i32, i32, i32, szp],
             "kvq_decode_attention": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz, vp],
+            "kvq_decode_attention_ex": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz,
+                                        ctypes.POINTER(KvqDecodeOptions), vp],
             "kvq_decode_attention_noalloc": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp],
         }
         for name, args in sigs.items():
@@ -104,6 +114,14 @@ def _check(status: int, what: str) -> None:
 
 def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+def _dense(*tensors) -> None:
+    """The C ABI takes dense row-major buffers: refuse strided views rather than read them
+    in the wrong order."""
+    for t in tensors:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors passed to libkvq must be contiguous")
 
 
 def _stream(stream) -> Optional[int]:
@@ -165,6 +183,7 @@ def kvq_codebook_tables(bits: int, centroids: np.ndarray):
 
 def kvq_quantize_append(cache: KvqCache, k, v, slot_mapping, stream=None) -> None:
     """k, v: fp16 CUDA tensors [T, Hkv, D] (either may be None); slot_mapping: int32 [T]."""
+    _dense(k, v, slot_mapping)
     t = (k if k is not None else v).shape[0]
     _check(lib().kvq_quantize_append(ctypes.byref(cache), _ptr(k), _ptr(v), t, _ptr(slot_mapping),
                                      _stream(stream)), "kvq_quantize_append")
@@ -173,6 +192,7 @@ def kvq_quantize_append(cache: KvqCache, k, v, slot_mapping, stream=None) -> Non
 def _views(tiers: Sequence["TierView"]):
     arr = (KvqTierView * len(tiers))()
     for i, t in enumerate(tiers):
+        _dense(t.block_table, t.seq_lens)
         arr[i].cache = ctypes.pointer(t.cache.struct)
         arr[i].block_table = _ptr(t.block_table)
         arr[i].seq_lens = _ptr(t.seq_lens)
@@ -188,13 +208,22 @@ def kvq_decode_workspace_size(tiers, batch: int, num_q_heads: int, split_tokens:
     return n.value
 
 
-def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream=None) -> None:
-    """q: fp16 [B, Hq, D]; out: fp32 [B, Hq, D]; workspace: uint8 CUDA tensor."""
+def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream=None, score_gate: bool = False,
+                         spike_flags=None) -> None:
+    """q: fp16 [B, Hq, D]; out: fp32 [B, Hq, D]; workspace: uint8 CUDA tensor.
+    score_gate / spike_flags (int32 [B, Hq] CUDA tensor): the options of
+    kvq_decode_attention_ex (FoveatedKV score-gated value loading and spike detection)."""
+    _dense(q, out, workspace, spike_flags)
     arr = _views(tiers)
     b, hq, _ = q.shape
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().kvq_decode_attention(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out), _ptr(workspace),
-                                      ws_bytes, _stream(stream)), "kvq_decode_attention")
+    if not score_gate and spike_flags is None:
+        _check(lib().kvq_decode_attention(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out),
+                                          _ptr(workspace), ws_bytes, _stream(stream)), "kvq_decode_attention")
+        return
+    opts = KvqDecodeOptions(1 if score_gate else 0, _ptr(spike_flags))
+    _check(lib().kvq_decode_attention_ex(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out), _ptr(workspace),
+                                         ws_bytes, ctypes.byref(opts), _stream(stream)), "kvq_decode_attention_ex")
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -204,6 +233,7 @@ def kvq_decode_attention_noalloc(tiers, q, out, split_tokens: int = 0, stream=No
     """Decode attention using the library's static device scratch (no allocation anywhere);
     for callers that may not allocate device memory.  Calls that overlap on the GPU race on
     the shared scratch."""
+    _dense(q, out)
     arr = _views(tiers)
     b, hq, _ = q.shape
     _check(lib().kvq_decode_attention_noalloc(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out),

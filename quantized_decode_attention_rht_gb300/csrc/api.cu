@@ -188,12 +188,14 @@ bool has_sketch(const kvq_tier_view* tiers, int n) {
   return false;
 }
 
-// Workspace: partial accumulators [B][Hq][S][D], (max, sum) [B][Hq][S][2], with keys that
-// carry a sketch the projected queries [B][Hq][KVQ_QJL_DIM], then the work counters.
+// Workspace: partial accumulators [B][Hq][S][D], (max, sum) [B][Hq][S][2], each split's
+// lowest score [B][Hq][S] (spike flags), with keys that carry a sketch the projected queries
+// [B][Hq][KVQ_QJL_DIM], then the work counters.
 size_t workspace_bytes(int batch, int hq, int d, int total_splits, bool sketch) {
   const size_t parts = (size_t)batch * hq * total_splits;
   const size_t pq = sketch ? align_up((size_t)batch * hq * KVQ_QJL_DIM * sizeof(float), 256) : 0;
-  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256) + pq + 256;
+  return align_up(parts * d * sizeof(float), 256) + align_up(parts * 2 * sizeof(float), 256) +
+         align_up(parts * sizeof(float), 256) + pq + 256;
 }
 
 }  // namespace
@@ -282,8 +284,17 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
 KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_tiers, const uint16_t* q,
                                         int32_t batch, int32_t num_q_heads, int32_t split_tokens, float* out,
                                         void* workspace, size_t ws_bytes, void* stream) {
+  return kvq_decode_attention_ex(tiers, num_tiers, q, batch, num_q_heads, split_tokens, out, workspace, ws_bytes,
+                                 nullptr, stream);
+}
+
+KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t num_tiers, const uint16_t* q,
+                                           int32_t batch, int32_t num_q_heads, int32_t split_tokens, float* out,
+                                           void* workspace, size_t ws_bytes, const kvq_decode_options* options,
+                                           void* stream) {
   kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
   if (st != KVQ_OK) return st;
+  if (options && options->spike_flags && !aligned(options->spike_flags, 4)) return KVQ_ERR_INVALID_ARGUMENT;
   if (batch == 0) return KVQ_OK;
   if (!q || !out || !aligned(q, 4) || !aligned(out, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   const kvq_cache* c0 = tiers[0].cache;
@@ -330,8 +341,11 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
   const size_t parts = (size_t)batch * num_q_heads * plan.total;
   p.ws_acc = static_cast<float*>(workspace);
   p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(parts * d * sizeof(float), 256));
-  p.ws_pq = sketch ? reinterpret_cast<float*>(reinterpret_cast<char*>(p.ws_ml) + align_up(parts * 2 * sizeof(float), 256))
+  p.ws_min = reinterpret_cast<float*>(reinterpret_cast<char*>(p.ws_ml) + align_up(parts * 2 * sizeof(float), 256));
+  p.ws_pq = sketch ? reinterpret_cast<float*>(reinterpret_cast<char*>(p.ws_min) + align_up(parts * sizeof(float), 256))
                    : nullptr;
+  p.spike = options ? options->spike_flags : nullptr;
+  p.gate = options && options->score_gate ? 1 : 0;
   p.batch = batch;
   p.hq = num_q_heads;
   p.hkv = hkv;

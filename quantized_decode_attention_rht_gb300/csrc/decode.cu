@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 
   __shared__ float q_s[G][D];
   __shared__ float lut_k[256], lut_v[256];
-  __shared__ float w_m[kWarps][G], w_l[kWarps][G];
+  __shared__ float w_m[kWarps][G], w_l[kWarps][G], w_mn[kWarps][G];
   __shared__ float w_acc[kWarps][G][D];
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -179,11 +179,13 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
     __syncthreads();
   }
   const int r = lane % LPT, gi = lane / LPT, e0 = r * DPL;
-  float qr[G][DPL], acc[G][DPL], m[G], l[G];
+  const bool track = p.spike != nullptr && tier_index == 0;  // lowest score, for spike flags
+  float qr[G][DPL], acc[G][DPL], m[G], l[G], mn[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     l[g] = 0.f;
+    mn[g] = INFINITY;
 #pragma unroll
     for (int j = 0; j < DPL; ++j) {
       qr[g][j] = q_s[g][e0 + j] * (kLog2e / (float)D);
@@ -230,8 +232,22 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
         }
         pr[g] = valid ? exp2f(sc[g] - m[g]) : 0.f;
         l[g] += pr[g];
+        if (track && valid) mn[g] = fminf(mn[g], sc[g]);
       }
-      if (valid) {
+      // score gate: a token far below the running maximum of every head keeps its value
+      // row unread; per head, a gated token adds nothing to that head's value sum
+      bool need = valid;
+      if (p.gate) {
+        bool any = false;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const bool keep = sc[g] - m[g] >= -kGateLog2;
+          pr[g] = keep ? pr[g] : 0.f;
+          any = any || keep;
+        }
+        need = need && any;
+      }
+      if (need) {
         float vs;
         Row<VF, D, DPL>::load(T.v_rows, T.v_aux, rowid, T.v_row_bytes, e0, lut_v, x, vs);
 #pragma unroll
@@ -249,6 +265,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 #pragma unroll
     for (int o = LPT; o < 32; o <<= 1) {
       l[g] += __shfl_xor_sync(0xFFFFFFFFu, l[g], o);
+      mn[g] = fminf(mn[g], __shfl_xor_sync(0xFFFFFFFFu, mn[g], o));
 #pragma unroll
       for (int j = 0; j < DPL; ++j) acc[g][j] += __shfl_xor_sync(0xFFFFFFFFu, acc[g][j], o);
     }
@@ -261,6 +278,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
       if (r == 0) {
         w_m[warp][g] = m[g];
         w_l[warp][g] = l[g];
+        w_mn[warp][g] = mn[g];
       }
     }
   }
@@ -285,6 +303,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
     if (j == 0) {
       p.ws_ml[2 * part] = mx;
       p.ws_ml[2 * part + 1] = s;
+      if (track) {
+        float lo = w_mn[0][g];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) lo = fminf(lo, w_mn[w][g]);
+        p.ws_min[part] = lo;
+      }
     }
   }
 }
@@ -308,6 +332,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
   __shared__ float s_w[kCombineMaxSplits];
   __shared__ int s_part[kCombineMaxSplits];
   __shared__ float s_red[kCombineWarps][2];
+  __shared__ float s_spk[kCombineWarps][2];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // partials of the split-K pass are complete
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = blockIdx.x;
@@ -315,29 +340,53 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
   const int hk = hq / (p.hq / p.hkv);
   const size_t base = ((size_t)b * p.hq + hq) * p.total_splits;
   // ---- splits holding tokens, over every tier: partial indices and (max, sum)
-  int n = 0;
+  int n = 0, n0 = 0;  // splits holding tokens; the first n0 are tier 0's
   for (int ti = 0; ti < p.num_tiers; ++ti) {
     const DecTier& T = p.tier[ti];
     const int nt = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
     for (int s = threadIdx.x; s < nt && n + s < kCombineMaxSplits; s += blockDim.x)
       s_part[n + s] = T.split_begin + s;
     n += nt;
+    if (ti == 0) n0 = nt;
   }
   n = min(n, kCombineMaxSplits);  // the plan refuses more splits than this
   __syncthreads();
   float mx = -INFINITY, lsum = 0.f;
+  float far_mx = -INFINITY, near_mn = INFINITY;  // spike flags: best far score, worst near score
   for (int s = threadIdx.x; s < n; s += blockDim.x) {
     const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + 2 * (base + s_part[s]));
     s_w[s] = ml.x;
     mx = fmaxf(mx, ml.x);
+    if (p.spike) {
+      if (s < n0) near_mn = fminf(near_mn, p.ws_min[base + s_part[s]]);
+      else far_mx = fmaxf(far_mx, ml.x);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   if (lane == 0) s_red[warp][0] = mx;
+  if (p.spike) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      far_mx = fmaxf(far_mx, __shfl_xor_sync(0xFFFFFFFFu, far_mx, o));
+      near_mn = fminf(near_mn, __shfl_xor_sync(0xFFFFFFFFu, near_mn, o));
+    }
+    if (lane == 0) {
+      s_spk[warp][0] = far_mx;
+      s_spk[warp][1] = near_mn;
+    }
+  }
   __syncthreads();
   mx = s_red[0][0];
 #pragma unroll
   for (int w = 1; w < kCombineWarps; ++w) mx = fmaxf(mx, s_red[w][0]);
+  if (p.spike && threadIdx.x == 0) {
+    for (int w = 1; w < kCombineWarps; ++w) {
+      far_mx = fmaxf(far_mx, s_spk[w][0]);
+      near_mn = fminf(near_mn, s_spk[w][1]);
+    }
+    p.spike[(size_t)b * p.hq + hq] = (n0 > 0 && n > n0 && far_mx > near_mn) ? 1 : 0;
+  }
   __syncthreads();  // s_red is reused below
   for (int s = threadIdx.x; s < n; s += blockDim.x) {
     const float m = s_w[s];

@@ -42,6 +42,9 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.ws_acc = dp.ws_acc;
     p.ws_ml = dp.ws_ml;
     p.pq = dp.ws_pq;
+    p.ws_min = dp.ws_min;
+    p.gate = dp.gate;
+    p.track = dp.spike != nullptr && i == 0;
     p.counter = counters + i;
     p.err = counters + cbk::kErrorWord;
     p.hq = dp.hq;

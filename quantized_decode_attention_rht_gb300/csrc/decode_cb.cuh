@@ -199,9 +199,11 @@ struct CbParams {
   float* ws_acc;
   float* ws_ml;
   float* pq;     // keys with a residual sketch: p' = S q' per query head, [B][Hq][KVQ_QJL_DIM]
+  float* ws_min; // lowest score per split, written when `track` (tier 0, spike flags asked for)
   int* counter;  // this launch's work counter
   int* err;      // error word: set when a wait for a bulk copy gives up
   int hq, hkv, total_splits, total_items, smem_bytes;
+  int gate, track;  // score-gated value loading; record the lowest score
 };
 
 // Shared-memory plan common to both paths: table region (aligned to its size), the residual
@@ -520,7 +522,7 @@ struct Path1 {
     }
 #pragma unroll
     for (int j = 0; j < NP; ++j) acc[j] = 0ull;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, mn = INFINITY;
     constexpr float sscale = kInvD / kQScale;
 #pragma unroll 1
     for (int i = 0; i < npg; ++i) {
@@ -602,6 +604,13 @@ struct Path1 {
       const float p0 = v0 ? exp2f(x0 - m) : 0.f;
       const float p1 = v1 ? exp2f(x1 - m) : 0.f;
       l += p0 + p1;
+      if (p.track) {
+        float lo = fminf(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY);
+        lo = fminf(lo, __shfl_xor_sync(kFull, lo, 4));
+        lo = fminf(lo, __shfl_xor_sync(kFull, lo, 8));
+        mn = fminf(mn, fminf(lo, __shfl_xor_sync(kFull, lo, 16)));
+      }
+      if (p.gate && mt - m < -kGateLog2) continue;  // score gate: mt is warp-uniform here
       const float w0 = v0 ? p0 * (__half2float(__ushort_as_half((uint16_t)nv0)) * kInvD) : 0.f;
       const float w1 = v1 ? p1 * (__half2float(__ushort_as_half((uint16_t)nv1)) * kInvD) : 0.f;
       const u64 W0 = pk2(w0, w0), W1 = pk2(w1, w1);
@@ -637,6 +646,7 @@ struct Path1 {
     if (lane == 0) {
       p.ws_ml[2 * part] = m;
       p.ws_ml[2 * part + 1] = l;
+      if (p.track) p.ws_min[part] = mn;
     }
   }
 };
@@ -721,7 +731,7 @@ struct PathM {
     float acc[KS][4];
 #pragma unroll
     for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f, mn = INFINITY;
     constexpr float kInvD = D == 128 ? 0.08838834764831845f : 0.0625f;
     constexpr float sscale = kInvD / (kQScale * kCScale);
     constexpr float wscale = kWScale * kInvD;
@@ -822,6 +832,14 @@ struct PathM {
       const float p0 = v0 ? exp2f(x0 - m) : 0.f;
       const float p1 = v1 ? exp2f(x1 - m) : 0.f;
       l += p0 + p1;
+      if (p.track) {
+        float lo = fminf(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY);
+        lo = fminf(lo, __shfl_xor_sync(kFull, lo, 4));
+        lo = fminf(lo, __shfl_xor_sync(kFull, lo, 8));
+        mn = fminf(mn, fminf(lo, __shfl_xor_sync(kFull, lo, 16)));
+      }
+      // score gate: every token of the page, for every live head, far below its running max
+      if (p.gate && __all_sync(kFull, c >= G || mt - m < -kGateLog2)) continue;
       // ---- weight B fragments: column g = (head g/2, part g%2), tokens 2c, 2c+1 | 2c+8, 2c+9
       const float w0 = v0 ? p0 * (__half2float(__ushort_as_half((uint16_t)nv0)) * wscale) : 0.f;
       const float w1 = v1 ? p1 * (__half2float(__ushort_as_half((uint16_t)nv1)) * wscale) : 0.f;
@@ -862,6 +880,7 @@ struct PathM {
       if (g == 0) {
         p.ws_ml[2 * part] = m;
         p.ws_ml[2 * part + 1] = l;
+        if (p.track) p.ws_min[part] = mn;
       }
     }
   }

@@ -112,6 +112,14 @@ __device__ __forceinline__ uint32_t split_pair(float x, float y, float hl) {
   return pack_f16x2(rx, ry);
 }
 
+// Lowest score of head c over the page's 16 tokens (lanes g = 0..7 of the same c).
+__device__ __forceinline__ float page_min(float a, float b) {
+  float v = fminf(a, b);
+  v = fminf(v, __shfl_xor_sync(kFull, v, 4));
+  v = fminf(v, __shfl_xor_sync(kFull, v, 8));
+  return fminf(v, __shfl_xor_sync(kFull, v, 16));
+}
+
 // ---------------------------------------------------------------- parameters
 struct GqaTier {
   const uint8_t* k_rows;
@@ -130,8 +138,10 @@ struct GqaParams {
   const int8_t* k_signs;
   float* ws_acc;
   float* ws_ml;
+  float* ws_min;  // lowest score per tier-0 split, when spike flags are asked for
   int* counter;
   int hq, hkv, total_splits, total_items;
+  int gate, spike;  // score-gated value loading; track tier 0's lowest scores
 };
 
 // ---------------------------------------------------------------- per-warp pieces
@@ -232,7 +242,7 @@ struct Far {
 
   struct State {
     float acc[4][2][4];  // [group][m][c0..c3]
-    float m, l;
+    float m, l, mn;
   };
 
   __device__ static void init(State& s) {
@@ -245,6 +255,7 @@ struct Far {
     }
     s.m = -INFINITY;
     s.l = 0.f;
+    s.mn = INFINITY;
   }
 
   __device__ static void rescale(State& s, float f) {
@@ -258,7 +269,8 @@ struct Far {
     }
   }
 
-  __device__ static void page(const uint8_t* st, int nvalid, const uint32_t (&qf)[8][2], State& s, int lane) {
+  __device__ static void page(const uint8_t* st, int nvalid, const uint32_t (&qf)[8][2], State& s, int lane,
+                              bool track, bool gate) {
     const int g = lane >> 2, c = lane & 3;
     const uint32_t s0 = smem_addr(st);
     // ---- scores
@@ -292,6 +304,9 @@ struct Far {
     const float p0 = v0 ? exp2f(x0 - s.m) : 0.f;
     const float p1 = v1 ? exp2f(x1 - s.m) : 0.f;
     s.l += p0 + p1;
+    if (track) s.mn = fminf(s.mn, page_min(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY));
+    // score gate: every token of the page, for all four heads, far below the running max
+    if (gate && __all_sync(kFull, mt - s.m < -kGateLog2)) return;
     // ---- weights w = p * scale (x 2^8) per group for this lane's tokens (g, g+8), head c
     const uint2 sc0 = lds64(s0 + F_S + 8 * g), sc1 = lds64(s0 + F_S + 8 * (g + 8));
     const __half2* h0 = reinterpret_cast<const __half2*>(&sc0);
@@ -365,7 +380,7 @@ struct Far {
   }
 
   // Partial for head c: acc[32a + 4g + k] = sum_t p_t s_ta (u - 8), relative to the max.
-  __device__ static void finish(State& s, float* acc_out, float* ml_out, int lane) {
+  __device__ static void finish(State& s, float* acc_out, float* ml_out, float* mn_out, int lane) {
     const int g = lane >> 2;
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) s.l += __shfl_xor_sync(kFull, s.l, o);
@@ -382,6 +397,7 @@ struct Far {
     if (g == 0) {
       ml_out[0] = s.m;
       ml_out[1] = s.l;
+      if (mn_out) *mn_out = s.mn;
     }
   }
 };
@@ -426,7 +442,7 @@ struct Near {
 
   struct State {
     float acc[8][4];  // [m-tile][c0..c3]
-    float m, l;
+    float m, l, mn;
   };
 
   __device__ static void init(State& s) {
@@ -436,9 +452,11 @@ struct Near {
       for (int k = 0; k < 4; ++k) s.acc[a][k] = 0.f;
     s.m = -INFINITY;
     s.l = 0.f;
+    s.mn = INFINITY;
   }
 
-  __device__ static void page(const uint8_t* st, int nvalid, const uint32_t (&qf)[8][2], State& s, int lane) {
+  __device__ static void page(const uint8_t* st, int nvalid, const uint32_t (&qf)[8][2], State& s, int lane,
+                              bool track, bool gate) {
     const int g = lane >> 2, c = lane & 3;
     const uint32_t s0 = smem_addr(st);
     const int t = lane & 7, mi = lane >> 3;
@@ -473,6 +491,8 @@ struct Near {
     const float p0 = v0 ? exp2f(x0 - s.m) : 0.f;
     const float p1 = v1 ? exp2f(x1 - s.m) : 0.f;
     s.l += p0 + p1;
+    if (track) s.mn = fminf(s.mn, page_min(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY));
+    if (gate && __all_sync(kFull, mt - s.m < -kGateLog2)) return;  // score gate (see Far)
     const int srcA = 4 * (2 * c) + (g >> 1), srcB = srcA + 4;
     const float q0 = p0 * kWScale, q1 = p1 * kWScale;
     const uint32_t hi = pack_f16x2(q0, q1);
@@ -493,7 +513,7 @@ struct Near {
     }
   }
 
-  __device__ static void finish(State& s, float* acc_out, float* ml_out, int lane) {
+  __device__ static void finish(State& s, float* acc_out, float* ml_out, float* mn_out, int lane) {
     const int g = lane >> 2;
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) s.l += __shfl_xor_sync(kFull, s.l, o);
@@ -506,6 +526,7 @@ struct Near {
     if (g == 0) {
       ml_out[0] = s.m;
       ml_out[1] = s.l;
+      if (mn_out) *mn_out = s.mn;
     }
   }
 };
@@ -513,7 +534,7 @@ struct Near {
 // One work item: pages [t0, t1) of sequence b, kv head hk in tier T.
 template <class TT>
 __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, int b, int hk, int chunk, int t0,
-                                         int t1, uint8_t* wsm, int lane) {
+                                         int t1, uint8_t* wsm, int lane, bool track) {
   const int g = lane >> 2, c = lane & 3;
   float* qbuf = reinterpret_cast<float*>(wsm);  // the ring is idle between items
   int* btab = reinterpret_cast<int*>(wsm + kBtab);
@@ -541,14 +562,14 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
     __syncwarp();
     const int slot = i % TT::S;
     const int nvalid = min(PS, t1 - (pg0 + i) * PS);
-    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane);
+    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0);
     __syncwarp();
     if (i + TT::S < npg) TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
     cp_commit();
   }
   cp_wait<0>();
   const size_t part = ((size_t)b * p.hq + hk * G + c) * p.total_splits + T.split_begin + chunk;
-  TT::finish(st, p.ws_acc + part * D, p.ws_ml + 2 * part, lane);
+  TT::finish(st, p.ws_acc + part * D, p.ws_ml + 2 * part, track ? p.ws_min + part : nullptr, lane);
   __syncwarp();
 }
 
@@ -573,8 +594,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
     const int t0 = chunk * T.chunk;
     if (t0 < len) {
       const int t1 = min(len, t0 + T.chunk);
-      if (T.far) run_item<Far>(p, T, b, hk, chunk, t0, t1, wsm, lane);
-      else run_item<Near>(p, T, b, hk, chunk, t0, t1, wsm, lane);
+      const bool track = p.spike && ti == 0;
+      if (T.far) run_item<Far>(p, T, b, hk, chunk, t0, t1, wsm, lane, track);
+      else run_item<Near>(p, T, b, hk, chunk, t0, t1, wsm, lane, track);
     }
     item = __shfl_sync(kFull, next, 0);
   }
@@ -625,6 +647,9 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
   p.k_signs = dp.k_signs;
   p.ws_acc = dp.ws_acc;
   p.ws_ml = dp.ws_ml;
+  p.ws_min = dp.ws_min;
+  p.gate = dp.gate;
+  p.spike = dp.spike != nullptr;
   p.counter = counter;
   p.hq = dp.hq;
   p.hkv = dp.hkv;

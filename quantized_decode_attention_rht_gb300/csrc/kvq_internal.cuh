@@ -62,8 +62,13 @@ struct DecParams {
   float* ws_acc;  // [B][Hq][S][D]
   float* ws_ml;   // [B][Hq][S][2]  (running max in log2 units, sum of exp2)
   float* ws_pq;   // [B][Hq][KVQ_QJL_DIM] projected queries when a tier's keys carry a sketch
+  float* ws_min;  // [B][Hq][S] lowest score of each tier-0 split (written when spike != null)
+  int* spike;     // [B][Hq] spike flags, or null
+  int gate;       // score-gated value loading
   int batch, hq, hkv, page_size, total_splits;
 };
+
+constexpr float kGateLog2 = 23.083120654223414f;  // KVQ_SCORE_GATE_NATS * log2(e): scores are base-2
 
 cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStream_t stream);
 // Fused tensor-core decode for head_dim 128, 4 query heads per kv head, tiers stored as

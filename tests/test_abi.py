@@ -159,8 +159,9 @@ def test_workspace_size_formula(kvq):
     # 2 sequences, 4 query heads, 8 pages of 16 tokens, 32-token splits -> 4 splits
     st, n = _ws(kvq, [c], batch=2, hq=4, split=32, max_pages=8)
     parts = 2 * 4 * 4
-    # partial accumulators + (max, sum) pairs, each rounded up to 256 B, + 256 B work counter
-    want = -(-parts * 128 * 4 // 256) * 256 + -(-parts * 2 * 4 // 256) * 256 + 256
+    # partial accumulators + (max, sum) pairs + lowest scores, each rounded up to 256 B,
+    # + 256 B work counter
+    want = -(-parts * 128 * 4 // 256) * 256 + -(-parts * 2 * 4 // 256) * 256 + -(-parts * 4 // 256) * 256 + 256
     assert st == 0 and n == want
 
 
