@@ -58,11 +58,17 @@ def encode(x16: np.ndarray, s: np.ndarray, fmt: str, bits: int = 0,
       codebook: aux = fp16 norms [...];  int4_g32: aux = fp16 scales [..., d/32];
       codebook_qjl: aux = fp16 [..., 2] (norm, residual norm); needs centroids32 and
       the projection proj [m, d] (float32)."""
-    d = x16.shape[-1]
-    xr = rotate(np.asarray(x16, dtype=np.float64), s)
+    return encode_rotated(rotate(np.asarray(x16, dtype=np.float64), s), fmt, bits, bounds32, centroids32, proj)
+
+
+def encode_rotated(xr: np.ndarray, fmt: str, bits: int = 0, bounds32: Optional[np.ndarray] = None,
+                   centroids32: Optional[np.ndarray] = None, proj: Optional[np.ndarray] = None):
+    """The encode of an already rotated vector x~ (float64 [..., d]): everything `encode`
+    does after the rotation.  Same returns."""
+    d = xr.shape[-1]
     if fmt == CODEBOOK_QJL:
         # 1. the codebook encode of x~ (codes of `bits` bits, fp16 norm)
-        codes, norm16 = encode(x16, s, CODEBOOK, bits, bounds32)
+        codes, norm16 = encode_rotated(xr, CODEBOOK, bits, bounds32)
         # 2. the residual against what the decoder reconstructs
         r = xr - decode_rotated(codes, norm16, CODEBOOK, d, bits, centroids32)
         rnorm16 = formats.to_f16(np.sqrt(np.sum(r * r, axis=-1)))
@@ -122,6 +128,17 @@ def qjl_correction(rows: np.ndarray, aux, q_rot: np.ndarray, proj: np.ndarray, d
     sq = np.asarray(proj, dtype=np.float32).astype(np.float64) @ np.asarray(q_rot, dtype=np.float64)
     rnorm = np.asarray(aux, dtype=np.float64)[..., 1]
     return rnorm * math.sqrt(math.pi / 2.0) / QJL_DIM * (z @ sq)
+
+
+def requantize(rows16: np.ndarray, fmt: str, bits: int = 0, bounds32: Optional[np.ndarray] = None,
+               centroids32: Optional[np.ndarray] = None, proj: Optional[np.ndarray] = None):
+    """Re-encode rows stored as fp16 (the rotated vector x~ in fp16, as an fp16 tier or a
+    recent-token window holds it) into another format: the encode of the stored x~, with
+    no second rotation (FoveatedKV page, "Making it fast": the unquantised decode buffer;
+    AdapTQ page, "Hybrid Execution": tokens move to the quantised path once past the
+    threshold).  Same returns as `encode`."""
+    d = np.shape(rows16)[-1] // 2
+    return encode_rotated(decode_rotated(rows16, None, FP16, d), fmt, bits, bounds32, centroids32, proj)
 
 
 def decode(rows, aux, fmt, s, d, bits=0, centroids32=None) -> np.ndarray:
