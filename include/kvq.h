@@ -175,6 +175,28 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
                                        const uint16_t* v, int32_t num_tokens,
                                        const int32_t* slot_mapping, void* stream);
 
+/* Move tokens from an fp16 tier into another tier, re-encoding their rows: the recent-token
+ * window of FoveatedKV's fused kernel ("Making it fast": the unquantised decode buffer in
+ * the same dispatch) and AdapTQ's hybrid execution ("Hybrid Execution: The Best of Both
+ * Worlds": short contexts stay unquantised, tokens switch to the quantised path past a
+ * threshold).  A caller keeps the newest tokens of each sequence in an fp16 tier (appended
+ * with kvq_quantize_append, attended with the other tiers in one kvq_decode_attention call)
+ * and moves the oldest ones out with this call once the window is full.
+ *   src       : host pointer; both sides KVQ_FMT_FP16 (it stores the rotated vector x~)
+ *   src_slots : int32 [num_tokens] pool slots of the tokens in src
+ *   dst       : host pointer; any formats; same head_dim, num_kv_heads, page_size and the
+ *               same K and V sign vectors as src (else KVQ_ERR_INVALID_ARGUMENT)
+ *   dst_slots : int32 [num_tokens] destination slots
+ * Token i's K and V rows of every kv head are read at src_slots[i] and written, encoded in
+ * dst's formats, at dst_slots[i]: the encode of the stored fp16 x~, with no second
+ * rotation (so a codebook row of a moved token can differ from appending the original x
+ * directly where the fp16 rounding of x~ crosses a decision boundary).  A token whose src
+ * or dst slot is negative or out of range is skipped.  src is left unchanged.  A src
+ * that is not fp16 returns KVQ_ERR_UNSUPPORTED. */
+KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots,
+                                  const kvq_cache* dst, const int32_t* dst_slots,
+                                  int32_t num_tokens, void* stream);
+
 /* Workspace bytes kvq_decode_attention needs for these tiers and shapes (host output).
  * split_tokens: tokens per split-K chunk (a multiple of page_size), or 0 to let the
  * library choose; pass the same value to kvq_decode_attention.  The chunks of the longest
@@ -184,9 +206,10 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
                                              int32_t batch, int32_t num_q_heads,
                                              int32_t split_tokens, size_t* bytes);
 
-/* Decode attention for one new query per sequence over all tiers (a split-K pass -- one
- * launch for every tier on the fp16 and fp8 + INT4 path, one launch per tier on the
- * codebook path -- then a combine pass):
+/* Decode attention for one new query per sequence over all tiers (a split-K pass, then a
+ * combine pass).  Each tier goes to the kernel family that fits its formats: fp16/fp16 and
+ * fp8/INT4 tiers (D = 128, 1, 2 or 4 query heads per kv head) share one fused launch,
+ * codebook tiers take one launch each, anything else the generic kernel:
  *   out[b][h] = softmax_t( q[b][h] . K[t] / sqrt(D) ) V[t]
  * over every cached token t < seq_lens[b] of every tier of kv head h / (Hq / Hkv), where
  * K[t], V[t] are the dequantised cache rows with the rotation undone; keys stored as

@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "kvq_uniform_codebook": [i32, dp, dp],
             "kvq_codebook_tables": [i32, dp, fp, fp],
             "kvq_quantize_append": [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp],
+            "kvq_requantize": [ctypes.POINTER(KvqCache), vp, ctypes.POINTER(KvqCache), vp, i32, vp],
             "kvq_decode_workspace_size": [ctypes.POINTER(KvqTierView), i32, i32, i32, i32, szp],
             "kvq_decode_attention": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz, vp],
             "kvq_decode_attention_ex": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz,
@@ -187,6 +188,14 @@ def kvq_quantize_append(cache: KvqCache, k, v, slot_mapping, stream=None) -> Non
     t = (k if k is not None else v).shape[0]
     _check(lib().kvq_quantize_append(ctypes.byref(cache), _ptr(k), _ptr(v), t, _ptr(slot_mapping),
                                      _stream(stream)), "kvq_quantize_append")
+
+
+def kvq_requantize(src: KvqCache, src_slots, dst: KvqCache, dst_slots, stream=None) -> None:
+    """Move tokens from an fp16 tier (a recent-token window) into another tier, re-encoding
+    their rows; src_slots / dst_slots: int32 CUDA tensors [T]."""
+    _dense(src_slots, dst_slots)
+    _check(lib().kvq_requantize(ctypes.byref(src), _ptr(src_slots), ctypes.byref(dst), _ptr(dst_slots),
+                                int(src_slots.shape[0]), _stream(stream)), "kvq_requantize")
 
 
 def _views(tiers: Sequence["TierView"]):

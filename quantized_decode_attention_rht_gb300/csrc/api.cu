@@ -73,13 +73,11 @@ int side_row_bytes(int fmt, int bits, int d) {
 }
 
 // Split-K plan: tokens per chunk for each tier (a multiple of page_size).
-enum PlanKind { PLAN_GENERIC = 0, PLAN_GQA, PLAN_CB };
-
 struct Plan {
   int chunk[KVQ_MAX_TIERS];
   int splits[KVQ_MAX_TIERS];
+  int kind[KVQ_MAX_TIERS];  // TierKind: which kernel family runs the tier
   int total;
-  PlanKind kind;  // GQA: the fused fp16 / fp8+INT4 kernel; CB: the fused codebook kernel
 };
 
 size_t token_bytes(const kvq_cache* c) {
@@ -89,34 +87,40 @@ size_t token_bytes(const kvq_cache* c) {
   return rk + ak + rv + av;
 }
 
-kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int split_tokens, Plan* plan) {
+// The kernel family of one tier: the fused fp16 / fp8 + INT4 kernel, the fused codebook
+// kernel, or the generic one.  q16: the queries are 16-byte aligned.
+int tier_kind(const kvq_cache* c, int group, int split_tokens, bool q16) {
+  const bool ps16 = c->page_size == 16;
+  if (ps16 && q16 && split_tokens <= gqa_max_chunk_tokens() &&
+      gqa_fast_supported(c->head_dim, group, c->k_format, c->v_format) && aligned(c->k_signs, 16) &&
+      aligned(c->v_signs, 16))
+    return TIER_GQA;
+  if (ps16 && cb_fast_supported(c->head_dim, group, c->k_format, c->v_format) && aligned(c->k_aux, 16) &&
+      aligned(c->v_aux, 16))  // bulk copies of the norm runs need 16-byte aligned sources
+    return TIER_CB;
+  return TIER_GENERIC;
+}
+
+kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int split_tokens, bool q16, Plan* plan) {
   const kvq_cache* c0 = tiers[0].cache;
   const int ps = c0->page_size, hkv = c0->num_kv_heads, group = hq / hkv;
   if (split_tokens < 0 || split_tokens % ps) return KVQ_ERR_INVALID_ARGUMENT;
-  bool gqa = ps == 16 && split_tokens <= gqa_max_chunk_tokens(), cb = ps == 16;
-  for (int i = 0; i < n; ++i) {
-    const kvq_cache* c = tiers[i].cache;
-    gqa = gqa && gqa_fast_supported(c0->head_dim, group, c->k_format, c->v_format);
-    cb = cb && cb_fast_supported(c0->head_dim, group, c->k_format, c->v_format);
-    // bulk copies of the norm runs need 16-byte aligned sources
-    cb = cb && aligned(c->k_aux, 16) && aligned(c->v_aux, 16);
-  }
-  // the fused fp16 / fp8 + INT4 kernel reads the sign vectors with 16-byte loads
-  gqa = gqa && aligned(c0->k_signs, 16) && aligned(c0->v_signs, 16);
-  plan->kind = gqa ? PLAN_GQA : (cb ? PLAN_CB : PLAN_GENERIC);
   // fused kernels: items of about equal bytes, several per warp of a full GPU
   size_t total_bytes = 0;
-  for (int i = 0; i < n; ++i)
+  for (int i = 0; i < n; ++i) {
+    plan->kind[i] = tier_kind(tiers[i].cache, group, split_tokens, q16);
     total_bytes += (size_t)batch * hkv * tiers[i].max_pages * ps * token_bytes(tiers[i].cache);
-  const size_t item_bytes = plan->kind == PLAN_GQA ? std::max<size_t>(64 << 10, total_bytes / (kSms * 8 * 4))
-                                                   : std::max<size_t>(16 << 10, total_bytes / (kSms * 12 * 6));
+  }
   plan->total = 0;
   for (int i = 0; i < n; ++i) {
     const long long max_len = (long long)tiers[i].max_pages * ps;
+    const int kind = plan->kind[i];
     int chunk = split_tokens;
-    if (chunk == 0 && plan->kind != PLAN_GENERIC) {
+    if (chunk == 0 && kind != TIER_GENERIC) {
+      const size_t item_bytes = kind == TIER_GQA ? std::max<size_t>(64 << 10, total_bytes / (kSms * 8 * 4))
+                                                 : std::max<size_t>(16 << 10, total_bytes / (kSms * 12 * 6));
       const size_t tok = item_bytes / token_bytes(tiers[i].cache);
-      const size_t cap = plan->kind == PLAN_GQA ? (size_t)gqa_max_chunk_tokens() : (size_t)1 << 20;
+      const size_t cap = kind == TIER_GQA ? (size_t)gqa_max_chunk_tokens() : (size_t)1 << 20;
       chunk = (int)std::min<size_t>(cap, std::max<size_t>(ps, tok / ps * ps));
     } else if (chunk == 0) {
       // aim at ~16 CTAs per SM in total, chunks of 256 .. 4096 tokens
@@ -169,16 +173,11 @@ kvq_status check_tiers(const kvq_tier_view* tiers, int n, int batch, int hq) {
       return KVQ_ERR_UNSUPPORTED;
     }
   }
-  // keys with a residual sketch run on the fused codebook kernel only: every tier attended
-  // with them must qualify for it
-  bool sketch = false, all_cb = c0->page_size == 16;
+  // keys with a residual sketch run on the fused codebook kernel only
   for (int i = 0; i < n; ++i) {
     const kvq_cache* c = tiers[i].cache;
-    sketch = sketch || c->k_format == KVQ_FMT_CODEBOOK_QJL;
-    all_cb = all_cb && cb_fast_supported(c->head_dim, g, c->k_format, c->v_format) && aligned(c->k_aux, 16) &&
-             aligned(c->v_aux, 16);
+    if (c->k_format == KVQ_FMT_CODEBOOK_QJL && tier_kind(c, g, 0, false) != TIER_CB) return KVQ_ERR_UNSUPPORTED;
   }
-  if (sketch && !all_cb) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -221,6 +220,68 @@ KVQ_API kvq_status kvq_row_bytes(int32_t format, int32_t bits, int32_t head_dim,
   return side_bytes(format, bits, head_dim, row_bytes, aux_bytes);
 }
 
+namespace {
+// The destination sides (K, V) of an append or a re-encode into cache c.
+void fill_sides(const kvq_cache* c, QuantParams* p) {
+  const int fmts[2] = {c->k_format, c->v_format}, bits[2] = {c->k_bits, c->v_bits};
+  void* rows[2] = {c->k_rows, c->v_rows};
+  void* aux[2] = {c->k_aux, c->v_aux};
+  const float* bnd[2] = {c->k_bounds, c->v_bounds};
+  const float* cnt[2] = {c->k_centroids, c->v_centroids};
+  const int8_t* sg[2] = {c->k_signs, c->v_signs};
+  for (int i = 0; i < 2; ++i) {
+    p->side[i].rows = static_cast<uint8_t*>(rows[i]);
+    p->side[i].aux = static_cast<__half*>(aux[i]);
+    p->side[i].bounds = bnd[i];
+    p->side[i].centroids = cnt[i];
+    p->side[i].qjl = i == 0 ? c->k_qjl : nullptr;
+    p->side[i].signs = sg[i];
+    p->side[i].fmt = fmts[i];
+    p->side[i].bits = bits[i];
+    p->side[i].row_bytes = side_row_bytes(fmts[i], bits[i], c->head_dim);
+  }
+}
+}  // namespace
+
+KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots, const kvq_cache* dst,
+                                  const int32_t* dst_slots, int32_t num_tokens, void* stream) {
+  kvq_status st = check_cache(src);
+  if (st != KVQ_OK || (st = check_cache(dst)) != KVQ_OK) return st;
+  if (num_tokens < 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (src->k_format != KVQ_FMT_FP16 || src->v_format != KVQ_FMT_FP16) return KVQ_ERR_UNSUPPORTED;
+  if (src->head_dim != dst->head_dim || src->num_kv_heads != dst->num_kv_heads ||
+      src->page_size != dst->page_size || src->k_signs != dst->k_signs || src->v_signs != dst->v_signs)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!src->k_rows || !src->v_rows || !aligned(src->k_rows, 16) || !aligned(src->v_rows, 16))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  const kvq_cache* c = dst;
+  if ((st = check_side(c, c->k_format, c->k_bits, c->k_rows, c->k_aux, c->k_centroids, c->k_bounds, c->k_signs,
+                       true, true)) != KVQ_OK ||
+      (st = check_side(c, c->v_format, c->v_bits, c->v_rows, c->v_aux, c->v_centroids, c->v_bounds, c->v_signs,
+                       true, false)) != KVQ_OK)
+    return st;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!src_slots || !dst_slots || !aligned(src_slots, 4) || !aligned(dst_slots, 4)) return KVQ_ERR_INVALID_ARGUMENT;
+  QuantParams p;
+  memset(&p, 0, sizeof(p));
+  fill_sides(dst, &p);
+  p.src_rows[0] = static_cast<const uint8_t*>(src->k_rows);
+  p.src_rows[1] = static_cast<const uint8_t*>(src->v_rows);
+  p.src_slots = src_slots;
+  p.src_num_slots = src->num_pages * src->page_size;
+  p.slots = dst_slots;
+  p.num_tokens = num_tokens;
+  p.hkv = dst->num_kv_heads;
+  p.page_size = dst->page_size;
+  p.num_slots = dst->num_pages * dst->page_size;
+  p.kind_first = 0;
+  p.num_kinds = 2;
+  p.num_vectors = 2LL * num_tokens * dst->num_kv_heads;
+  if (p.num_slots == 0 || p.src_num_slots == 0) return KVQ_OK;
+  cudaError_t e = launch_requantize(p, dst->head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k, const uint16_t* v,
                                        int32_t num_tokens, const int32_t* slot_mapping, void* stream) {
   kvq_status st = check_cache(cache);
@@ -240,23 +301,7 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
   memset(&p, 0, sizeof(p));
   p.x[0] = k;
   p.x[1] = v;
-  const int fmts[2] = {c->k_format, c->v_format}, bits[2] = {c->k_bits, c->v_bits};
-  void* rows[2] = {c->k_rows, c->v_rows};
-  void* aux[2] = {c->k_aux, c->v_aux};
-  const float* bnd[2] = {c->k_bounds, c->v_bounds};
-  const float* cnt[2] = {c->k_centroids, c->v_centroids};
-  const int8_t* sg[2] = {c->k_signs, c->v_signs};
-  for (int i = 0; i < 2; ++i) {
-    p.side[i].rows = static_cast<uint8_t*>(rows[i]);
-    p.side[i].aux = static_cast<__half*>(aux[i]);
-    p.side[i].bounds = bnd[i];
-    p.side[i].centroids = cnt[i];
-    p.side[i].qjl = i == 0 ? c->k_qjl : nullptr;
-    p.side[i].signs = sg[i];
-    p.side[i].fmt = fmts[i];
-    p.side[i].bits = bits[i];
-    p.side[i].row_bytes = side_row_bytes(fmts[i], bits[i], c->head_dim);
-  }
+  fill_sides(c, &p);
   p.slots = slot_mapping;
   p.num_tokens = num_tokens;
   p.hkv = c->num_kv_heads;
@@ -276,7 +321,7 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
   kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
   if (st != KVQ_OK) return st;
   Plan plan;
-  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, &plan)) != KVQ_OK) return st;
+  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, true, &plan)) != KVQ_OK) return st;
   *bytes = workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total, has_sketch(tiers, num_tiers));
   return KVQ_OK;
 }
@@ -300,7 +345,8 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
   const kvq_cache* c0 = tiers[0].cache;
   const int d = c0->head_dim, hkv = c0->num_kv_heads;
   Plan plan;
-  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, &plan)) != KVQ_OK) return st;
+  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, aligned(q, 16), &plan)) != KVQ_OK)
+    return st;
   const bool sketch = has_sketch(tiers, num_tiers);
   const size_t need = workspace_bytes(batch, num_q_heads, d, plan.total, sketch);
   if (need > 0 && (!workspace || !aligned(workspace, 256))) return KVQ_ERR_INVALID_ARGUMENT;
@@ -332,6 +378,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
     t.split_begin = at;
     t.num_splits = plan.splits[i];
     t.chunk = plan.chunk[i];
+    t.kind = plan.kind[i];
     at += plan.splits[i];
   }
   p.q = reinterpret_cast<const __half*>(q);
@@ -351,12 +398,17 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
   p.hkv = hkv;
   p.page_size = c0->page_size;
   p.total_splits = plan.total;
-  int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + need - 256);
+  // one split-K launch per kernel family present (the fused fp16 / fp8 + INT4 kernel takes
+  // all its tiers at once, the codebook and generic kernels one launch per tier), all
+  // writing partials into the one workspace, then the combine pass over every tier
+  int* counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + need - 256);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (plan.kind == PLAN_GQA && aligned(q, 16)) e = launch_decode_gqa(p, counter, s);
-  else if (plan.kind == PLAN_CB) e = launch_decode_cb(p, d, counter, s);
-  else e = launch_decode(p, d, num_q_heads / hkv, s);
+  bool fam[3] = {false, false, false};
+  for (int i = 0; i < num_tiers; ++i) fam[plan.kind[i]] = true;
+  cudaError_t e = cudaMemsetAsync(counters, 0, 256, s);  // work counters and the error word
+  if (e == cudaSuccess && fam[TIER_GQA]) e = launch_decode_gqa(p, counters + kGqaCounter, s);
+  if (e == cudaSuccess && fam[TIER_CB]) e = launch_decode_cb(p, d, counters, s);
+  if (e == cudaSuccess && fam[TIER_GENERIC]) e = launch_decode(p, d, num_q_heads / hkv, s);
   if (e == cudaSuccess) e = launch_combine(p, d, s);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

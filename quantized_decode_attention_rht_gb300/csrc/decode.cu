@@ -504,6 +504,7 @@ cudaError_t launch_tier_fmt(const DecParams& p, int ti, cudaStream_t stream) {
 template <int D>
 cudaError_t launch_decode_d(const DecParams& p, int group, cudaStream_t stream) {
   for (int ti = 0; ti < p.num_tiers; ++ti) {
+    if (p.tier[ti].kind != TIER_GENERIC) continue;
     cudaError_t e;
     switch (group) {
       case 1: e = launch_tier_fmt<D, 1>(p, ti, stream); break;

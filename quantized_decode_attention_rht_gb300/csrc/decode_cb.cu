@@ -16,12 +16,11 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(counters, 0, 64 * sizeof(int), stream);  // work counters and the error word
-  if (e != cudaSuccess) return e;
   const int group = dp.hq / dp.hkv;
   bool projected = false;  // every sketched tier shares the projection and the queries
   for (int i = 0; i < dp.num_tiers; ++i) {
     const DecTier& t = dp.tier[i];
+    if (t.kind != TIER_CB) continue;
     cbk::CbParams p;
     memset(&p, 0, sizeof(p));
     p.t.k_rows = t.k_rows;
@@ -46,7 +45,7 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.gate = dp.gate;
     p.track = dp.spike != nullptr && i == 0;
     p.counter = counters + i;
-    p.err = counters + cbk::kErrorWord;
+    p.err = counters + kCbErrorWord;
     p.hq = dp.hq;
     p.hkv = dp.hkv;
     p.total_splits = dp.total_splits;

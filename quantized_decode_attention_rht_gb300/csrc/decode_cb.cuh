@@ -64,7 +64,6 @@ constexpr float kQScale = 64.0f;   // the rotated queries hold 2^6 q'
 constexpr float kWScale = 8.0f;    // weight fragments hold 2^3 p norm / sqrt(D); with p <= 1
                                    // every fp16 norm stays below the fp16 maximum
 constexpr int kSpinLimit = 1 << 22;  // try_wait rounds before a slot counts as lost
-constexpr int kErrorWord = 32;       // index of the error word in the counter block
 typedef unsigned long long u64;
 
 // ---------------------------------------------------------------- PTX helpers

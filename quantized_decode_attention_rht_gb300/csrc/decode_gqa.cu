@@ -1,6 +1,7 @@
-// Fused decode attention for GQA groups of 4 query heads, head_dim 128, over fp16 tiers
-// (FoveatedKV near tier) and fp8-E4M3-key / INT4-g32-value tiers (far tier), every tier in
-// one launch ("Making it fast", FoveatedKV page: both tiers in a single dispatch).
+// Fused decode attention for groups of 1, 2 or 4 query heads per kv head, head_dim 128, over
+// fp16 tiers (FoveatedKV near tier, or a recent-token window) and fp8-E4M3-key /
+// INT4-g32-value tiers (far tier), all of them in one launch ("Making it fast", FoveatedKV
+// page: both tiers and the decode buffer in a single dispatch).
 //
 // Work: items of (tier, sequence, kv head, chunk of pages) with about equal bytes, handed
 // to warps from an atomic counter; 12 warps per SM.  Each warp is independent: it owns a
@@ -8,8 +9,9 @@
 // by 16 bytes so every fragment load below is free of bank conflicts), and writes one
 // split-K partial (running max, sum, rotated-domain accumulator) per item.
 //
-// The G = 4 query heads of a kv head form a real contraction with every key and value
-// row, done with mma.sync.m16n8k16 (fp16 inputs, fp32 accumulation):
+// The query heads of a kv head (up to G = 4; smaller groups leave zero columns) form a real
+// contraction with every key and value row, done with mma.sync.m16n8k16 (fp16 inputs, fp32
+// accumulation):
 //   scores  S[16 tokens x 8] = K[16 tokens x 128] . Qt[128 x 8]
 //   values  O[16 dims x 8]  += V^T[16 dims x 16 tokens] . Pt[16 tokens x 8]
 // The 8 columns are (head, hi/lo): the rotated query q' and the weights p are split into
@@ -31,7 +33,7 @@
 namespace kvq {
 namespace {
 
-constexpr int D = 128, G = 4, PS = 16;
+constexpr int D = 128, G = 4, PS = 16;  // G: query heads one item can carry (a group of 1, 2 or 4)
 constexpr int kWarps = 12;
 constexpr int kWarpSmem = 19360;               // per warp: stage ring + block-table slice
 constexpr int kMaxPagesPerItem = 128;
@@ -127,7 +129,8 @@ struct GqaTier {
   const __half* v_aux;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  int far;  // 1: fp8 K + INT4-g32 V; 0: fp16 K + fp16 V
+  int far;    // 1: fp8 K + INT4-g32 V; 0: fp16 K + fp16 V
+  int first;  // tier 0 of the call (the near tier of spike detection)
   int max_pages, chunk, nchunks, split_begin, item_begin;
 };
 
@@ -141,6 +144,7 @@ struct GqaParams {
   float* ws_min;  // lowest score per tier-0 split, when spike flags are asked for
   int* counter;
   int hq, hkv, total_splits, total_items;
+  int group;        // query heads per kv head (1, 2 or 4); heads group.. of an item are idle
   int gate, spike;  // score-gated value loading; track tier 0's lowest scores
 };
 
@@ -151,8 +155,10 @@ struct GqaParams {
 // three across the 8 lanes of the head.
 __device__ __forceinline__ void rotate_query(const GqaParams& p, int b, int hk, float* qbuf, int lane) {
   const int hh = lane >> 3, d0 = (lane & 7) * 16;
-  const uint4* qs = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.hq + hk * G + hh) * D + d0);
-  const uint4 q0 = __ldg(qs), q1 = __ldg(qs + 1);
+  const bool live = hh < p.group;  // idle heads get a zero query (zero B columns)
+  const uint4* qs = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.hq + hk * p.group + (live ? hh : 0)) * D + d0);
+  uint4 q0 = __ldg(qs), q1 = __ldg(qs + 1);
+  if (!live) q0 = q1 = make_uint4(0u, 0u, 0u, 0u);
   const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.k_signs + hk * D + d0));
   const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
   const int8_t* sb = reinterpret_cast<const int8_t*>(&sg);
@@ -270,7 +276,7 @@ struct Far {
   }
 
   __device__ static void page(const uint8_t* st, int nvalid, const uint32_t (&qf)[8][2], State& s, int lane,
-                              bool track, bool gate) {
+                              bool track, bool gate, bool live) {
     const int g = lane >> 2, c = lane & 3;
     const uint32_t s0 = smem_addr(st);
     // ---- scores
@@ -305,8 +311,8 @@ struct Far {
     const float p1 = v1 ? exp2f(x1 - s.m) : 0.f;
     s.l += p0 + p1;
     if (track) s.mn = fminf(s.mn, page_min(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY));
-    // score gate: every token of the page, for all four heads, far below the running max
-    if (gate && __all_sync(kFull, mt - s.m < -kGateLog2)) return;
+    // score gate: every token of the page, for every live head, far below the running max
+    if (gate && __all_sync(kFull, !live || mt - s.m < -kGateLog2)) return;
     // ---- weights w = p * scale (x 2^8) per group for this lane's tokens (g, g+8), head c
     const uint2 sc0 = lds64(s0 + F_S + 8 * g), sc1 = lds64(s0 + F_S + 8 * (g + 8));
     const __half2* h0 = reinterpret_cast<const __half2*>(&sc0);
@@ -380,10 +386,11 @@ struct Far {
   }
 
   // Partial for head c: acc[32a + 4g + k] = sum_t p_t s_ta (u - 8), relative to the max.
-  __device__ static void finish(State& s, float* acc_out, float* ml_out, float* mn_out, int lane) {
+  __device__ static void finish(State& s, float* acc_out, float* ml_out, float* mn_out, int lane, bool live) {
     const int g = lane >> 2;
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) s.l += __shfl_xor_sync(kFull, s.l, o);
+    if (!live) return;  // an idle head of a group smaller than 4
     constexpr float even = 1.0f / kWScale, odd = 1.0f / (kWScale * 16.0f);
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -456,7 +463,7 @@ struct Near {
   }
 
   __device__ static void page(const uint8_t* st, int nvalid, const uint32_t (&qf)[8][2], State& s, int lane,
-                              bool track, bool gate) {
+                              bool track, bool gate, bool live) {
     const int g = lane >> 2, c = lane & 3;
     const uint32_t s0 = smem_addr(st);
     const int t = lane & 7, mi = lane >> 3;
@@ -492,7 +499,7 @@ struct Near {
     const float p1 = v1 ? exp2f(x1 - s.m) : 0.f;
     s.l += p0 + p1;
     if (track) s.mn = fminf(s.mn, page_min(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY));
-    if (gate && __all_sync(kFull, mt - s.m < -kGateLog2)) return;  // score gate (see Far)
+    if (gate && __all_sync(kFull, !live || mt - s.m < -kGateLog2)) return;  // score gate (see Far)
     const int srcA = 4 * (2 * c) + (g >> 1), srcB = srcA + 4;
     const float q0 = p0 * kWScale, q1 = p1 * kWScale;
     const uint32_t hi = pack_f16x2(q0, q1);
@@ -513,10 +520,11 @@ struct Near {
     }
   }
 
-  __device__ static void finish(State& s, float* acc_out, float* ml_out, float* mn_out, int lane) {
+  __device__ static void finish(State& s, float* acc_out, float* ml_out, float* mn_out, int lane, bool live) {
     const int g = lane >> 2;
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) s.l += __shfl_xor_sync(kFull, s.l, o);
+    if (!live) return;  // an idle head of a group smaller than 4
     constexpr float unw = 1.0f / kWScale;
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
@@ -562,14 +570,15 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
     __syncwarp();
     const int slot = i % TT::S;
     const int nvalid = min(PS, t1 - (pg0 + i) * PS);
-    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0);
+    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.group);
     __syncwarp();
     if (i + TT::S < npg) TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
     cp_commit();
   }
   cp_wait<0>();
-  const size_t part = ((size_t)b * p.hq + hk * G + c) * p.total_splits + T.split_begin + chunk;
-  TT::finish(st, p.ws_acc + part * D, p.ws_ml + 2 * part, track ? p.ws_min + part : nullptr, lane);
+  const bool live = c < p.group;
+  const size_t part = live ? ((size_t)b * p.hq + hk * p.group + c) * p.total_splits + T.split_begin + chunk : 0;
+  TT::finish(st, p.ws_acc + part * D, p.ws_ml + 2 * part, track ? p.ws_min + part : nullptr, lane, live);
   __syncwarp();
 }
 
@@ -594,7 +603,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
     const int t0 = chunk * T.chunk;
     if (t0 < len) {
       const int t1 = min(len, t0 + T.chunk);
-      const bool track = p.spike && ti == 0;
+      const bool track = p.spike && T.first;
       if (T.far) run_item<Far>(p, T, b, hk, chunk, t0, t1, wsm, lane, track);
       else run_item<Near>(p, T, b, hk, chunk, t0, t1, wsm, lane, track);
     }
@@ -605,7 +614,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
 }  // namespace
 
 bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
-  if (head_dim != D || group != G) return false;
+  if (head_dim != D || (group != 1 && group != 2 && group != 4)) return false;
   return (k_fmt == KVQ_FMT_FP16 && v_fmt == KVQ_FMT_FP16) || (k_fmt == KVQ_FMT_FP8_E4M3 && v_fmt == KVQ_FMT_INT4_G32);
 }
 
@@ -625,11 +634,12 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
   }
   GqaParams p;
   memset(&p, 0, sizeof(p));
-  p.num_tiers = dp.num_tiers;
-  int items = 0;
+  int items = 0, n = 0;
   for (int i = 0; i < dp.num_tiers; ++i) {
     const DecTier& t = dp.tier[i];
-    GqaTier& g = p.tier[i];
+    if (t.kind != TIER_GQA) continue;
+    GqaTier& g = p.tier[n++];
+    g.first = i == 0;
     g.k_rows = t.k_rows;
     g.v_rows = t.v_rows;
     g.v_aux = t.v_aux;
@@ -643,6 +653,8 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
     g.item_begin = items;
     items += dp.batch * dp.hkv * t.num_splits;
   }
+  p.num_tiers = n;
+  p.group = dp.hq / dp.hkv;
   p.q = dp.q;
   p.k_signs = dp.k_signs;
   p.ws_acc = dp.ws_acc;
@@ -660,8 +672,6 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int ctas = std::max(1, std::min(sms, (items + kWarps - 1) / kWarps));
-  e = cudaMemsetAsync(counter, 0, sizeof(int), stream);
-  if (e != cudaSuccess) return e;
   decode_gqa_kernel<<<ctas, kWarps * 32, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();

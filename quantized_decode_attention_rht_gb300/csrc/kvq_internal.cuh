@@ -33,11 +33,25 @@ struct QuantParams {
   int num_tokens, hkv, page_size, num_slots;
   int kind_first, num_kinds;  // kinds present: [kind_first, kind_first + num_kinds)
   long long num_vectors;      // num_kinds * num_tokens * hkv
+  // re-encode of stored fp16 rows (kvq_requantize) instead of new vectors: the source
+  // pool's K and V rows (rotated fp16, same page size and kv heads) and slots
+  const uint8_t* src_rows[2];
+  const int32_t* src_slots;
+  int src_num_slots;
 };
 
 cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t stream);
+// Re-encode: one warp per vector, every destination format.
+cudaError_t launch_requantize(const QuantParams& p, int head_dim, cudaStream_t stream);
 
 // ------------------------------------------------------------------------ decode
+// Kernel family of a decode tier (chosen per tier on the host).
+enum TierKind { TIER_GENERIC = 0, TIER_GQA = 1, TIER_CB = 2 };
+// The 256-byte counter block at the end of the decode workspace (cleared once per call):
+// ints [0, KVQ_MAX_TIERS) codebook work counters, kCbErrorWord the codebook kernel's error
+// word, kGqaCounter the fused fp16 / fp8 + INT4 kernel's work counter.
+constexpr int kCbErrorWord = 32, kGqaCounter = 40;
+
 struct DecTier {
   const uint8_t* k_rows;
   const uint8_t* v_rows;
@@ -49,6 +63,7 @@ struct DecTier {
   const int32_t* block_table;
   const int32_t* seq_lens;
   int k_fmt, v_fmt, k_bits, v_bits, k_row_bytes, v_row_bytes;
+  int kind;  // TierKind
   int max_pages, split_begin, num_splits, chunk;
 };
 
@@ -70,18 +85,20 @@ struct DecParams {
 
 constexpr float kGateLog2 = 23.083120654223414f;  // KVQ_SCORE_GATE_NATS * log2(e): scores are base-2
 
+// Split-K launchers: each runs the tiers of its family (DecTier::kind) and skips the rest.
+// Generic kernel, every format pair: one launch per tier.
 cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStream_t stream);
-// Fused tensor-core decode for head_dim 128, 4 query heads per kv head, tiers stored as
-// fp16/fp16 or fp8-E4M3/INT4-g32 (one launch for every tier).  `counter` is one int of
-// device scratch, cleared by the launcher.
+// Fused tensor-core decode for head_dim 128, 1, 2 or 4 query heads per kv head, tiers stored
+// as fp16/fp16 or fp8-E4M3/INT4-g32 (one launch for all of them).  `counter`: one int of
+// device scratch, zero at launch.
 bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
 int gqa_max_chunk_tokens();
 cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t stream);
 // Fused tensor-core decode over codebook tiers (codebook K and V), head_dim 128 or 256,
 // 1, 2 or 4 query heads per kv head; one launch per tier (after one projection launch when
-// a tier's keys carry a sketch).  `counters` is 64 ints (256 bytes)
-// of device scratch, cleared by the launcher: one work counter per tier, and at index 32 an
-// error word that a kernel sets when a wait for its own bulk copies gives up.
+// a tier's keys carry a sketch).  `counters`: the 256-byte counter block, zero at launch
+// (ints [0, KVQ_MAX_TIERS) work counters, kCbErrorWord set when a wait for one of the
+// kernel's own bulk copies gives up).
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
 cudaError_t launch_decode_cb(const DecParams& p, int head_dim, int* counters, cudaStream_t stream);
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream);

@@ -71,6 +71,29 @@ __device__ __forceinline__ void load_rotate(const uint16_t* src, const int8_t* s
   }
 }
 
+// y = x~ for the lane's coordinates, from a stored fp16 row of the rotated vector.
+template <int E>
+__device__ __forceinline__ void load_row(const uint8_t* row, int lane, float (&y)[E]) {
+  uint32_t xw[E / 2];
+  if constexpr (E == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * lane);
+    xw[0] = u.x;
+    xw[1] = u.y;
+  } else {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + 16 * lane);
+    xw[0] = u.x;
+    xw[1] = u.y;
+    xw[2] = u.z;
+    xw[3] = u.w;
+  }
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) {
+    const __half2 h2 = *reinterpret_cast<const __half2*>(&xw[k]);
+    y[2 * k] = __low2float(h2);
+    y[2 * k + 1] = __high2float(h2);
+  }
+}
+
 // The lane's E fields of `bits` bits each (coordinate order) into the row's little-endian
 // bit stream; `buf` is the warp's shared staging area (D * bits / 32 words).
 template <int D, int E, int BITS>
@@ -126,12 +149,16 @@ __device__ __forceinline__ uint4 sketch_words(const float* __restrict__ proj, co
   return make_uint4(zw[0], zw[1], zw[2], zw[3]);
 }
 
-template <int D, int FMT, int BITS>
+// FROM_ROWS: the vectors are stored fp16 rows of x~ (src, re-encode) rather than new fp16
+// inputs x to rotate.  y is H s x (= sqrt(D) x~) for new inputs and x~ itself for stored
+// rows; ys maps y to x~.  Codes and the norm direction do not depend on the scale of y.
+template <int D, int FMT, int BITS, bool FROM_ROWS>
 __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSide& side, const uint16_t* x,
-                                            uint32_t* buf) {
+                                            const uint8_t* src, uint32_t* buf) {
   constexpr int E = D / 32;
   constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
   constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
+  constexpr float ys = FROM_ROWS ? 1.0f : inv_sqrt_d;
   constexpr int NB = (FMT == F_CB || FMT == F_CBQ) ? (1 << BITS) - 1 : 1;
   const int lane = threadIdx.x & 31;
   float bnd[NB];
@@ -145,7 +172,14 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
     const int slot = p.slots[token];
     if (slot < 0 || slot >= p.num_slots) continue;  // warp-uniform
     float y[E];
-    load_rotate<E>(x + (size_t)v * D, side.signs + (size_t)h * D, lane, y);
+    if constexpr (FROM_ROWS) {
+      const int ss = p.src_slots[token];
+      if (ss < 0 || ss >= p.src_num_slots) continue;
+      const size_t srow = ((size_t)(ss / p.page_size) * p.hkv + h) * p.page_size + (ss % p.page_size);
+      load_row<E>(src + srow * (2 * D), lane, y);
+    } else {
+      load_rotate<E>(x + (size_t)v * D, side.signs + (size_t)h * D, lane, y);
+    }
     const size_t prow = ((size_t)(slot / p.page_size) * p.hkv + h) * p.page_size + (slot % p.page_size);
     uint8_t* row = side.rows + prow * side.row_bytes;
     if constexpr (FMT == F_CB || FMT == F_CBQ) {
@@ -154,7 +188,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
       for (int e = 0; e < E; ++e) ss = fmaf(y[e], y[e], ss);
       const float ny = sqrtf(warp_sum(ss));
       const float inv = ny > 0.0f ? sqrt_d / ny : 0.0f;  // u = sqrt(D) y / ||y||
-      const __half norm16 = __float2half_rn(ny * inv_sqrt_d);
+      const __half norm16 = __float2half_rn(ny * ys);
       uint32_t fields = 0u;
       int idx[E];
 #pragma unroll
@@ -175,7 +209,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
         float rs = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          y[e] = fmaf(-dscale, __ldg(side.centroids + idx[e]), y[e] * inv_sqrt_d);
+          y[e] = fmaf(-dscale, __ldg(side.centroids + idx[e]), y[e] * ys);
           rs = fmaf(y[e], y[e], rs);
         }
         const float rn = sqrtf(warp_sum(rs));
@@ -189,7 +223,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
       uint32_t w[E / 2];
 #pragma unroll
       for (int k = 0; k < E / 2; ++k) {
-        const __half2 h2 = __floats2half2_rn(y[2 * k] * inv_sqrt_d, y[2 * k + 1] * inv_sqrt_d);
+        const __half2 h2 = __floats2half2_rn(y[2 * k] * ys, y[2 * k + 1] * ys);
         w[k] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       if constexpr (E == 4) reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
@@ -199,8 +233,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
 #pragma unroll
       for (int k = 0; k < E / 4; ++k) {
         const int e = 4 * k;
-        w[k] = float2_to_fp8x2(y[e] * inv_sqrt_d, y[e + 1] * inv_sqrt_d) |
-               (float2_to_fp8x2(y[e + 2] * inv_sqrt_d, y[e + 3] * inv_sqrt_d) << 16);
+        w[k] = float2_to_fp8x2(y[e] * ys, y[e + 1] * ys) | (float2_to_fp8x2(y[e + 2] * ys, y[e + 3] * ys) << 16);
       }
       if constexpr (E == 4) reinterpret_cast<uint32_t*>(row)[lane] = w[0];
       else reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
@@ -208,7 +241,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
       constexpr int LG = kGroup / E;
       float amax = 0.0f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e] * inv_sqrt_d));
+      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e] * ys));
 #pragma unroll
       for (int m = 1; m < LG; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, m));
       const __half s16 = __float2half_rn(amax / 7.0f);
@@ -217,7 +250,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
       uint32_t nib = 0u;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        const float xv = y[e] * inv_sqrt_d;
+        const float xv = y[e] * ys;
         // level = rint(x / s): x * (1/s) is within one ulp of the quotient; where that
         // leaves the result next to a half-integer, divide exactly
         float tq = xv * rcp;
@@ -232,44 +265,60 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
   }
 }
 
-template <int D, int FMT>
+template <int D, int FMT, bool FROM_ROWS>
 __device__ __forceinline__ void append_bits(const QuantParams& p, const QuantSide& side, const uint16_t* x,
-                                            uint32_t* buf) {
-  if (side.bits == 4) append_side<D, FMT, 4>(p, side, x, buf);
-  else if (side.bits == 3) append_side<D, FMT, 3>(p, side, x, buf);
-  else append_side<D, FMT, 2>(p, side, x, buf);
+                                            const uint8_t* src, uint32_t* buf) {
+  if (side.bits == 4) append_side<D, FMT, 4, FROM_ROWS>(p, side, x, src, buf);
+  else if (side.bits == 3) append_side<D, FMT, 3, FROM_ROWS>(p, side, x, src, buf);
+  else append_side<D, FMT, 2, FROM_ROWS>(p, side, x, src, buf);
 }
 
 // Grid row blockIdx.y = side kind_first + y; the format is a warp-uniform branch (only the
 // taken path's instructions are fetched).
-template <int D>
+template <int D, bool FROM_ROWS>
 __global__ void __launch_bounds__(kWarps * 32) append_kernel(const QuantParams p) {
   __shared__ __align__(16) uint32_t words[kWarps][32];
   const int kind = p.kind_first + blockIdx.y;  // 0 or 1
   const QuantSide side = kind ? p.side[1] : p.side[0];
   const uint16_t* x = kind ? p.x[1] : p.x[0];
+  const uint8_t* src = kind ? p.src_rows[1] : p.src_rows[0];
   uint32_t* buf = words[threadIdx.x >> 5];
   switch (side.fmt) {
-    case KVQ_FMT_CODEBOOK: append_bits<D, F_CB>(p, side, x, buf); break;
-    case KVQ_FMT_CODEBOOK_QJL: append_bits<D, F_CBQ>(p, side, x, buf); break;
-    case KVQ_FMT_FP16: append_side<D, F_F16, 0>(p, side, x, buf); break;
-    case KVQ_FMT_FP8_E4M3: append_side<D, F_F8, 0>(p, side, x, buf); break;
-    default: append_side<D, F_I4, 0>(p, side, x, buf); break;
+    case KVQ_FMT_CODEBOOK: append_bits<D, F_CB, FROM_ROWS>(p, side, x, src, buf); break;
+    case KVQ_FMT_CODEBOOK_QJL: append_bits<D, F_CBQ, FROM_ROWS>(p, side, x, src, buf); break;
+    case KVQ_FMT_FP16: append_side<D, F_F16, 0, FROM_ROWS>(p, side, x, src, buf); break;
+    case KVQ_FMT_FP8_E4M3: append_side<D, F_F8, 0, FROM_ROWS>(p, side, x, src, buf); break;
+    default: append_side<D, F_I4, 0, FROM_ROWS>(p, side, x, src, buf); break;
   }
+}
+
+template <bool FROM_ROWS>
+cudaError_t launch_warp_kernel(const QuantParams& p, int head_dim, int sms, cudaStream_t stream) {
+  const long long nvec = (long long)p.num_tokens * p.hkv;
+  const unsigned blocks =
+      (unsigned)std::max<long long>(1, std::min<long long>((nvec + kWarps - 1) / kWarps, (long long)sms * 8));
+  const dim3 grid(blocks, p.num_kinds);
+  if (head_dim == 128) append_kernel<128, FROM_ROWS><<<grid, kWarps * 32, 0, stream>>>(p);
+  else append_kernel<256, FROM_ROWS><<<grid, kWarps * 32, 0, stream>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_small(const QuantParams& p, int head_dim, int sms, cudaStream_t stream) {
-  const long long nvec = (long long)p.num_tokens * p.hkv;
-  const unsigned blocks =
-      (unsigned)std::max<long long>(1, std::min<long long>((nvec + kWarps - 1) / kWarps, (long long)sms * 8));
-  const dim3 grid(blocks, p.num_kinds);
-  if (head_dim == 128) append_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
-  else append_kernel<256><<<grid, kWarps * 32, 0, stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) note_launch();
-  return e;
+  return launch_warp_kernel<false>(p, head_dim, sms, stream);
+}
+
+cudaError_t launch_requantize(const QuantParams& p, int head_dim, cudaStream_t stream) {
+  if (p.num_tokens == 0) return cudaSuccess;
+  if ((long long)p.num_tokens * p.hkv > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  return launch_warp_kernel<true>(p, head_dim, sms, stream);
 }
 
 }  // namespace kvq

@@ -76,15 +76,21 @@ def pool_rows(tensor, slots):
 # ----------------------------------------------------------------------------- codes
 
 
-def check_codebook_codes(x16, signs, bits, rows_gpu, norms_gpu, kind="lloyd_max"):
-    """x16 [T, d] of one head, signs [d]; rows_gpu [T, row_bytes]; norms_gpu fp16 [T].
-    Returns (mismatches, near-boundary count, elements)."""
+def rotated(x16, signs, xr):
+    """The exact rotated vectors: of x16 with signs, or xr as given (a re-encode of stored
+    rows, whose input is already rotated)."""
+    return orot.rotate(x16.astype(np.float64), signs) if xr is None else np.asarray(xr, dtype=np.float64)
+
+
+def check_codebook_codes(x16, signs, bits, rows_gpu, norms_gpu, kind="lloyd_max", xr=None):
+    """x16 [T, d] of one head, signs [d] (or xr: the exact rotated vectors); rows_gpu
+    [T, row_bytes]; norms_gpu fp16 [T].  Returns (mismatches, near-boundary count, elements)."""
     c32, b32 = tables(kind, bits)
-    d = x16.shape[-1]
-    rows_o, norm_o = ocache.encode(x16, signs, "codebook", bits, b32)
+    xr = rotated(x16, signs, xr)
+    d = xr.shape[-1]
+    rows_o, norm_o = ocache.encode_rotated(xr, "codebook", bits, b32)
     idx_o = ofmt.unpack_bits(rows_o, bits, d)
     idx_g = ofmt.unpack_bits(rows_gpu, bits, d)
-    xr = orot.rotate(x16.astype(np.float64), signs)
     n = np.sqrt(np.sum(xr * xr, axis=-1))
     with np.errstate(divide="ignore", invalid="ignore"):
         u = np.where(n[:, None] > 0, math.sqrt(d) * xr / n[:, None], 0.0)
@@ -105,7 +111,7 @@ def check_codebook_codes(x16, signs, bits, rows_gpu, norms_gpu, kind="lloyd_max"
     return int(np.sum(bad)), int(np.sum(near)), idx_o.size, int(np.sum(diff))
 
 
-def check_qjl_rows(x16, signs, bits, proj, rows_gpu, aux_gpu, kind="lloyd_max"):
+def check_qjl_rows(x16, signs, bits, proj, rows_gpu, aux_gpu, kind="lloyd_max", xr=None):
     """Keys with a residual sign sketch: x16 [T, d] of one head, proj float32 [m, d];
     rows_gpu [T, row_bytes]; aux_gpu fp16 [T, 2].
 
@@ -117,13 +123,13 @@ def check_qjl_rows(x16, signs, bits, proj, rows_gpu, aux_gpu, kind="lloyd_max"):
     Rows whose codes or norm differ carry a different residual and are checked only for
     their codes.  Returns (rows compared, sign bits differing, residual norms differing)."""
     c32, b32 = tables(kind, bits)
-    d = x16.shape[-1]
+    xr = rotated(x16, signs, xr)
+    d = xr.shape[-1]
     nb = d * bits // 8
     aux_gpu = np.asarray(aux_gpu, dtype=np.float16)
-    check_codebook_codes(x16, signs, bits, rows_gpu[:, :nb], aux_gpu[:, 0], kind)
-    rows_o, aux_o = ocache.encode(x16, signs, "codebook_qjl", bits, b32, c32, proj)
+    check_codebook_codes(None, None, bits, rows_gpu[:, :nb], aux_gpu[:, 0], kind, xr=xr)
+    rows_o, aux_o = ocache.encode_rotated(xr, "codebook_qjl", bits, b32, c32, proj)
     same = np.all(rows_gpu[:, :nb] == rows_o[:, :nb], axis=-1) & (aux_gpu[:, 0] == aux_o[:, 0])
-    xr = orot.rotate(x16.astype(np.float64), signs)
     r = xr - ocache.decode_rotated(rows_o, aux_o, "codebook_qjl", d, bits, c32)
     s64 = np.asarray(proj, dtype=np.float32).astype(np.float64)
     sr = r @ s64.T
@@ -139,14 +145,14 @@ def check_qjl_rows(x16, signs, bits, proj, rows_gpu, aux_gpu, kind="lloyd_max"):
     return int(np.sum(same)), int(np.sum(bad)), int(np.sum(rdiff))
 
 
-def check_float_rows(x16, signs, fmt, rows_gpu):
+def check_float_rows(x16, signs, fmt, rows_gpu, xr=None):
     """fp16 / fp8 rows: every stored value must be the format's rounding of SOME value within
     the kernel's rotation error tau of the exact rotated coordinate, i.e. lie between the
     roundings of x~ - tau and x~ + tau (rounding is monotone; +0 and -0 compare equal).
     Returns (values differing from the oracle's, values)."""
-    rows_o, _ = ocache.encode(x16, signs, fmt)
-    xr = orot.rotate(x16.astype(np.float64), signs)
-    tau = fwht_error_bound(x16)[:, None]
+    tau = fwht_error_bound(x16)[:, None] if xr is None else np.zeros((len(xr), 1))  # stored rows: exact input
+    xr = rotated(x16, signs, xr)
+    rows_o, _ = ocache.encode_rotated(xr, fmt)
     if fmt == "fp16":
         def rnd(z):
             return ofmt.to_f16(z).astype(np.float64)
@@ -165,16 +171,15 @@ def check_float_rows(x16, signs, fmt, rows_gpu):
     return int(np.sum(vo != vg)), vo.size
 
 
-def check_int4_rows(x16, signs, rows_gpu, scales_gpu):
+def check_int4_rows(x16, signs, rows_gpu, scales_gpu, xr=None):
     """INT4-g32 rows: each stored scale must be the rounding of max|x~|/7 for some max within
     tau of the exact one, and each level the rounding of (x~ +- tau) / s with the scale the
     GPU stored (plus one float32 rounding of the quotient).  Returns (levels differing from the
     oracle's, scales differing, levels)."""
-    d = x16.shape[-1]
-    n = len(x16)
-    rows_o, sc_o = ocache.encode(x16, signs, "int4_g32")
-    xr = orot.rotate(x16.astype(np.float64), signs)
-    tau = fwht_error_bound(x16)[:, None]
+    tau = fwht_error_bound(x16)[:, None] if xr is None else np.zeros((len(xr), 1))
+    xr = rotated(x16, signs, xr)
+    n, d = xr.shape
+    rows_o, sc_o = ocache.encode_rotated(xr, "int4_g32")
     g = xr.reshape(n, d // 32, 32)
     amax = np.max(np.abs(g), axis=-1)
     s_lo = ofmt.to_f16(ofmt.to_f32(np.maximum(amax - tau, 0) / 7)).astype(np.float64)

@@ -185,8 +185,30 @@ def test_qjl_key_checks(kvq):
     assert _ws(kvq, [_qjl_cache(kvq, head_dim=256)])[0] == 2  # the sketched decode is built for D=128
     assert _ws(kvq, [_qjl_cache(kvq, v_format=kvq.FMT_FP16, v_bits=0)])[0] == 2
     assert _ws(kvq, [_qjl_cache(kvq), _fake_cache(kvq)])[0] == 0  # with a plain codebook tier
+    # a tier of another kernel family runs on its own kernel in the same call
     assert _ws(kvq, [_qjl_cache(kvq), _fake_cache(kvq, k_format=kvq.FMT_FP8_E4M3, k_bits=0,
-                                                    v_format=kvq.FMT_INT4_G32, v_bits=0)])[0] == 2
+                                                    v_format=kvq.FMT_INT4_G32, v_bits=0)])[0] == 0
     assert _ws(kvq, [_qjl_cache(kvq), _qjl_cache(kvq, k_qjl=(1 << 40) + 4096 * 31)])[0] == 1
     assert _ws(kvq, [_qjl_cache(kvq, page_size=32)])[0] == 2
     assert _ws(kvq, [_qjl_cache(kvq)], hq=2 * 8)[0] == 2  # 8 query heads per kv head
+
+
+def test_requantize_checks(kvq):
+    """Moving tokens out of an fp16 window: argument checks before any launch."""
+    L = kvq.lib()
+    win = _fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_bits=0, v_bits=0)
+    dst = _fake_cache(kvq)
+
+    def rq(src, d, n=3, ss=1 << 42, ds=1 << 43):
+        return L.kvq_requantize(ctypes.byref(src), ss, ctypes.byref(d), ds, n, None)
+
+    assert rq(win, dst, n=0) == 0  # nothing to move
+    assert rq(win, dst, n=-1) == 1
+    assert rq(dst, dst, n=0) == 2  # the source must be an fp16 tier
+    assert rq(win, _fake_cache(kvq, head_dim=256), n=0) == 1
+    assert rq(win, _fake_cache(kvq, num_kv_heads=4), n=0) == 1
+    assert rq(win, _fake_cache(kvq, k_signs=(1 << 40) + 4096 * 20), n=0) == 1  # another rotation
+    assert rq(win, _fake_cache(kvq, k_bounds=None), n=0) == 1
+    assert rq(win, dst, n=2, ss=None) == 1
+    assert rq(win, dst, n=2, ds=(1 << 43) + 2) == 1
+    assert rq(_fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_rows=(1 << 40) + 8), dst, n=0) == 1
