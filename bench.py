@@ -184,6 +184,11 @@ def step_bytes(cfg, wl, kvq):
     rk, ak = kvq.kvq_row_bytes(tier.k_format, tier.k_bits, d)
     rv, av = kvq.kvq_row_bytes(tier.v_format, tier.v_bits, d)
     quant = cfg.batch * cfg.num_kv_heads * (2 * 2 * d + rk + ak + rv + av) + 4 * cfg.batch
+    if tier.window > 0:  # the oldest window token moves into the tier before it
+        main = cfg.tiers[-2]
+        rk, ak = kvq.kvq_row_bytes(main.k_format, main.k_bits, d)
+        rv, av = kvq.kvq_row_bytes(main.v_format, main.v_bits, d)
+        quant += cfg.batch * cfg.num_kv_heads * (2 * 2 * d + rk + ak + rv + av) + 8 * cfg.batch
     return dec, quant
 
 
@@ -374,9 +379,16 @@ def run_ours(args):
     views = wl.views()
     last = len(cfg.tiers) - 1
     cache_last = wl.caches[last]
-    # newest token of every sequence: written over the last slot of the last tier
-    pos = wl.tier_len[last] - 1
+    # newest token of every sequence: written over the last slot of the last tier; with a
+    # recent-token window it replaces the window's oldest token (position 0), which first
+    # moves into the spare slot after the end of the tier before the window
+    window = cfg.tiers[-1].window > 0
+    pos = np.zeros(cfg.batch, np.int64) if window else wl.tier_len[last] - 1
     slots_new = np.array([wl.maps[last].slots(b, [int(pos[b])])[0] for b in range(cfg.batch)], dtype=np.int32)
+    if window:
+        main = last - 1
+        moved = np.array([wl.maps[main].slots(b, [int(wl.tier_len[main][b])])[0] for b in range(cfg.batch)],
+                         dtype=np.int32)
     k_new = np.concatenate([W.chunk_kv(cfg, b, 1, 1)[0] for b in range(cfg.batch)])
     v_new = np.concatenate([W.chunk_kv(cfg, b, 1, 1)[1] for b in range(cfg.batch)])
     q_host = W.queries(cfg)
@@ -384,6 +396,11 @@ def run_ours(args):
         q_host = (q_host.astype(np.float32) * args.query_scale).astype(np.float16)
     dev = torch.device("cuda")
     slots_d = torch.from_numpy(slots_new).to(dev)
+    moved_d = torch.from_numpy(moved).to(dev) if window else None
+
+    def move_oldest():
+        if window:
+            kvq.kvq_requantize(cache_last.struct, slots_d, wl.caches[main].struct, moved_d, stream)
     k_d, v_d = torch.from_numpy(k_new).to(dev), torch.from_numpy(v_new).to(dev)
     q_d = torch.from_numpy(q_host).to(dev)
     out_d = torch.empty((cfg.batch, cfg.num_q_heads, cfg.head_dim), dtype=torch.float32, device=dev)
@@ -395,6 +412,7 @@ def run_ours(args):
     opts = dict(score_gate=args.score_gate, spike_flags=flags_d)
 
     def step():
+        move_oldest()
         kvq.kvq_quantize_append(cache_last.struct, k_d, v_d, slots_d, stream)
         kvq.kvq_decode_attention(views, q_d, out_d, ws_d, 0, stream, **opts)
 
@@ -413,6 +431,7 @@ def run_ours(args):
     torch.cuda.nvtx.range_push("timed")  # lets a profiler select the timed launches
     t0.record(stream)
     for i in range(args.steps):
+        move_oldest()
         kvq.kvq_quantize_append(cache_last.struct, k_d, v_d, slots_d, stream)
         ev[i][0].record(stream)
         kvq.kvq_decode_attention(views, q_d, out_d, ws_d, 0, stream, **opts)

@@ -105,11 +105,12 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
   const kvq_cache* c0 = tiers[0].cache;
   const int ps = c0->page_size, hkv = c0->num_kv_heads, group = hq / hkv;
   if (split_tokens < 0 || split_tokens % ps) return KVQ_ERR_INVALID_ARGUMENT;
-  // fused kernels: items of about equal bytes, several per warp of a full GPU
-  size_t total_bytes = 0;
+  // fused kernels: items of about equal bytes, several per warp of a full GPU, sized from
+  // the bytes of the tiers their launch covers (a small recent-token window gets small items)
+  size_t family_bytes[3] = {0, 0, 0};
   for (int i = 0; i < n; ++i) {
     plan->kind[i] = tier_kind(tiers[i].cache, group, split_tokens, q16);
-    total_bytes += (size_t)batch * hkv * tiers[i].max_pages * ps * token_bytes(tiers[i].cache);
+    family_bytes[plan->kind[i]] += (size_t)batch * hkv * tiers[i].max_pages * ps * token_bytes(tiers[i].cache);
   }
   plan->total = 0;
   for (int i = 0; i < n; ++i) {
@@ -117,8 +118,9 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
     const int kind = plan->kind[i];
     int chunk = split_tokens;
     if (chunk == 0 && kind != TIER_GENERIC) {
-      const size_t item_bytes = kind == TIER_GQA ? std::max<size_t>(64 << 10, total_bytes / (kSms * 8 * 4))
-                                                 : std::max<size_t>(16 << 10, total_bytes / (kSms * 12 * 6));
+      const size_t fb = family_bytes[kind];
+      const size_t item_bytes = kind == TIER_GQA ? std::max<size_t>(16 << 10, fb / (kSms * 8 * 4))
+                                                 : std::max<size_t>(16 << 10, fb / (kSms * 12 * 6));
       const size_t tok = item_bytes / token_bytes(tiers[i].cache);
       const size_t cap = kind == TIER_GQA ? (size_t)gqa_max_chunk_tokens() : (size_t)1 << 20;
       chunk = (int)std::min<size_t>(cap, std::max<size_t>(ps, tok / ps * ps));
@@ -406,8 +408,8 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
   bool fam[3] = {false, false, false};
   for (int i = 0; i < num_tiers; ++i) fam[plan.kind[i]] = true;
   cudaError_t e = cudaMemsetAsync(counters, 0, 256, s);  // work counters and the error word
-  if (e == cudaSuccess && fam[TIER_GQA]) e = launch_decode_gqa(p, counters + kGqaCounter, s);
-  if (e == cudaSuccess && fam[TIER_CB]) e = launch_decode_cb(p, d, counters, s);
+  if (e == cudaSuccess && fam[TIER_GQA]) e = launch_decode_gqa(p, counters + kGqaCounter, s, fam[TIER_CB]);
+  if (e == cudaSuccess && fam[TIER_CB]) e = launch_decode_cb(p, d, counters, s, fam[TIER_GQA]);
   if (e == cudaSuccess && fam[TIER_GENERIC]) e = launch_decode(p, d, num_q_heads / hkv, s);
   if (e == cudaSuccess) e = launch_combine(p, d, s);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

@@ -11,7 +11,8 @@ bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
          (k_fmt == KVQ_FMT_CODEBOOK || (k_fmt == KVQ_FMT_CODEBOOK_QJL && head_dim == 128));
 }
 
-cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, cudaStream_t stream) {
+cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, cudaStream_t stream,
+                             bool after_split_k) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -51,14 +52,21 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.total_splits = dp.total_splits;
     p.total_items = dp.batch * dp.hkv * t.num_splits;
     if (p.total_items == 0) continue;
+    // run alongside the previous split-K grid, unless the projection (whose output this
+    // launch reads) is what precedes it
+    p.pdl = after_split_k ? 1 : 0;
+    p.trigger = 0;
+    for (int j = i + 1; j < dp.num_tiers; ++j) p.trigger |= dp.tier[j].kind == TIER_CB ? 1 : 0;
     if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL && !projected) {
       if ((e = cbk::launch_project_qjl(p, group, dp.batch, stream)) != cudaSuccess) return e;
       projected = true;
+      p.pdl = 0;
     }
     if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL) e = cbk::launch_cb_qjl(p, group, t.k_bits, t.v_bits, sms, stream);
     else if (head_dim == 128) e = cbk::launch_g<128, false>(p, group, t.k_bits, t.v_bits, sms, stream);
     else e = cbk::launch_g<256, false>(p, group, t.k_bits, t.v_bits, sms, stream);
     if (e != cudaSuccess) return e;
+    after_split_k = true;
   }
   return cudaSuccess;
 }

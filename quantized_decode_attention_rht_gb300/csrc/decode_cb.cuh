@@ -203,6 +203,8 @@ struct CbParams {
   int* err;      // error word: set when a wait for a bulk copy gives up
   int hq, hkv, total_splits, total_items, smem_bytes;
   int gate, track;  // score-gated value loading; record the lowest score
+  int pdl;          // launched as a programmatic dependent of the previous split-K launch
+  int trigger;      // another split-K launch follows: let it start on SMs this grid leaves
 };
 
 // Shared-memory plan common to both paths: table region (aligned to its size), the residual
@@ -897,7 +899,13 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   const int nfit = min(L::WARPS, (int)((a_t - base) / L::WSM));
   const uint32_t a_w = a_t + L::TABLE + L::SKT;  // warp areas that do not fit before the tables
   const uint32_t end = nfit == L::WARPS ? a_w : a_w + (L::WARPS - nfit) * L::WSM;
-  if (end > base + (uint32_t)p.smem_bytes) return;  // the launcher sizes smem for any base
+  // A later split-K launch may start on SMs this grid leaves; whatever depends on this
+  // grid's completion also sees the launch before it (the wait at the end).
+  if (p.trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (end > base + (uint32_t)p.smem_bytes) {  // the launcher sizes smem for any base
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t area = warp < nfit ? base + warp * L::WSM : a_w + (warp - nfit) * L::WSM;
   Ring rg;
@@ -949,6 +957,11 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
       }
     }
   }
+  // A programmatic dependent (p.pdl) ran alongside the previous split-K grid, whose partials
+  // it does not read; it completes only after that grid has, so whatever depends on this
+  // grid's completion (the combine) sees every earlier partial.  Without the attribute
+  // there is nothing to wait for.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <class P>
@@ -968,8 +981,18 @@ cudaError_t launch_path(const CbParams& p, int sms, cudaStream_t stream) {
     configured[dev] = true;
   }
   const int ctas = std::max(1, std::min(sms, (p.total_items + 2 * L::WARPS - 1) / (2 * L::WARPS)));
-  kern<<<ctas, L::WARPS * 32, L::SMEM, stream>>>(q);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(L::WARPS * 32);
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, q);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }

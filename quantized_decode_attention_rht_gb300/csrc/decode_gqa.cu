@@ -145,6 +145,7 @@ struct GqaParams {
   int* counter;
   int hq, hkv, total_splits, total_items;
   int group;        // query heads per kv head (1, 2 or 4); heads group.. of an item are idle
+  int trigger;      // a codebook split-K launch follows (as a programmatic dependent)
   int gate, spike;  // score-gated value loading; track tier 0's lowest scores
 };
 
@@ -586,6 +587,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* wsm = smem + warp * kWarpSmem;
+  // a codebook split-K grid that follows may start on SMs this grid leaves idle
+  if (p.trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int item = 0;
   if (lane == 0) item = atomicAdd(p.counter, 1);
   item = __shfl_sync(kFull, item, 0);
@@ -620,7 +623,7 @@ bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
 
 int gqa_max_chunk_tokens() { return kMaxPagesPerItem * PS; }
 
-cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t stream) {
+cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t stream, bool trigger) {
   constexpr int smem = kWarps * kWarpSmem;
   static bool configured[64] = {};
   int dev = 0;
@@ -655,6 +658,7 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
   }
   p.num_tiers = n;
   p.group = dp.hq / dp.hkv;
+  p.trigger = trigger ? 1 : 0;
   p.q = dp.q;
   p.k_signs = dp.k_signs;
   p.ws_acc = dp.ws_acc;

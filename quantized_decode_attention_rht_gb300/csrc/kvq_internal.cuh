@@ -93,14 +93,18 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
 // device scratch, zero at launch.
 bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
 int gqa_max_chunk_tokens();
-cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t stream);
+// trigger: a codebook split-K launch follows and may start on SMs this grid leaves idle.
+cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t stream, bool trigger);
 // Fused tensor-core decode over codebook tiers (codebook K and V), head_dim 128 or 256,
 // 1, 2 or 4 query heads per kv head; one launch per tier (after one projection launch when
 // a tier's keys carry a sketch).  `counters`: the 256-byte counter block, zero at launch
 // (ints [0, KVQ_MAX_TIERS) work counters, kCbErrorWord set when a wait for one of the
 // kernel's own bulk copies gives up).
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
-cudaError_t launch_decode_cb(const DecParams& p, int head_dim, int* counters, cudaStream_t stream);
+// after_split_k: a split-K launch of this call precedes; the codebook grids then run as its
+// programmatic dependents (overlapping its tail) and complete only after it.
+cudaError_t launch_decode_cb(const DecParams& p, int head_dim, int* counters, cudaStream_t stream,
+                             bool after_split_k);
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream);
 
 // ------------------------------------------------------------------------ device helpers

@@ -209,7 +209,7 @@ def pool_index(torch, wl, t, b, n):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["tiny", "llama7b", "llama7b_prod", "gqa32k", "ragged", "append"])
+@pytest.mark.parametrize("name", ["tiny", "llama7b", "llama7b_prod", "llama7b_window", "gqa32k", "ragged", "append"])
 def test_full_size_sampled_heads(name):
     """Every workload at its full size, built on the GPU by kvq_quantize_append and decoded with
     the split plan the benchmark uses.  For sampled (sequence, kv head) pairs:

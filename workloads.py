@@ -49,6 +49,7 @@ class Tier:
     v_bits: int = 0
     codebook: str = "lloyd_max"  # or "uniform"
     fraction: float = 1.0  # share of each (sequence, kv head)'s tokens held here
+    window: int = 0  # > 0 (last tier only): the newest min(window, L) tokens, stored fp16
 
 
 @dataclasses.dataclass(frozen=True)
@@ -88,6 +89,10 @@ CONFIGS: Dict[str, Config] = {
     # Llama-7B-shaped layer: B8, 32/32 heads, D128, ctx 8192, 1% outlier channels x50, 4-bit LM
     "llama7b": Config("llama7b", 8, 32, 32, 128, 8192, (LM4,), seed=1,
                       outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
+    # the same layer with a recent-token window: the newest 256 tokens of every sequence in
+    # fp16 (the hybrid threshold), the older ones 4-bit LM
+    "llama7b_window": Config("llama7b_window", 8, 32, 32, 128, 8192, (LM4, Tier(FP16, FP16, window=256)), seed=1,
+                             outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
     # the same layer with product-quantised keys: 3-bit LM codes + 128-bit residual sign
     # sketch (4 bits per coordinate), 4-bit LM values
     "llama7b_prod": Config("llama7b_prod", 8, 32, 32, 128, 8192, (Tier(CODEBOOK_QJL, CODEBOOK, 3, 4),), seed=1,
@@ -122,14 +127,26 @@ def seq_lens(cfg: Config) -> np.ndarray:
     return np.full(cfg.batch, cfg.seq_len, dtype=np.int64)
 
 
+def window_len(cfg: Config, total: int) -> int:
+    """Tokens in the recent-token window (a last tier with `window` > 0), else 0."""
+    w = cfg.tiers[-1].window
+    return min(w, total) if w > 0 else 0
+
+
 def tier_lens(cfg: Config, total: int) -> List[int]:
-    """Tokens per tier for one (sequence, kv head) of `total` tokens.  The first tier
-    gets round(fraction*total); the last tier takes the rest."""
-    out, left = [], total
-    for i, t in enumerate(cfg.tiers):
-        n = left if i == len(cfg.tiers) - 1 else min(left, int(round(t.fraction * total)))
+    """Tokens per tier for one (sequence, kv head) of `total` tokens.  A window tier (last)
+    takes the newest min(window, total); of the older ones the first tier gets
+    round(fraction * older) and the last of the other tiers the rest."""
+    w = window_len(cfg, total)
+    base = cfg.tiers[:-1] if cfg.tiers[-1].window > 0 else cfg.tiers
+    rest = total - w
+    out, left = [], rest
+    for i, t in enumerate(base):
+        n = left if i == len(base) - 1 else min(left, int(round(t.fraction * rest)))
         out.append(n)
         left -= n
+    if cfg.tiers[-1].window > 0:
+        out.append(w)
     return out
 
 
@@ -201,15 +218,19 @@ def tier_members(cfg: Config, b: int, h: int, total: int) -> List[np.ndarray]:
     tier all tokens are in it; otherwise the first tier takes the tokens with the highest
     seeded U(0,1) score (ties cannot occur with continuous draws) and the rest follow."""
     lens = tier_lens(cfg, total)
-    if len(cfg.tiers) == 1:
-        return [np.arange(total)]
-    score = rng(cfg, S_TIER, b, h).random(total)
+    w = window_len(cfg, total)
+    rest = total - w
+    tail = [np.arange(rest, total)] if cfg.tiers[-1].window > 0 else []  # the window: newest tokens
+    base = lens[:-1] if tail else lens
+    if len(base) == 1:
+        return [np.arange(rest)] + tail
+    score = rng(cfg, S_TIER, b, h).random(rest)
     order = np.argsort(-score, kind="stable")
     out, at = [], 0
-    for n in lens:
+    for n in base:
         out.append(np.sort(order[at: at + n]))
         at += n
-    return out
+    return out + tail
 
 
 # ----------------------------------------------------------------------------- paging
@@ -321,9 +342,14 @@ class GpuWorkload:
         cap = np.array([min(capacity(cfg), int(n) + cfg.prefill_chunk + cfg.decode_steps)
                         for n in self.lens])
         ntier = len(cfg.tiers)
-        # capacity per tier: every appended token goes to the last tier
+        # capacity per tier: every appended token goes to the last tier; with a window, the
+        # window keeps its size and the tier before it gets one spare slot per sequence (the
+        # token a decode step moves out of the window)
         cap_t = [np.array([tier_lens(cfg, int(n))[t] for n in self.lens]) for t in range(ntier)]
-        cap_t[-1] = cap_t[-1] + (cap - self.lens)
+        if cfg.tiers[-1].window > 0:
+            cap_t[-2] = cap_t[-2] + 1
+        else:
+            cap_t[-1] = cap_t[-1] + (cap - self.lens)
         self.maps = [page_map(cfg, cap_t[t], tier=t) for t in range(ntier)]
         self.tier_len = [np.array([tier_lens(cfg, int(n))[t] for n in self.lens]) for t in range(ntier)]
         ks, vs = signs(cfg, 0), signs(cfg, 1)
