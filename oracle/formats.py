@@ -139,9 +139,29 @@ def unpack_bits(rows: np.ndarray, bits: int, n: int) -> np.ndarray:
 QJL_DIM = 128  # sign-sketch dimensions m of the residual correction
 
 
+# ----------------------------------------------------------------------------- outlier stream
+
+OUTLIER_CHANNELS = 8  # K of the outlier two-stream cache (VeloxQuant-MLX page: "at K=8")
+
+
+def outlier_int8_encode(x: np.ndarray):
+    """int8 with a per-token scale (VeloxQuant-MLX page, "Outlier Two-Stream Cache"): for
+    the K outlier values x [..., K] of a token, s = fp16(max|x| / 127) (divided in float32,
+    as a kernel does), q = clamp(rint(x / s), -127, 127) with the quotient rounded to
+    float32 first; s = 0 gives q = 0.  Returns (q int8 [..., K], s float16 [...])."""
+    x = np.asarray(x, dtype=np.float64)
+    amax = np.max(np.abs(x), axis=-1)
+    s16 = to_f16(to_f32(amax / 127.0))
+    sv = s16.astype(np.float64)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = to_f32(np.where(sv > 0, x / np.where(sv > 0, sv, 1.0), 0.0)).astype(np.float64)
+    q = np.where(sv > 0, np.clip(np.rint(t), -127, 127), 0.0)
+    return q.astype(np.int8), s16
+
+
 def row_bytes(fmt: str, bits: int, d: int) -> int:
     """Bytes of one packed row (one token's vector) in the given format."""
-    if fmt == "codebook":
+    if fmt in ("codebook", "codebook_outlier"):  # outlier format: the inlier codes
         return (d * bits + 7) // 8
     if fmt == "codebook_qjl":  # codes, then the m sign bits of the residual sketch
         return (d * bits + 7) // 8 + QJL_DIM // 8
@@ -161,6 +181,8 @@ def aux_bytes(fmt: str, d: int) -> int:
         return 2
     if fmt == "codebook_qjl":  # fp16 norm, fp16 residual norm
         return 4
+    if fmt == "codebook_outlier":  # fp16 norm, fp16 outlier scale, K int8 outlier values
+        return 4 + OUTLIER_CHANNELS
     if fmt == "int4_g32":
         return 2 * (d // GROUP)
     return 0
