@@ -48,6 +48,7 @@ extern "C" {
 #define KVQ_MAX_SPLITS 1024  /* split-K chunks per sequence, summed over the tiers */
 #define KVQ_INT4_GROUP 32 /* coordinates sharing one fp16 scale in KVQ_FMT_INT4_G32 */
 #define KVQ_QJL_DIM 128   /* rows m of the residual sketch's projection (KVQ_FMT_CODEBOOK_QJL) */
+#define KVQ_OUTLIER_CHANNELS 8  /* outlier channels per kv head (KVQ_FMT_CODEBOOK_OUTLIER) */
 
 typedef enum kvq_status {
   KVQ_OK = 0,
@@ -79,13 +80,24 @@ typedef enum kvq_status {
  *                      Decode adds ||r~|| sqrt(pi/2) / KVQ_QJL_DIM * sum_j (2 z_j - 1)
  *                      <S_j, q~> to the key's inner product with the rotated query q~
  *                      (the unbiased estimator of <q~, r~>).
+ *   KVQ_FMT_CODEBOOK_OUTLIER (keys only; VeloxQuant-MLX page, "Outlier Two-Stream
+ *                      Cache"): the kv head's KVQ_OUTLIER_CHANNELS outlier channels c_j
+ *                      (k_outliers, indices of the UNROTATED vector, e.g. from
+ *                      kvq_outlier_calibrate) are stored as int8 with a per-token scale,
+ *                      s = fp16(max_j |x_cj| / 127), q_j = clamp(rint(x_cj / s), -127,
+ *                      127); the rest of the vector, those channels set to zero, is
+ *                      rotated and stored as a KVQ_FMT_CODEBOOK row.  Side data: 4 +
+ *                      KVQ_OUTLIER_CHANNELS bytes per row = fp16 norm, fp16 s, then the
+ *                      int8 q_j in channel-list order.  Decode adds sum_j q[c_j] q_j s
+ *                      (unrotated query) to the inlier inner product.
  * Rounding decisions are taken on float32 values. */
 typedef enum kvq_format {
   KVQ_FMT_CODEBOOK = 0,
   KVQ_FMT_FP16 = 1,
   KVQ_FMT_FP8_E4M3 = 2,
   KVQ_FMT_INT4_G32 = 3,
-  KVQ_FMT_CODEBOOK_QJL = 4
+  KVQ_FMT_CODEBOOK_QJL = 4,
+  KVQ_FMT_CODEBOOK_OUTLIER = 5
 } kvq_format;
 
 /* One tier of a paged cache.  A token of a sequence at position t lives in physical
@@ -96,6 +108,8 @@ typedef enum kvq_format {
  *          fp16  [num_pages][num_kv_heads][page_size][2]        (codebook + sketch:
  *                                                                norm, residual norm)
  *          fp16  [num_pages][num_kv_heads][page_size][D/32]     (INT4: group scales)
+ *          uint8 [num_pages][num_kv_heads][page_size][12]       (codebook + outlier
+ *                                                                stream, 16-byte aligned)
  *          unused (may be NULL) for fp16 / fp8.
  * row_bytes / aux bytes per row come from kvq_row_bytes().  Codebook tables are fp32:
  * centroids [2^bits] increasing, bounds [2^bits - 1] with centroids[i] < bounds[i] <
@@ -124,6 +138,9 @@ typedef struct kvq_cache {
   const float* k_qjl;       /* KVQ_FMT_CODEBOOK_QJL keys only: the projection S, fp32
                                [KVQ_QJL_DIM][head_dim] (iid N(0,1) entries), 16-byte
                                aligned; the same for every tier attended together */
+  const int32_t* k_outliers; /* KVQ_FMT_CODEBOOK_OUTLIER keys only: int32
+                               [num_kv_heads][KVQ_OUTLIER_CHANNELS] distinct channels in
+                               [0, head_dim), 16-byte aligned */
 } kvq_cache;
 
 /* One tier as seen by a decode call: the cache plus each sequence's pages and length.
@@ -192,10 +209,22 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
  * rotation (so a codebook row of a moved token can differ from appending the original x
  * directly where the fp16 rounding of x~ crosses a decision boundary).  A token whose src
  * or dst slot is negative or out of range is skipped.  src is left unchanged.  A src
- * that is not fp16 returns KVQ_ERR_UNSUPPORTED. */
+ * that is not fp16, or a dst whose keys are KVQ_FMT_CODEBOOK_OUTLIER (its channel split
+ * needs the unrotated vector), returns KVQ_ERR_UNSUPPORTED. */
 KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots,
                                   const kvq_cache* dst, const int32_t* dst_slots,
                                   int32_t num_tokens, void* stream);
+
+/* Calibration of the outlier two-stream cache (VeloxQuant-MLX page, "Outlier Two-Stream
+ * Cache", steps 1 and 2): over the first num_tokens tokens of a sequence, the population
+ * variance of every channel of every kv head's keys (computed in fp64), and per head the
+ * KVQ_OUTLIER_CHANNELS channels of largest variance, largest first, ties to the lower
+ * channel.
+ *   k          : fp16 [num_tokens][num_kv_heads][head_dim] keys (unrotated), 4-byte aligned
+ *   out_idx    : int32 [num_kv_heads][KVQ_OUTLIER_CHANNELS], written
+ * head_dim 128 or 256; num_tokens >= 1. */
+KVQ_API kvq_status kvq_outlier_calibrate(const uint16_t* k, int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t* out_idx, void* stream);
 
 /* Workspace bytes kvq_decode_attention needs for these tiers and shapes (host output).
  * split_tokens: tokens per split-K chunk (a multiple of page_size), or 0 to let the

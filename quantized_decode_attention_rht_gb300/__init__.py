@@ -20,10 +20,11 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
-FMT_CODEBOOK, FMT_FP16, FMT_FP8_E4M3, FMT_INT4_G32, FMT_CODEBOOK_QJL = 0, 1, 2, 3, 4
+FMT_CODEBOOK, FMT_FP16, FMT_FP8_E4M3, FMT_INT4_G32, FMT_CODEBOOK_QJL, FMT_CODEBOOK_OUTLIER = 0, 1, 2, 3, 4, 5
 FORMATS = {"codebook": FMT_CODEBOOK, "fp16": FMT_FP16, "fp8_e4m3": FMT_FP8_E4M3, "int4_g32": FMT_INT4_G32,
-           "codebook_qjl": FMT_CODEBOOK_QJL}
+           "codebook_qjl": FMT_CODEBOOK_QJL, "codebook_outlier": FMT_CODEBOOK_OUTLIER}
 QJL_DIM = 128
+OUTLIER_CHANNELS = 8
 MAX_TIERS = 4
 INT4_GROUP = 32
 
@@ -50,7 +51,7 @@ class KvqCache(ctypes.Structure):
         ("k_centroids", ctypes.c_void_p), ("k_bounds", ctypes.c_void_p),
         ("v_centroids", ctypes.c_void_p), ("v_bounds", ctypes.c_void_p),
         ("k_signs", ctypes.c_void_p), ("v_signs", ctypes.c_void_p),
-        ("k_qjl", ctypes.c_void_p),
+        ("k_qjl", ctypes.c_void_p), ("k_outliers", ctypes.c_void_p),
     ]
 
 
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "kvq_codebook_tables": [i32, dp, fp, fp],
             "kvq_quantize_append": [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp],
             "kvq_requantize": [ctypes.POINTER(KvqCache), vp, ctypes.POINTER(KvqCache), vp, i32, vp],
+            "kvq_outlier_calibrate": [vp, i32, i32, i32, vp, vp],
             "kvq_decode_workspace_size": [ctypes.POINTER(KvqTierView), i32, i32, i32, i32, szp],
             "kvq_decode_attention": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz, vp],
             "kvq_decode_attention_ex": [ctypes.POINTER(KvqTierView), i32, vp, i32, i32, i32, vp, vp, sz,
@@ -190,6 +192,14 @@ def kvq_quantize_append(cache: KvqCache, k, v, slot_mapping, stream=None) -> Non
                                      _stream(stream)), "kvq_quantize_append")
 
 
+def kvq_outlier_calibrate(k, out_idx, stream=None) -> None:
+    """k: fp16 CUDA tensor [N, Hkv, D] (the calibration tokens' keys); out_idx: int32 CUDA
+    tensor [Hkv, OUTLIER_CHANNELS], written with each head's largest-variance channels."""
+    _dense(k, out_idx)
+    n, hkv, d = k.shape
+    _check(lib().kvq_outlier_calibrate(_ptr(k), n, hkv, d, _ptr(out_idx), _stream(stream)), "kvq_outlier_calibrate")
+
+
 def kvq_requantize(src: KvqCache, src_slots, dst: KvqCache, dst_slots, stream=None) -> None:
     """Move tokens from an fp16 tier (a recent-token window) into another tier, re-encoding
     their rows; src_slots / dst_slots: int32 CUDA tensors [T]."""
@@ -259,10 +269,13 @@ class PagedCache:
     "codebook_qjl" (codes + residual sign sketch); codebook tiers take `k_bits` / `v_bits` and
     a codebook kind ("lloyd_max" or "uniform") computed by the library.
     k_signs / v_signs: int8 [Hkv, D] tensors or arrays of +1/-1 (shared by every tier).
-    k_qjl: float32 [QJL_DIM, D] projection (tensor or array) for "codebook_qjl" keys."""
+    k_qjl: float32 [QJL_DIM, D] projection (tensor or array) for "codebook_qjl" keys.
+    k_outliers: int32 [Hkv, OUTLIER_CHANNELS] channels (tensor or array) for
+    "codebook_outlier" keys (e.g. from kvq_outlier_calibrate)."""
 
     def __init__(self, head_dim, num_kv_heads, num_pages, k_format, v_format, k_bits=0, v_bits=0,
-                 k_signs=None, v_signs=None, page_size=16, codebook="lloyd_max", device="cuda", k_qjl=None):
+                 k_signs=None, v_signs=None, page_size=16, codebook="lloyd_max", device="cuda", k_qjl=None,
+                 k_outliers=None):
         import torch
         self.head_dim, self.num_kv_heads, self.num_pages, self.page_size = head_dim, num_kv_heads, num_pages, page_size
         self.k_format, self.v_format = FORMATS.get(k_format, k_format), FORMATS.get(v_format, v_format)
@@ -273,10 +286,12 @@ class PagedCache:
             row, aux = kvq_row_bytes(fmt, bits, head_dim)
             rows = torch.zeros((num_pages, num_kv_heads, page_size, row), dtype=torch.uint8, device=dev)
             a = None
-            if aux:
+            if aux and fmt == FMT_CODEBOOK_OUTLIER:  # byte records (norm, scale, int8 values)
+                a = torch.zeros((num_pages, num_kv_heads, page_size, aux), dtype=torch.uint8, device=dev)
+            elif aux:
                 a = torch.zeros((num_pages, num_kv_heads, page_size, aux // 2), dtype=torch.float16, device=dev)
             cent = bnd = None
-            if fmt in (FMT_CODEBOOK, FMT_CODEBOOK_QJL):
+            if fmt in (FMT_CODEBOOK, FMT_CODEBOOK_QJL, FMT_CODEBOOK_OUTLIER):
                 c = (kvq_lloyd_max_codebook if codebook == "lloyd_max" else kvq_uniform_codebook)(bits)[0]
                 c32, b32 = kvq_codebook_tables(bits, c)
                 cent = torch.from_numpy(c32).to(dev)
@@ -300,6 +315,11 @@ class PagedCache:
         s.v_centroids, s.v_bounds = _ptr(self.v_centroids), _ptr(self.v_bounds)
         s.k_signs, s.v_signs = _ptr(self.k_signs), _ptr(self.v_signs)
         s.k_qjl = _ptr(self.k_qjl)
+        self.k_outliers = None
+        if k_outliers is not None:
+            self.k_outliers = (k_outliers if hasattr(k_outliers, "data_ptr")
+                               else torch.as_tensor(np.asarray(k_outliers, dtype=np.int32)).to(dev)).contiguous()
+        s.k_outliers = _ptr(self.k_outliers)
         self.struct = s
 
     def append(self, k, v, slot_mapping, stream=None) -> None:

@@ -28,6 +28,11 @@ kvq_status side_bytes(int fmt, int bits, int d, size_t* row, size_t* aux) {
       *row = (size_t)d * bits / 8;
       *aux = 2;
       return KVQ_OK;
+    case KVQ_FMT_CODEBOOK_OUTLIER:  // inlier codes; norm, outlier scale, int8 outlier values
+      if (bits < 2 || bits > 4) return KVQ_ERR_UNSUPPORTED;
+      *row = (size_t)d * bits / 8;
+      *aux = 4 + KVQ_OUTLIER_CHANNELS;
+      return KVQ_OK;
     case KVQ_FMT_CODEBOOK_QJL:  // codes, then the sketch's sign bits; norm + residual norm
       if (bits < 2 || bits > 4) return KVQ_ERR_UNSUPPORTED;
       *row = (size_t)d * bits / 8 + KVQ_QJL_DIM / 8;
@@ -40,7 +45,9 @@ kvq_status side_bytes(int fmt, int bits, int d, size_t* row, size_t* aux) {
   }
 }
 
-bool is_codebook(int fmt) { return fmt == KVQ_FMT_CODEBOOK || fmt == KVQ_FMT_CODEBOOK_QJL; }
+bool is_codebook(int fmt) {
+  return fmt == KVQ_FMT_CODEBOOK || fmt == KVQ_FMT_CODEBOOK_QJL || fmt == KVQ_FMT_CODEBOOK_OUTLIER;
+}
 
 // One side of a cache; is_key: the side holds keys (only keys may carry a residual sketch).
 kvq_status check_side(const kvq_cache* c, int fmt, int bits, const void* rows, const void* aux,
@@ -54,6 +61,9 @@ kvq_status check_side(const kvq_cache* c, int fmt, int bits, const void* rows, c
   if (is_codebook(fmt) && (!cent || (need_bounds && !bounds))) return KVQ_ERR_INVALID_ARGUMENT;
   if (fmt == KVQ_FMT_CODEBOOK_QJL &&
       (!is_key || !c->k_qjl || !aligned(c->k_qjl, 16) || !aligned(aux, 16)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (fmt == KVQ_FMT_CODEBOOK_OUTLIER &&
+      (!is_key || !c->k_outliers || !aligned(c->k_outliers, 16) || !aligned(aux, 16)))
     return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;
 }
@@ -171,14 +181,18 @@ kvq_status check_tiers(const kvq_tier_view* tiers, int n, int batch, int hq) {
       for (int j = 0; j < n; ++j)
         if (tiers[j].cache->k_format == KVQ_FMT_CODEBOOK_QJL && tiers[j].cache->k_qjl != c->k_qjl)
           return KVQ_ERR_INVALID_ARGUMENT;  // one projection for every tier attended together
+    } else if (c->k_format == KVQ_FMT_CODEBOOK_OUTLIER) {
+      // the codebook kernel family; checked below
     } else if (!decode_supports(c->k_format, c->k_bits, c->v_format, c->v_bits)) {
       return KVQ_ERR_UNSUPPORTED;
     }
   }
-  // keys with a residual sketch run on the fused codebook kernel only
+  // keys with a residual sketch or an outlier stream run on the fused codebook kernel only
   for (int i = 0; i < n; ++i) {
     const kvq_cache* c = tiers[i].cache;
-    if (c->k_format == KVQ_FMT_CODEBOOK_QJL && tier_kind(c, g, 0, false) != TIER_CB) return KVQ_ERR_UNSUPPORTED;
+    if ((c->k_format == KVQ_FMT_CODEBOOK_QJL || c->k_format == KVQ_FMT_CODEBOOK_OUTLIER) &&
+        tier_kind(c, g, 0, false) != TIER_CB)
+      return KVQ_ERR_UNSUPPORTED;
   }
   return KVQ_OK;
 }
@@ -237,6 +251,7 @@ void fill_sides(const kvq_cache* c, QuantParams* p) {
     p->side[i].bounds = bnd[i];
     p->side[i].centroids = cnt[i];
     p->side[i].qjl = i == 0 ? c->k_qjl : nullptr;
+    p->side[i].outl = i == 0 ? c->k_outliers : nullptr;
     p->side[i].signs = sg[i];
     p->side[i].fmt = fmts[i];
     p->side[i].bits = bits[i];
@@ -245,12 +260,23 @@ void fill_sides(const kvq_cache* c, QuantParams* p) {
 }
 }  // namespace
 
+KVQ_API kvq_status kvq_outlier_calibrate(const uint16_t* k, int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t* out_idx, void* stream) {
+  if (!k || !out_idx || !aligned(k, 4) || !aligned(out_idx, 4) || num_tokens < 1 || num_kv_heads < 1)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  cudaError_t e = launch_outlier_calibrate(k, num_tokens, num_kv_heads, head_dim, out_idx,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots, const kvq_cache* dst,
                                   const int32_t* dst_slots, int32_t num_tokens, void* stream) {
   kvq_status st = check_cache(src);
   if (st != KVQ_OK || (st = check_cache(dst)) != KVQ_OK) return st;
   if (num_tokens < 0) return KVQ_ERR_INVALID_ARGUMENT;
   if (src->k_format != KVQ_FMT_FP16 || src->v_format != KVQ_FMT_FP16) return KVQ_ERR_UNSUPPORTED;
+  if (dst->k_format == KVQ_FMT_CODEBOOK_OUTLIER) return KVQ_ERR_UNSUPPORTED;
   if (src->head_dim != dst->head_dim || src->num_kv_heads != dst->num_kv_heads ||
       src->page_size != dst->page_size || src->k_signs != dst->k_signs || src->v_signs != dst->v_signs)
     return KVQ_ERR_INVALID_ARGUMENT;
@@ -367,6 +393,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
     t.v_aux = static_cast<const __half*>(c->v_aux);
     t.k_cent = c->k_centroids;
     t.k_qjl = c->k_qjl;
+    t.k_outl = c->k_outliers;
     t.v_cent = c->v_centroids;
     t.block_table = tiers[i].block_table;
     t.seq_lens = tiers[i].seq_lens;

@@ -8,7 +8,8 @@ namespace kvq {
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
   return (head_dim == 128 || head_dim == 256) && (group == 1 || group == 2 || group == 4) &&
          v_fmt == KVQ_FMT_CODEBOOK &&
-         (k_fmt == KVQ_FMT_CODEBOOK || (k_fmt == KVQ_FMT_CODEBOOK_QJL && head_dim == 128));
+         (k_fmt == KVQ_FMT_CODEBOOK || k_fmt == KVQ_FMT_CODEBOOK_OUTLIER ||
+          (k_fmt == KVQ_FMT_CODEBOOK_QJL && head_dim == 128));
 }
 
 cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, cudaStream_t stream,
@@ -28,6 +29,7 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.t.v_rows = t.v_rows;
     p.t.k_norm = t.k_aux;
     p.t.qjl = t.k_qjl;
+    p.t.outl = t.k_outl;
     p.t.v_norm = t.v_aux;
     p.t.block_table = t.block_table;
     p.t.seq_lens = t.seq_lens;
@@ -63,8 +65,10 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
       p.pdl = 0;
     }
     if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL) e = cbk::launch_cb_qjl(p, group, t.k_bits, t.v_bits, sms, stream);
-    else if (head_dim == 128) e = cbk::launch_g<128, false>(p, group, t.k_bits, t.v_bits, sms, stream);
-    else e = cbk::launch_g<256, false>(p, group, t.k_bits, t.v_bits, sms, stream);
+    else if (t.k_fmt == KVQ_FMT_CODEBOOK_OUTLIER)
+      e = cbk::launch_cb_outlier(p, head_dim, group, t.k_bits, t.v_bits, sms, stream);
+    else if (head_dim == 128) e = cbk::launch_g<128, cbk::kModePlain>(p, group, t.k_bits, t.v_bits, sms, stream);
+    else e = cbk::launch_g<256, cbk::kModePlain>(p, group, t.k_bits, t.v_bits, sms, stream);
     if (e != cudaSuccess) return e;
     after_split_k = true;
   }

@@ -184,6 +184,7 @@ struct CbTier {
   const __half* k_norm;  // keys with a residual sketch: (norm, residual norm) pairs
   const __half* v_norm;
   const float* qjl;      // keys with a residual sketch: projection [KVQ_QJL_DIM][D]
+  const int32_t* outl;   // keys with an outlier stream: channels [Hkv][KVQ_OUTLIER_CHANNELS]
   const int32_t* block_table;
   const int32_t* seq_lens;
   int max_pages, chunk, nchunks, split_begin;
@@ -210,13 +211,17 @@ struct CbParams {
 // Shared-memory plan common to both paths: table region (aligned to its size), the residual
 // sketch's +-1 pair table after it (keys with a sketch), then per warp a ring of STAGES page
 // slots, a buffer for the rotated queries and the slot barriers.
-template <int D, int G, int KB, int VB, int WARPS_, bool QJL_>
+// Key formats of the codebook kernel: plain codes, codes + residual sign sketch, codes +
+// outlier stream.
+constexpr int kModePlain = 0, kModeSketch = 1, kModeOutlier = 2;
+
+template <int D, int G, int KB, int VB, int WARPS_, int MODE_>
 struct Layout {
-  static constexpr bool QJL = QJL_;
+  static constexpr bool QJL = MODE_ == kModeSketch, OUT = MODE_ == kModeOutlier;
   static constexpr int KCODE = D * KB / 8;                            // code bytes of a key row
   static constexpr int KROW = KCODE + (QJL ? KVQ_QJL_DIM / 8 : 0), VROW = D * VB / 8;
   static constexpr int KBLK = PS * KROW, VBLK = PS * VROW;
-  static constexpr int KNORM = PS * (QJL ? 4 : 2);  // key side data of a page block
+  static constexpr int KNORM = PS * (QJL ? 4 : (OUT ? 4 + KVQ_OUTLIER_CHANNELS : 2));  // key side data of a page block
   static constexpr int STAGE = KBLK + VBLK + KNORM + 32;  // + 16 fp16 value norms
   static constexpr int STAGES = 3;
   static constexpr int WARPS = WARPS_;
@@ -420,6 +425,16 @@ struct Feeder {
 // 4-entry table of (+-1, +-1) like any other code pair.
 constexpr float kSketch = 1.2533141373155003f / KVQ_QJL_DIM / kQScale;
 
+// Outlier stream (VeloxQuant-MLX page, "Outlier Two-Stream Cache"): the score gains
+// sum_j q[c_j] q_j s, in base-2 score units times log2(e) / sqrt(D).
+template <int D>
+struct OutlierScale {
+  static constexpr float v = D == 128 ? 0.12751743074960564f : 0.09016844005556021f;  // log2(e) / sqrt(D)
+};
+
+// Sign-extended int8 k of a 32-bit word, as float.
+__device__ __forceinline__ float i8f(uint32_t w, int k) { return (float)(int)(int8_t)(w >> (8 * k)); }
+
 // p' = S q' for every query head, once per call (every split of a head reads it): one block
 // of 4 warps per (sequence, kv head); lane l of warp w computes row 32w + l for the G heads.
 template <int D, int G>
@@ -463,9 +478,10 @@ __device__ void build_sketch_table(uint32_t base) {
 }
 
 // ================================================================ G = 1: FMA path
-template <int D, int KB, int VB, bool QJL>
+template <int D, int KB, int VB, int MODE>
 struct Path1 {
-  using L = Layout<D, 1, KB, VB, D == 128 ? (QJL ? 12 : 16) : 8, QJL>;
+  static constexpr bool QJL = MODE == kModeSketch, OUT = MODE == kModeOutlier;
+  using L = Layout<D, 1, KB, VB, D == 128 ? (QJL ? 12 : 16) : 8, MODE>;
   static constexpr int kD = D, kG = 1;
   static constexpr int SNP = KVQ_QJL_DIM / 8;  // sketch sign pairs per lane and token (a quarter of m)
   static constexpr int DL = D / 4;  // coordinates per lane and token
@@ -521,6 +537,13 @@ struct Path1 {
         p2[j + 1] = pk2(v.z, v.w);
       }
     }
+    float qo0 = 0.f, qo1 = 0.f;  // outlier stream: q[c_2c], q[c_2c+1] in score units
+    if constexpr (OUT) {
+      const int2 ch = __ldg(reinterpret_cast<const int2*>(T.outl + hk * KVQ_OUTLIER_CHANNELS) + c);
+      const __half* qrow = p.q + ((size_t)b * p.hq + hk) * D;
+      qo0 = __half2float(qrow[ch.x & (D - 1)]) * OutlierScale<D>::v;  // the mask keeps a bad list in bounds
+      qo1 = __half2float(qrow[ch.y & (D - 1)]) * OutlierScale<D>::v;
+    }
 #pragma unroll
     for (int j = 0; j < NP; ++j) acc[j] = 0ull;
     float m = -INFINITY, l = 0.f, mn = INFINITY;
@@ -534,7 +557,7 @@ struct Path1 {
       lds_run<KBYTES>(st + (t + 8) * L::KROW + c * KBYTES, k[1]);
       lds_run<VBYTES>(st + L::KBLK + t * L::VROW + c * VBYTES, v[0]);
       lds_run<VBYTES>(st + L::KBLK + (t + 8) * L::VROW + c * VBYTES, v[1]);
-      uint32_t sw[2][1] = {{0u}, {0u}}, rn0 = 0, rn1 = 0, nk0, nk1;
+      uint32_t sw[2][1] = {{0u}, {0u}}, rn0 = 0, rn1 = 0, nk0, nk1, op0 = 0, op1 = 0;
       if constexpr (QJL) {  // sign bits [32c, 32c + 32) of both tokens; (norm, residual norm)
         lds_run<4>(st + t * L::KROW + L::KCODE + 4 * c, sw[0]);
         lds_run<4>(st + (t + 8) * L::KROW + L::KCODE + 4 * c, sw[1]);
@@ -543,6 +566,14 @@ struct Path1 {
         rn0 = lds_u16(kn + 2);
         nk1 = lds_u16(kn + 32);
         rn1 = lds_u16(kn + 34);
+      } else if constexpr (OUT) {  // (norm, scale) and the int8 pair 2c, 2c+1 of both tokens
+        const uint32_t kn = st + L::KBLK + L::VBLK + 12 * t;
+        nk0 = lds_u16(kn);
+        rn0 = lds_u16(kn + 2);
+        op0 = lds_u16(kn + 4 + 2 * c);
+        nk1 = lds_u16(kn + 96);
+        rn1 = lds_u16(kn + 98);
+        op1 = lds_u16(kn + 100 + 2 * c);
       } else {
         const uint32_t kn = st + L::KBLK + L::VBLK + 2 * t;
         nk0 = lds_u16(kn);
@@ -582,6 +613,10 @@ struct Path1 {
         upk2(z1, zc, zd);
         x0 = fmaf(za + zb, __half2float(__ushort_as_half((uint16_t)rn0)) * kSketch, x0);
         x1 = fmaf(zc + zd, __half2float(__ushort_as_half((uint16_t)rn1)) * kSketch, x1);
+      }
+      if constexpr (OUT) {  // this lane's two of the eight outlier terms, times the token's scale
+        x0 = fmaf(fmaf(qo1, i8f(op0, 1), qo0 * i8f(op0, 0)), __half2float(__ushort_as_half((uint16_t)rn0)), x0);
+        x1 = fmaf(fmaf(qo1, i8f(op1, 1), qo0 * i8f(op1, 0)), __half2float(__ushort_as_half((uint16_t)rn1)), x1);
       }
       x0 += __shfl_xor_sync(kFull, x0, 1);
       x1 += __shfl_xor_sync(kFull, x1, 1);
@@ -653,9 +688,10 @@ struct Path1 {
 };
 
 // ================================================================ G = 2, 4: tensor-core path
-template <int D, int G, int KB, int VB, bool QJL>
+template <int D, int G, int KB, int VB, int MODE>
 struct PathM {
-  using L = Layout<D, G, KB, VB, D == 128 ? (QJL ? 10 : 12) : 8, QJL>;
+  static constexpr bool QJL = MODE == kModeSketch, OUT = MODE == kModeOutlier;
+  using L = Layout<D, G, KB, VB, D == 128 ? (QJL ? 10 : 12) : 8, MODE>;
   static constexpr int kD = D, kG = G;
   static constexpr int SKS = KVQ_QJL_DIM / 16;  // sketch mma k-steps
   static constexpr int KS = D / 16;            // key mma k-steps; also value m-tiles
@@ -729,6 +765,14 @@ struct PathM {
         for (int ks = 0; ks < SKS; ++ks) pf[ks][0] = pf[ks][1] = 0u;
       }
     }
+    float qo[OUT ? KVQ_OUTLIER_CHANNELS : 1];  // outlier stream: q[c_j] of head c, score units
+    if constexpr (OUT) {
+      const int32_t* ch = T.outl + hk * KVQ_OUTLIER_CHANNELS;
+      const __half* qrow = p.q + ((size_t)b * p.hq + hk * G + (c < G ? c : 0)) * D;
+#pragma unroll
+      for (int j = 0; j < KVQ_OUTLIER_CHANNELS; ++j)
+        qo[j] = c < G ? __half2float(qrow[__ldg(ch + j) & (D - 1)]) * OutlierScale<D>::v : 0.f;
+    }
     float acc[KS][4];
 #pragma unroll
     for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -764,6 +808,7 @@ struct PathM {
         }
       }
       uint32_t sw[2][1] = {{0u}, {0u}}, rn0 = 0, rn1 = 0, nk0, nk1;
+      uint32_t ow[2][2] = {{0u, 0u}, {0u, 0u}};
       if constexpr (QJL) {  // sign bits [32c, 32c + 32) of rows g, g+8; (norm, residual norm)
         lds_run<4>(st + g * L::KROW + L::KCODE + 4 * c, sw[0]);
         lds_run<4>(st + (g + 8) * L::KROW + L::KCODE + 4 * c, sw[1]);
@@ -772,6 +817,16 @@ struct PathM {
         rn0 = lds_u16(kn + 2);
         nk1 = lds_u16(kn + 32);
         rn1 = lds_u16(kn + 34);
+      } else if constexpr (OUT) {  // (norm, scale) and the eight int8 of tokens g, g+8
+        const uint32_t kn = st + L::KBLK + L::VBLK + 12 * g;
+        nk0 = lds_u16(kn);
+        rn0 = lds_u16(kn + 2);
+        lds_run<4>(kn + 4, ow[0]);
+        lds_run<4>(kn + 8, ow[0] + 1);
+        nk1 = lds_u16(kn + 96);
+        rn1 = lds_u16(kn + 98);
+        lds_run<4>(kn + 100, ow[1]);
+        lds_run<4>(kn + 104, ow[1] + 1);
       } else {
         const uint32_t kn = st + L::KBLK + L::VBLK + 2 * g;
         nk0 = lds_u16(kn);
@@ -813,6 +868,16 @@ struct PathM {
         }
         x0 = fmaf(ss[0] + ss[1], __half2float(__ushort_as_half((uint16_t)rn0)) * kSketch, x0);
         x1 = fmaf(ss[2] + ss[3], __half2float(__ushort_as_half((uint16_t)rn1)) * kSketch, x1);
+      }
+      if constexpr (OUT) {  // the eight outlier terms of head c, times each token's scale
+        float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < KVQ_OUTLIER_CHANNELS; ++j) {
+          o0 = fmaf(qo[j], i8f(ow[0][j / 4], j % 4), o0);
+          o1 = fmaf(qo[j], i8f(ow[1][j / 4], j % 4), o1);
+        }
+        x0 = fmaf(o0, __half2float(__ushort_as_half((uint16_t)rn0)), x0);
+        x1 = fmaf(o1, __half2float(__ushort_as_half((uint16_t)rn1)), x1);
       }
       x0 = v0 ? x0 : -INFINITY;
       x1 = v1 ? x1 : -INFINITY;
@@ -997,36 +1062,36 @@ cudaError_t launch_path(const CbParams& p, int sms, cudaStream_t stream) {
   return e;
 }
 
-template <int D, int G, int KB, int VB, bool QJL>
+template <int D, int G, int KB, int VB, int MODE>
 cudaError_t launch_bits(const CbParams& p, int sms, cudaStream_t s) {
-  if constexpr (G == 1) return launch_path<Path1<D, KB, VB, QJL>>(p, sms, s);
-  else return launch_path<PathM<D, G, KB, VB, QJL>>(p, sms, s);
+  if constexpr (G == 1) return launch_path<Path1<D, KB, VB, MODE>>(p, sms, s);
+  else return launch_path<PathM<D, G, KB, VB, MODE>>(p, sms, s);
 }
 
-template <int D, int G, int KB, bool QJL>
+template <int D, int G, int KB, int MODE>
 cudaError_t launch_vb(const CbParams& p, int vb, int sms, cudaStream_t s) {
   switch (vb) {
-    case 2: return launch_bits<D, G, KB, 2, QJL>(p, sms, s);
-    case 3: return launch_bits<D, G, KB, 3, QJL>(p, sms, s);
-    default: return launch_bits<D, G, KB, 4, QJL>(p, sms, s);
+    case 2: return launch_bits<D, G, KB, 2, MODE>(p, sms, s);
+    case 3: return launch_bits<D, G, KB, 3, MODE>(p, sms, s);
+    default: return launch_bits<D, G, KB, 4, MODE>(p, sms, s);
   }
 }
 
-template <int D, int G, bool QJL>
+template <int D, int G, int MODE>
 cudaError_t launch_kb(const CbParams& p, int kb, int vb, int sms, cudaStream_t s) {
   switch (kb) {
-    case 2: return launch_vb<D, G, 2, QJL>(p, vb, sms, s);
-    case 3: return launch_vb<D, G, 3, QJL>(p, vb, sms, s);
-    default: return launch_vb<D, G, 4, QJL>(p, vb, sms, s);
+    case 2: return launch_vb<D, G, 2, MODE>(p, vb, sms, s);
+    case 3: return launch_vb<D, G, 3, MODE>(p, vb, sms, s);
+    default: return launch_vb<D, G, 4, MODE>(p, vb, sms, s);
   }
 }
 
-template <int D, bool QJL>
+template <int D, int MODE>
 cudaError_t launch_g(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s) {
   switch (g) {
-    case 1: return launch_kb<D, 1, QJL>(p, kb, vb, sms, s);
-    case 2: return launch_kb<D, 2, QJL>(p, kb, vb, sms, s);
-    default: return launch_kb<D, 4, QJL>(p, kb, vb, sms, s);
+    case 1: return launch_kb<D, 1, MODE>(p, kb, vb, sms, s);
+    case 2: return launch_kb<D, 2, MODE>(p, kb, vb, sms, s);
+    default: return launch_kb<D, 4, MODE>(p, kb, vb, sms, s);
   }
 }
 
@@ -1034,6 +1099,8 @@ cudaError_t launch_g(const CbParams& p, int g, int kb, int vb, int sms, cudaStre
 cudaError_t launch_cb_qjl(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s);
 // p' = S q' of every query head into p.pq (batch * hkv blocks), before the sketched tiers.
 cudaError_t launch_project_qjl(const CbParams& p, int g, int batch, cudaStream_t s);
+// Keys with an outlier stream (head_dim 128 or 256): instantiated in decode_cb_outlier.cu.
+cudaError_t launch_cb_outlier(const CbParams& p, int d, int g, int kb, int vb, int sms, cudaStream_t s);
 
 }  // namespace cbk
 }  // namespace kvq

@@ -6,7 +6,7 @@ namespace kvq {
 namespace cbk {
 
 cudaError_t launch_cb_qjl(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s) {
-  return launch_g<128, true>(p, g, kb, vb, sms, s);
+  return launch_g<128, kModeSketch>(p, g, kb, vb, sms, s);
 }
 
 cudaError_t launch_project_qjl(const CbParams& p, int g, int batch, cudaStream_t s) {

@@ -23,6 +23,7 @@ struct QuantSide {
   const float* centroids;
   const int8_t* signs;
   const float* qjl;  // KVQ_FMT_CODEBOOK_QJL: projection [KVQ_QJL_DIM][D]
+  const int32_t* outl;  // KVQ_FMT_CODEBOOK_OUTLIER: outlier channels [Hkv][KVQ_OUTLIER_CHANNELS]
   int fmt, bits, row_bytes;
 };
 
@@ -41,6 +42,9 @@ struct QuantParams {
 };
 
 cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t stream);
+// Outlier channels of every kv head (kvq_outlier_calibrate): one block per head.
+cudaError_t launch_outlier_calibrate(const uint16_t* k, int num_tokens, int hkv, int head_dim, int32_t* out,
+                                     cudaStream_t stream);
 // Re-encode: one warp per vector, every destination format.
 cudaError_t launch_requantize(const QuantParams& p, int head_dim, cudaStream_t stream);
 
@@ -60,6 +64,7 @@ struct DecTier {
   const float* k_cent;
   const float* v_cent;
   const float* k_qjl;  // KVQ_FMT_CODEBOOK_QJL keys: projection [KVQ_QJL_DIM][D]
+  const int32_t* k_outl;  // KVQ_FMT_CODEBOOK_OUTLIER keys: outlier channels [Hkv][8]
   const int32_t* block_table;
   const int32_t* seq_lens;
   int k_fmt, v_fmt, k_bits, v_bits, k_row_bytes, v_row_bytes;

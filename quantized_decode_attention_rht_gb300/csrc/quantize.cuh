@@ -180,7 +180,7 @@ __device__ __forceinline__ void encode_codebook(const Table& tb, float (&y)[E], 
   }
 }
 
-enum { F_CB = 0, F_F16 = 1, F_F8 = 2, F_I4 = 3, F_CBQ = 4 };
+enum { F_CB = 0, F_F16 = 1, F_F8 = 2, F_I4 = 3, F_CBQ = 4, F_CBO = 5 };
 
 // Residual sign sketch of one vector (VeloxQuant-MLX page, "Stage 3: QJL Residual
 // Correction"): r holds the lane's kE coordinates of the rotated residual; the bits

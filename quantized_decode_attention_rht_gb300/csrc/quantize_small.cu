@@ -71,6 +71,71 @@ __device__ __forceinline__ void load_rotate(const uint16_t* src, const int8_t* s
   }
 }
 
+// Keys with an outlier stream (VeloxQuant-MLX page, "Outlier Two-Stream Cache"): the
+// lane's coordinates of x (unrotated, fp16 -> fp32) with the head's outlier channels c_j
+// set to zero; xo[j] = x[c_j] in every lane.  Then y = H (s * x_inlier).
+template <int E>
+__device__ __forceinline__ void load_split_rotate(const uint16_t* src, const int8_t* sg, const int32_t* outl, int lane,
+                                                  float (&y)[E], float (&xo)[KVQ_OUTLIER_CHANNELS]) {
+  uint32_t xw[E / 2];
+  if constexpr (E == 4) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(src) + lane);
+    xw[0] = u.x;
+    xw[1] = u.y;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + lane);
+    xw[0] = u.x;
+    xw[1] = u.y;
+    xw[2] = u.z;
+    xw[3] = u.w;
+  }
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) {
+    const __half2 h2 = *reinterpret_cast<const __half2*>(&xw[k]);
+    y[2 * k] = __low2float(h2);
+    y[2 * k + 1] = __high2float(h2);
+  }
+  const int4 c0 = __ldg(reinterpret_cast<const int4*>(outl)), c1 = __ldg(reinterpret_cast<const int4*>(outl) + 1);
+  const int ch[KVQ_OUTLIER_CHANNELS] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int j = 0; j < KVQ_OUTLIER_CHANNELS; ++j) {
+    float mine = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (lane * E + e == ch[j]) {
+        mine = y[e];
+        y[e] = 0.f;
+      }
+    }
+    xo[j] = __shfl_sync(0xFFFFFFFFu, mine, (ch[j] / E) & 31);
+  }
+  int8_t s8[E];
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint32_t*>(s8) = __ldg(reinterpret_cast<const uint32_t*>(sg) + lane);
+  } else {
+    *reinterpret_cast<uint2*>(s8) = __ldg(reinterpret_cast<const uint2*>(sg) + lane);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) y[e] = s8[e] < 0 ? -y[e] : y[e];
+#pragma unroll
+  for (int hs = 1; hs < E; hs <<= 1) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if ((e & hs) == 0) {
+        const float a = y[e], c = y[e + hs];
+        y[e] = a + c;
+        y[e + hs] = a - c;
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) y[e] = fmaf(sgn, y[e], __shfl_xor_sync(0xFFFFFFFFu, y[e], m));
+  }
+}
+
 // y = x~ for the lane's coordinates, from a stored fp16 row of the rotated vector.
 template <int E>
 __device__ __forceinline__ void load_row(const uint8_t* row, int lane, float (&y)[E]) {
@@ -159,10 +224,11 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
   constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
   constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
   constexpr float ys = FROM_ROWS ? 1.0f : inv_sqrt_d;
-  constexpr int NB = (FMT == F_CB || FMT == F_CBQ) ? (1 << BITS) - 1 : 1;
+  constexpr bool CB = FMT == F_CB || FMT == F_CBQ || FMT == F_CBO;
+  constexpr int NB = CB ? (1 << BITS) - 1 : 1;
   const int lane = threadIdx.x & 31;
   float bnd[NB];
-  if constexpr (FMT == F_CB || FMT == F_CBQ) {
+  if constexpr (CB) {
 #pragma unroll
     for (int i = 0; i < NB; ++i) bnd[i] = __ldg(side.bounds + i);
   }
@@ -171,8 +237,11 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
     const int token = v / p.hkv, h = v - token * p.hkv;
     const int slot = p.slots[token];
     if (slot < 0 || slot >= p.num_slots) continue;  // warp-uniform
-    float y[E];
-    if constexpr (FROM_ROWS) {
+    float y[E], xo[KVQ_OUTLIER_CHANNELS];
+    if constexpr (FMT == F_CBO) {
+      load_split_rotate<E>(x + (size_t)v * D, side.signs + (size_t)h * D, side.outl + h * KVQ_OUTLIER_CHANNELS,
+                           lane, y, xo);
+    } else if constexpr (FROM_ROWS) {
       const int ss = p.src_slots[token];
       if (ss < 0 || ss >= p.src_num_slots) continue;
       const size_t srow = ((size_t)(ss / p.page_size) * p.hkv + h) * p.page_size + (ss % p.page_size);
@@ -182,7 +251,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
     }
     const size_t prow = ((size_t)(slot / p.page_size) * p.hkv + h) * p.page_size + (slot % p.page_size);
     uint8_t* row = side.rows + prow * side.row_bytes;
-    if constexpr (FMT == F_CB || FMT == F_CBQ) {
+    if constexpr (CB) {
       float ss = 0.f;
 #pragma unroll
       for (int e = 0; e < E; ++e) ss = fmaf(y[e], y[e], ss);
@@ -203,6 +272,26 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
       store_fields<D, E, BITS>(buf, fields, row, lane);
       if constexpr (FMT == F_CB) {
         if (lane == 0) side.aux[prow] = norm16;
+      } else if constexpr (FMT == F_CBO) {
+        // the outlier stream: int8 with a per-token scale s = fp16(max |x_cj| / 127)
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < KVQ_OUTLIER_CHANNELS; ++j) amax = fmaxf(amax, fabsf(xo[j]));
+        const __half s16 = __float2half_rn(amax / 127.0f);
+        const float sc = __half2float(s16);
+        uint32_t qw[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < KVQ_OUTLIER_CHANNELS; ++j) {
+          const float qv = sc > 0.f ? fminf(fmaxf(rintf(xo[j] / sc), -127.f), 127.f) : 0.f;
+          qw[j / 4] |= ((uint32_t)(int)qv & 0xFFu) << (8 * (j % 4));
+        }
+        if (lane == 0) {
+          uint32_t* rec = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(side.aux) +
+                                                      prow * (4 + KVQ_OUTLIER_CHANNELS));
+          rec[0] = (uint32_t)__half_as_ushort(norm16) | ((uint32_t)__half_as_ushort(s16) << 16);
+          rec[1] = qw[0];
+          rec[2] = qw[1];
+        }
       } else {
         // y <- the rotated residual x~ - x^~ against the decoded vector (stored fp16 norm)
         const float dscale = __half2float(norm16) * inv_sqrt_d;
@@ -286,6 +375,9 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(const QuantParams p
   switch (side.fmt) {
     case KVQ_FMT_CODEBOOK: append_bits<D, F_CB, FROM_ROWS>(p, side, x, src, buf); break;
     case KVQ_FMT_CODEBOOK_QJL: append_bits<D, F_CBQ, FROM_ROWS>(p, side, x, src, buf); break;
+    case KVQ_FMT_CODEBOOK_OUTLIER:  // new vectors only (the host refuses a re-encode into it)
+      if constexpr (!FROM_ROWS) append_bits<D, F_CBO, false>(p, side, x, src, buf);
+      break;
     case KVQ_FMT_FP16: append_side<D, F_F16, 0, FROM_ROWS>(p, side, x, src, buf); break;
     case KVQ_FMT_FP8_E4M3: append_side<D, F_F8, 0, FROM_ROWS>(p, side, x, src, buf); break;
     default: append_side<D, F_I4, 0, FROM_ROWS>(p, side, x, src, buf); break;

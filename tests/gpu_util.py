@@ -145,6 +145,23 @@ def check_qjl_rows(x16, signs, bits, proj, rows_gpu, aux_gpu, kind="lloyd_max", 
     return int(np.sum(same)), int(np.sum(bad)), int(np.sum(rdiff))
 
 
+def check_outlier_rows(x16, signs, bits, channels, rows_gpu, aux_gpu, kind="lloyd_max"):
+    """Keys with an outlier stream: x16 [T, d] of one head, channels [K].  The inlier codes
+    and norm follow the codebook criteria on the rotated inlier vector (outlier channels
+    zeroed); the outlier scale and the int8 values must equal the oracle's exactly (both
+    come from exact fp16 inputs through one float32 division and one rounding each)."""
+    c32, b32 = tables(kind, bits)
+    x_in = np.array(x16, dtype=np.float16)
+    x_in[:, np.asarray(channels)] = 0
+    norm_g, scale_g, q_g = ocache.unpack_outlier_aux(aux_gpu)
+    stats = check_codebook_codes(x_in, signs, bits, rows_gpu, norm_g)
+    _, aux_o = ocache.encode(x16, signs, "codebook_outlier", bits, b32, c32, outliers=channels)
+    _, scale_o, q_o = ocache.unpack_outlier_aux(aux_o)
+    assert np.array_equal(scale_g.view(np.uint16), scale_o.view(np.uint16)), "outlier scales differ"
+    assert np.array_equal(q_g, q_o), "int8 outlier values differ"
+    return stats
+
+
 def check_float_rows(x16, signs, fmt, rows_gpu, xr=None):
     """fp16 / fp8 rows: every stored value must be the format's rounding of SOME value within
     the kernel's rotation error tau of the exact rotated coordinate, i.e. lie between the
@@ -208,7 +225,8 @@ class Built:
         self.ora, self.gpu, self.views, self.k_signs, self.v_signs = ora_tiers, gpu_caches, views, k_signs, v_signs
 
 
-def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16, shuffle_seed=None, k_qjl=None):
+def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16, shuffle_seed=None, k_qjl=None,
+                k_outl=None):
     """tier_specs: list of workloads.Tier; tier_kv: per tier, per sequence, (k [L, Hkv, D], v)
     fp16.  The ORACLE encodes every row into numpy pools; those bytes are uploaded into the
     GPU caches unchanged.  Returns Built."""
@@ -229,10 +247,12 @@ def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16,
         for b, n in enumerate(per):
             bt[b, :n] = phys[at: at + n]
             at += n
-        kc = tables(spec.codebook, spec.k_bits) if spec.k_format in ("codebook", "codebook_qjl") else (None, None)
+        kc = tables(spec.codebook, spec.k_bits) if spec.k_format.startswith("codebook") else (None, None)
         vc = tables(spec.codebook, spec.v_bits) if spec.v_format == "codebook" else (None, None)
         proj = k_qjl if spec.k_format == "codebook_qjl" else None
-        ks = ocache.new_side(spec.k_format, spec.k_bits, kc[0], kc[1], k_signs, num_pages, hkv, page_size, d, proj)
+        outl = k_outl if spec.k_format == "codebook_outlier" else None
+        ks = ocache.new_side(spec.k_format, spec.k_bits, kc[0], kc[1], k_signs, num_pages, hkv, page_size, d, proj,
+                             outl)
         vs = ocache.new_side(spec.v_format, spec.v_bits, vc[0], vc[1], v_signs, num_pages, hkv, page_size, d)
         for b, (k, v) in enumerate(seqs):
             t = np.arange(k.shape[0])
@@ -241,7 +261,7 @@ def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16,
             ocache.write(vs, slots, v, page_size)
         ora_tiers.append(oatt.TierState(ks, vs, bt, lens, page_size))
         c = kvq.PagedCache(d, hkv, num_pages, spec.k_format, spec.v_format, spec.k_bits, spec.v_bits,
-                           ks_dev, vs_dev, page_size, spec.codebook, k_qjl=proj)
+                           ks_dev, vs_dev, page_size, spec.codebook, k_qjl=proj, k_outliers=outl)
         c.k_rows.copy_(torch.from_numpy(ks.rows))
         c.v_rows.copy_(torch.from_numpy(vs.rows))
         if ks.aux is not None:

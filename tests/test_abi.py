@@ -54,7 +54,7 @@ def test_status_strings(kvq):
 
 @pytest.mark.parametrize("d", [128, 256])
 def test_row_bytes_match_oracle(kvq, d):
-    for fmt in ("codebook", "codebook_qjl", "fp16", "fp8_e4m3", "int4_g32"):
+    for fmt in ("codebook", "codebook_qjl", "codebook_outlier", "fp16", "fp8_e4m3", "int4_g32"):
         for bits in ((2, 3, 4) if fmt.startswith("codebook") else (0,)):
             assert kvq.kvq_row_bytes(fmt, bits, d) == (ofmt.row_bytes(fmt, bits, d), ofmt.aux_bytes(fmt, d))
     with pytest.raises(kvq.KvqError):
@@ -212,3 +212,38 @@ def test_requantize_checks(kvq):
     assert rq(win, dst, n=2, ss=None) == 1
     assert rq(win, dst, n=2, ds=(1 << 43) + 2) == 1
     assert rq(_fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_rows=(1 << 40) + 8), dst, n=0) == 1
+
+
+def _outl_cache(kvq, **kw):
+    args = dict(k_format=kvq.FMT_CODEBOOK_OUTLIER, k_outliers=(1 << 40) + 4096 * 32)
+    args.update(kw)
+    return _fake_cache(kvq, **args)
+
+
+def test_outlier_key_checks(kvq):
+    """Keys with an outlier stream need the channel list (16-byte aligned) and 16-byte
+    aligned side data; values may not carry one; decode runs on the codebook kernel
+    (head_dim 128 or 256, groups 1, 2, 4); a re-encode into it is not offered."""
+    assert kvq.kvq_row_bytes("codebook_outlier", 4, 128) == (64, 12)
+    assert _quant(kvq, _outl_cache(kvq), n=0) == 0
+    assert _quant(kvq, _outl_cache(kvq, k_outliers=None)) == 1
+    assert _quant(kvq, _outl_cache(kvq, k_outliers=(1 << 40) + 4096 * 32 + 4)) == 1
+    assert _quant(kvq, _outl_cache(kvq, k_aux=(1 << 40) + 4096 * 2 + 4)) == 1
+    assert _quant(kvq, _outl_cache(kvq, v_format=kvq.FMT_CODEBOOK_OUTLIER)) == 1
+    assert _ws(kvq, [_outl_cache(kvq)])[0] == 0
+    assert _ws(kvq, [_outl_cache(kvq, head_dim=256)])[0] == 0
+    assert _ws(kvq, [_outl_cache(kvq)], hq=2 * 4)[0] == 0
+    assert _ws(kvq, [_outl_cache(kvq)], hq=2 * 8)[0] == 2
+    assert _ws(kvq, [_outl_cache(kvq, v_format=kvq.FMT_FP16, v_bits=0)])[0] == 2
+    win = _fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_bits=0, v_bits=0)
+    assert kvq.lib().kvq_requantize(ctypes.byref(win), 1 << 42, ctypes.byref(_outl_cache(kvq)), 1 << 43, 0,
+                                    None) == 2
+
+
+def test_outlier_calibrate_checks(kvq):
+    L = kvq.lib()
+    assert L.kvq_outlier_calibrate(None, 10, 2, 128, 1 << 42, None) == 1
+    assert L.kvq_outlier_calibrate(1 << 41, 0, 2, 128, 1 << 42, None) == 1
+    assert L.kvq_outlier_calibrate(1 << 41, 10, 0, 128, 1 << 42, None) == 1
+    assert L.kvq_outlier_calibrate(1 << 41, 10, 2, 64, 1 << 42, None) == 2
+    assert L.kvq_outlier_calibrate(1 << 41, 10, 2, 128, (1 << 42) + 2, None) == 1
