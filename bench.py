@@ -262,7 +262,9 @@ def cpu_oracle_run(config: str, steps: int, warmup: int, out_json: str | None = 
         pm = W.page_map(cfg.scaled(batch=nb), tl, tier=t)
         k_side = ocache.new_side(tier.k_format, tier.k_bits, kt[0], kt[1], ks, pm.num_pages, cfg.num_kv_heads,
                                  cfg.page_size, cfg.head_dim,
-                                 W.qjl_projection(cfg) if tier.k_format == "codebook_qjl" else None)
+                                 W.qjl_projection(cfg) if tier.k_format == "codebook_qjl" else None,
+                                 ocache.outlier_channels(W.calibration_keys(cfg))
+                                 if tier.k_format == "codebook_outlier" else None)
         v_side = ocache.new_side(tier.v_format, tier.v_bits, vt[0], vt[1], vs, pm.num_pages, cfg.num_kv_heads,
                                  cfg.page_size, cfg.head_dim)
         tiers.append(oatt.TierState(k_side, v_side, pm.block_table, tl, cfg.page_size))

@@ -209,7 +209,8 @@ def pool_index(torch, wl, t, b, n):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["tiny", "llama7b", "llama7b_prod", "llama7b_window", "gqa32k", "ragged", "append"])
+@pytest.mark.parametrize("name", ["tiny", "llama7b", "llama7b_prod", "llama7b_window", "llama7b_outlier", "gqa32k",
+                                  "ragged", "append"])
 def test_full_size_sampled_heads(name):
     """Every workload at its full size, built on the GPU by kvq_quantize_append and decoded with
     the split plan the benchmark uses.  For sampled (sequence, kv head) pairs:
@@ -235,6 +236,10 @@ def test_full_size_sampled_heads(name):
     picks.append((cfg.batch - 1, cfg.num_q_heads - 1))
     ks_all, vs_all = W.signs(cfg, 0), W.signs(cfg, 1)
     proj = W.qjl_projection(cfg)
+    chans = None
+    if any(t.k_format == "codebook_outlier" for t in cfg.tiers):
+        chans = ocache.outlier_channels(W.calibration_keys(cfg))  # the oracle's calibration ...
+        assert np.array_equal(wl.k_outliers.cpu().numpy(), chans)  # ... equals the library's
     kv_ref, sketch_rows = {}, {}
     near = total_el = 0
     for b, g in sorted({(b, h // cfg.group) for b, h in picks}):
@@ -254,6 +259,8 @@ def test_full_size_sampled_heads(name):
                 tab = gu.tables(tier.codebook, bits) if fmt.startswith("codebook") else (None, None)
                 if fmt == "codebook_qjl":
                     gu.check_qjl_rows(x, sg, bits, proj, rows_g, aux_g, kind=tier.codebook)
+                elif fmt == "codebook_outlier":
+                    gu.check_outlier_rows(x, sg, bits, chans[g], rows_g, aux_g, kind=tier.codebook)
                 elif fmt == "codebook":
                     st = gu.check_codebook_codes(x, sg, bits, rows_g, aux_g[:, 0], kind=tier.codebook)
                     near, total_el = near + st[1], total_el + st[2]
@@ -261,13 +268,15 @@ def test_full_size_sampled_heads(name):
                     gu.check_int4_rows(x, sg, rows_g, aux_g)
                 else:
                     gu.check_float_rows(x, sg, fmt, rows_g)
-                rows_o, aux_o = ocache.encode(x, sg, fmt, bits, tab[1], tab[0], proj)
+                rows_o, aux_o = ocache.encode(x, sg, fmt, bits, tab[1], tab[0], proj,
+                                              chans[g] if fmt == "codebook_outlier" else None)
                 if side == "k":
                     SK.append((rows_o, aux_o) if fmt == "codebook_qjl" else n)
                 rows_t[pages, g, offs] = torch.from_numpy(rows_o).cuda()
                 if aux_t is not None:
                     aux_t[pages, g, offs] = torch.from_numpy(np.asarray(aux_o).reshape(n, -1)).cuda()
-                dec = ocache.decode(rows_o, aux_o, fmt, sg, cfg.head_dim, bits, tab[0])
+                dec = ocache.decode(rows_o, aux_o, fmt, sg, cfg.head_dim, bits, tab[0],
+                                    chans[g] if fmt == "codebook_outlier" else None)
                 (K if side == "k" else V).append(dec)
         kv_ref[(b, g)] = (np.concatenate(K), np.concatenate(V))
         sketch_rows[(b, g)] = SK

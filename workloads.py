@@ -36,6 +36,8 @@ S_K, S_V, S_Q, S_OUTLIER, S_TIER, S_LENS, S_PAGES, S_SIGNS, S_SIGMA, S_NEWTOK, S
 # Storage format names (the same four the C header enumerates).
 CODEBOOK, FP16, FP8_E4M3, INT4_G32 = "codebook", "fp16", "fp8_e4m3", "int4_g32"
 CODEBOOK_QJL = "codebook_qjl"  # keys: codebook codes + residual sign sketch
+CODEBOOK_OUTLIER = "codebook_outlier"  # keys: codebook codes + int8 outlier channels
+OUTLIER_CALIBRATION = 256  # calibration tokens of the outlier stream (the first of sequence 0)
 QJL_DIM = 128
 
 
@@ -93,6 +95,10 @@ CONFIGS: Dict[str, Config] = {
     # fp16 (the hybrid threshold), the older ones 4-bit LM
     "llama7b_window": Config("llama7b_window", 8, 32, 32, 128, 8192, (LM4, Tier(FP16, FP16, window=256)), seed=1,
                              outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
+    # the same layer with outlier two-stream keys: 8 channels per kv head (calibrated on the
+    # first 256 tokens of sequence 0) as int8, the rest 4-bit LM; 4-bit LM values
+    "llama7b_outlier": Config("llama7b_outlier", 8, 32, 32, 128, 8192, (Tier(CODEBOOK_OUTLIER, CODEBOOK, 4, 4),),
+                              seed=1, outlier_mode="pairs", outlier_count=41, outlier_scale=50.0),
     # the same layer with product-quantised keys: 3-bit LM codes + 128-bit residual sign
     # sketch (4 bits per coordinate), 4-bit LM values
     "llama7b_prod": Config("llama7b_prod", 8, 32, 32, 128, 8192, (Tier(CODEBOOK_QJL, CODEBOOK, 3, 4),), seed=1,
@@ -320,6 +326,13 @@ def sequence_tiers(cfg: Config, b: int, total: int):
     return out
 
 
+def calibration_keys(cfg: Config) -> np.ndarray:
+    """fp16 keys [N, Hkv, D] of the first N = min(OUTLIER_CALIBRATION, L_0) tokens of sequence
+    0, in position order: the calibration sample of the outlier stream."""
+    n = min(OUTLIER_CALIBRATION, int(seq_lens(cfg)[0]))
+    return np.stack([kv_head(cfg, 0, 0, h, n) for h in range(cfg.num_kv_heads)], axis=1)
+
+
 def chunk_kv(cfg: Config, b: int, stream: int, n: int):
     """Token-major fp16 K/V [n, Hkv, D] of n appended tokens of sequence b, drawn from the
     appended-token stream `stream` (0 = prefill chunk, 1 + s = decode step s)."""
@@ -357,12 +370,21 @@ class GpuWorkload:
         self.v_signs = torch.from_numpy(vs).to(device)
         self.k_qjl = (torch.from_numpy(qjl_projection(cfg)).to(device)
                       if any(t.k_format == CODEBOOK_QJL for t in cfg.tiers) else None)
+        self.k_outliers = None
+        if any(t.k_format == CODEBOOK_OUTLIER for t in cfg.tiers):
+            # the library's calibration over the first tokens of sequence 0
+            self.calib_tokens = calibration_keys(cfg)
+            self.k_outliers = torch.empty((cfg.num_kv_heads, kvq.OUTLIER_CHANNELS), dtype=torch.int32,
+                                          device=device)
+            kvq.kvq_outlier_calibrate(torch.from_numpy(self.calib_tokens).to(device), self.k_outliers)
         self.caches = []
         for t, tier in enumerate(cfg.tiers):
             self.caches.append(kvq.PagedCache(cfg.head_dim, cfg.num_kv_heads, self.maps[t].num_pages,
                                               tier.k_format, tier.v_format, tier.k_bits, tier.v_bits,
                                               self.k_signs, self.v_signs, cfg.page_size, tier.codebook, device,
-                                              k_qjl=self.k_qjl if tier.k_format == CODEBOOK_QJL else None))
+                                              k_qjl=self.k_qjl if tier.k_format == CODEBOOK_QJL else None,
+                                              k_outliers=self.k_outliers if tier.k_format == CODEBOOK_OUTLIER
+                                              else None))
         self.block_tables = [torch.from_numpy(np.maximum(m.block_table, 0)).to(device) for m in self.maps]
         self.seq_lens_dev = [torch.from_numpy(l.astype(np.int32)).to(device) for l in self.tier_len]
         self.device = device
