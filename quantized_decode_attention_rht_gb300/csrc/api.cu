@@ -128,9 +128,13 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
     const int kind = plan->kind[i];
     int chunk = split_tokens;
     if (chunk == 0 && kind != TIER_GENERIC) {
+      // items per SM: enough that the last ones to finish leave little idle time.  The
+      // codebook kernel's tensor-core path (groups of 2 and 4) spends more time per byte
+      // than its FMA path, so its items carry fewer bytes (measured on GB300: 4-bit G = 1
+      // best at 72 items per SM, 3/2-bit G = 4 at 288, the fp16 / fp8 kernel at 64)
       const size_t fb = family_bytes[kind];
-      const size_t item_bytes = kind == TIER_GQA ? std::max<size_t>(16 << 10, fb / (kSms * 8 * 4))
-                                                 : std::max<size_t>(16 << 10, fb / (kSms * 12 * 6));
+      const size_t per_sm = kind == TIER_GQA ? 64 : (group >= 2 ? 288 : 72);
+      const size_t item_bytes = std::max<size_t>(16 << 10, fb / (kSms * per_sm));
       const size_t tok = item_bytes / token_bytes(tiers[i].cache);
       const size_t cap = kind == TIER_GQA ? (size_t)gqa_max_chunk_tokens() : (size_t)1 << 20;
       chunk = (int)std::min<size_t>(cap, std::max<size_t>(ps, tok / ps * ps));
