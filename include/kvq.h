@@ -182,12 +182,15 @@ KVQ_API kvq_status kvq_uniform_codebook(int32_t bits, double* centroids, double*
 KVQ_API kvq_status kvq_codebook_tables(int32_t bits, const double* centroids,
                                        float* centroids32, float* bounds32);
 
-/* Quantise-and-append (one launch): for every token i < num_tokens and kv head h, rotate
+/* Quantise-and-append: for every token i < num_tokens and kv head h, rotate
  * k[i][h][:] (fp16, [num_tokens][num_kv_heads][head_dim]) with k_signs[h], encode it in
  * cache->k_format and store it at pool slot slot_mapping[i]; the same for v with v_signs.
- * k or v may be NULL to append only the other side.  slot_mapping: int32 [num_tokens];
- * a negative slot skips the token; slots >= num_pages * page_size are skipped too.
- * Two tokens of one call must not share a slot.  k, v: 16-byte aligned. */
+ * k or v may be NULL to append only the other side (not both, unless num_tokens is 0:
+ * an empty append returns KVQ_OK whatever the pointers).  slot_mapping: int32
+ * [num_tokens]; a negative slot skips the token; slots >= num_pages * page_size are
+ * skipped too.  Two tokens of one call must not share a slot.  k, v: 16-byte aligned.
+ * Up to 16384 vectors per side (a decode step) take one launch for both sides; larger
+ * appends one launch per side (keys with an outlier stream: one launch). */
 KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k,
                                        const uint16_t* v, int32_t num_tokens,
                                        const int32_t* slot_mapping, void* stream);

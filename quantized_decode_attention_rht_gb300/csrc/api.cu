@@ -318,8 +318,9 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
                                        int32_t num_tokens, const int32_t* slot_mapping, void* stream) {
   kvq_status st = check_cache(cache);
   if (st != KVQ_OK) return st;
-  if (num_tokens < 0 || (!k && !v)) return KVQ_ERR_INVALID_ARGUMENT;
-  if (num_tokens == 0) return KVQ_OK;
+  if (num_tokens < 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (num_tokens == 0) return KVQ_OK;  // nothing to append (an empty tensor may have no address)
+  if (!k && !v) return KVQ_ERR_INVALID_ARGUMENT;
   if (!slot_mapping || !aligned(slot_mapping, 4)) return KVQ_ERR_INVALID_ARGUMENT;
   if ((k && !aligned(k, 16)) || (v && !aligned(v, 16))) return KVQ_ERR_INVALID_ARGUMENT;
   const kvq_cache* c = cache;

@@ -117,6 +117,7 @@ def test_quantize_argument_checks(kvq):
     assert _quant(kvq, _fake_cache(kvq), slots=None) == 1
     assert _quant(kvq, _fake_cache(kvq), k=(1 << 41) + 2) == 1  # input not 16-byte aligned
     assert _quant(kvq, _fake_cache(kvq), n=0) == 0  # nothing to do
+    assert _quant(kvq, _fake_cache(kvq), k=None, v=None, n=0, slots=None) == 0  # empty tensors may have no address
 
 
 def _views(kvq, caches, max_pages=8):

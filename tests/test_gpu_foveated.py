@@ -1,7 +1,7 @@
 """GPU parity of the FoveatedKV kernel features (FoveatedKV page, "Making it fast") through
 kvq_decode_attention_ex, on every decode kernel family: the fused fp16 / fp8 + INT4 kernel,
 the codebook kernel (one query head per kv head, and the tensor-core path for 2 and 4),
-keys with a residual sketch, and the generic kernel.
+keys with a residual sketch or an outlier stream, and the generic kernel.
 
 Spike flags: caches built so that, per (sequence, query head), the near tier's scores sit
 well above or well below the far tier's (margins of several nats), so the float32
@@ -25,7 +25,11 @@ PATHS = {
     "codebook_g4": ((W.Tier("codebook", "codebook", 4, 4), W.Tier("codebook", "codebook", 3, 2)), 4),
     "sketched_g2": ((W.Tier("codebook_qjl", "codebook", 3, 4), W.Tier("codebook", "codebook", 2, 2)), 2),
     "generic_g2": ((W.Tier("fp16", "fp16"), W.Tier("codebook", "codebook", 4, 4)), 2),
+    "outlier_g1": ((W.Tier("codebook_outlier", "codebook", 4, 4), W.Tier("codebook", "codebook", 2, 2)), 1),
+    "outlier_g4": ((W.Tier("codebook_outlier", "codebook", 3, 2), W.Tier("fp8_e4m3", "int4_g32")), 4),
 }
+# any valid channel list serves exact-bytes parity (oracle and kernel read the same one)
+OUTLIER_LIST = np.tile(np.array([0, 5, 17, 40, 64, 99, 100, 127], dtype=np.int32), (2, 1))
 
 
 def decode_ex(kvq, torch, views, q16, split_tokens=0, score_gate=False, spikes=False):
@@ -65,7 +69,7 @@ def test_spike_flags(name):
     q16 = (4.0 * sign[..., None] * u[np.arange(hq) // group][None]).astype(np.float16)
     cfg = W.CONFIGS["llama7b"].scaled(num_q_heads=hq, num_kv_heads=hkv)
     built = gu.build_exact(kvq, torch, list(tiers), kv, W.signs(cfg, 0), W.signs(cfg, 1), 16, 3,
-                           k_qjl=W.qjl_projection(cfg))
+                           k_qjl=W.qjl_projection(cfg), k_outl=OUTLIER_LIST)
     got, flags = decode_ex(kvq, torch, built.views, q16, split_tokens=32, spikes=True)
     want_flags, margin = oatt.spike_flags(q16, built.ora)
     defined = ~np.isnan(margin)
@@ -102,7 +106,7 @@ def test_score_gate_within_bound(name):
                                dtype=np.float16)
     cfg = W.CONFIGS["llama7b"].scaled(num_q_heads=hq, num_kv_heads=hkv)
     built = gu.build_exact(kvq, torch, list(tiers), kv, W.signs(cfg, 0), W.signs(cfg, 1), 16, None,
-                           k_qjl=W.qjl_projection(cfg))
+                           k_qjl=W.qjl_projection(cfg), k_outl=OUTLIER_LIST)
     split = 1024  # one chunk per tier and sequence: the sink sets the running maximum early
     gated_gpu, _ = decode_ex(kvq, torch, built.views, q16, split, score_gate=True)
     plain_gpu, _ = decode_ex(kvq, torch, built.views, q16, split)
