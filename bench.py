@@ -192,6 +192,35 @@ def step_bytes(cfg, wl, kvq):
     return dec, quant
 
 
+def output_error_vs_fp16(cfg, wl, q_host, out, k_new, v_new, window, samples=4):
+    """Relative error of the decode output against exact attention over the UNQUANTISED fp16
+    cache (the quality cost of the compression, not a parity check): for a few (sequence,
+    query head) pairs, softmax(q K^T / sqrt(d)) V in float64 over the fp16 keys and values
+    the cache holds -- the seeded inputs, with the token each step overwrote replaced by the
+    step's new one.  Plain numpy; returns the mean and max of ||out - exact|| / ||exact||."""
+    import numpy as np
+    import workloads as W
+    rng = np.random.default_rng(5)
+    picks = sorted({(int(rng.integers(cfg.batch)), int(rng.integers(cfg.num_q_heads))) for _ in range(samples)})
+    errs = []
+    for b, h in picks:
+        g = h // cfg.group
+        n = int(wl.lens[b])
+        k = W.kv_head(cfg, 0, b, g, n).astype(np.float64)
+        v = W.kv_head(cfg, 1, b, g, n).astype(np.float64)
+        members = W.tier_members(cfg, b, g, n)[-1]
+        if len(members):
+            i = members[0] if window else members[-1]  # the slot the bench step writes
+            k[i], v[i] = k_new[b, g], v_new[b, g]
+        s = k @ q_host[b, h].astype(np.float64) / np.sqrt(cfg.head_dim)
+        w = np.exp(s - s.max())
+        exact = (w / w.sum()) @ v
+        errs.append(float(np.linalg.norm(out[b, h].astype(np.float64) - exact) / np.linalg.norm(exact)))
+    return {"rel_err_vs_fp16_cache": {"mean": float(np.mean(errs)), "max": float(np.max(errs))},
+            "sample": f"{len(picks)} (sequence, query head) pairs; exact softmax(qK^T/sqrt(d))V over the "
+                      "unquantised fp16 K/V in float64"}
+
+
 def quantize_throughput(kvq, torch, reps=5):
     """Quantise-and-append of the append workload's prefill chunk: 4 sequences x 16384 tokens x
     16 kv heads x (K, V), head_dim 256, 4-bit Lloyd-Max, per-channel std log-uniform in
@@ -473,6 +502,11 @@ def run_ours(args):
     h2d = k_new.nbytes + v_new.nbytes + q_host.nbytes
     d2h = out_d.numel() * 4
 
+    quality = None
+    if rank == 0:
+        kvq.kvq_decode_attention(views, q_d, out_d, ws_d, 0, stream)  # the step's output, options off
+        torch.cuda.synchronize()
+        quality = output_error_vs_fp16(cfg, wl, q_host, out_d.cpu().numpy(), k_new, v_new, window)
     quant = quantize_throughput(kvq, torch) if rank == 0 else None
     barrier(ws)
     if rank != 0:
@@ -499,6 +533,7 @@ def run_ours(args):
         "e2e": {"value": ws * (dec_bytes + quant_bytes) / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "gpu_launches": launches,
+        "quality": quality,
         "clocks": clk,
         "options": {"score_gate": args.score_gate, "spike_flags": args.spike_flags, "query_scale": args.query_scale},
     }
