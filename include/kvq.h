@@ -22,8 +22,10 @@
  * Conventions that hold for every function:
  *   - Pointers are DEVICE pointers unless the comment says "host".
  *   - The caller owns every buffer.  The library allocates nothing, keeps no mutable
- *     global state (kvq_decode_attention_noalloc, at the end, is the one exception),
- *     never synchronises, and is safe to call from several threads.
+ *     global state besides a kernel-launch counter (kvq_kernel_launches) and a per-device
+ *     note of the kernels whose shared-memory limit it has raised (both atomic;
+ *     kvq_decode_attention_noalloc, at the end, adds its scratch array), never
+ *     synchronises, and is safe to call from several threads.
  *   - GPU work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
  *     stream) and ordered with the caller's other work on that stream.
  *   - Arguments are checked on the host before anything is launched; a failed check

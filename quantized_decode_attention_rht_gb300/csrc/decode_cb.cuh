@@ -49,6 +49,7 @@
 // -- keys with a residual sketch -- so the two instance sets compile in parallel.)
 #pragma once
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "kvq_internal.cuh"
@@ -1035,15 +1036,16 @@ cudaError_t launch_path(const CbParams& p, int sms, cudaStream_t stream) {
   auto kern = decode_cb_kernel<P>;
   CbParams q = p;
   q.smem_bytes = L::SMEM;
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // shared-memory limit raised on this device (threads may race: a
+                                           // second raise is harmless)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_relaxed);
   }
   const int ctas = std::max(1, std::min(sms, (p.total_items + 2 * L::WARPS - 1) / (2 * L::WARPS)));
   cudaLaunchConfig_t cfg = {};

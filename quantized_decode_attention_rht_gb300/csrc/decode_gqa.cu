@@ -26,6 +26,7 @@
 // carries log2(e) / D), one exp2 per score, a running max per head; accumulators rescale
 // only when the max grows.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "kvq_internal.cuh"
@@ -625,15 +626,16 @@ int gqa_max_chunk_tokens() { return kMaxPagesPerItem * PS; }
 
 cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t stream, bool trigger) {
   constexpr int smem = kWarps * kWarpSmem;
-  static bool configured[64] = {};
+  static std::atomic<bool> configured[64];  // shared-memory limit raised on this device (threads may race: a
+                                           // second raise is harmless)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
+  if (!configured[dev].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(decode_gqa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_relaxed);
   }
   GqaParams p;
   memset(&p, 0, sizeof(p));
