@@ -92,6 +92,9 @@ WINDOW_CASES = {
     "fp8_int4_g1": ((W.Tier("fp8_e4m3", "int4_g32"), W.Tier("fp16", "fp16")), 1),
     "fp8_int4_g2": ((W.Tier("fp8_e4m3", "int4_g32"), W.Tier("fp16", "fp16")), 2),
     "three_tiers_g1": ((W.Tier("fp16", "fp16"), W.Tier("codebook", "codebook", 2, 2), W.Tier("fp16", "fp16")), 1),
+    # head_dim 256: the window tier runs on the generic kernel next to the codebook one
+    "codebook_d256_g2": ((W.Tier("codebook", "codebook", 4, 4), W.Tier("fp16", "fp16")), 2, 256),
+    "outlier_d256_g1": ((W.Tier("codebook_outlier", "codebook", 3, 3), W.Tier("fp16", "fp16")), 1, 256),
 }
 
 
@@ -102,24 +105,25 @@ def test_window_tier_decode(name):
     call, each tier on its kernel family: exact bytes, oracle dequantise-then-attend."""
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
-    tiers, group = WINDOW_CASES[name]
+    tiers, group, d = (WINDOW_CASES[name] + (128,))[:3]
     hkv = 2
-    cfg = W.CONFIGS["llama7b"].scaled(batch=5, num_q_heads=hkv * group, num_kv_heads=hkv, tiers=tiers)
+    cfg = W.CONFIGS["llama7b"].scaled(batch=5, num_q_heads=hkv * group, num_kv_heads=hkv, tiers=tiers, head_dim=d)
     lens = [0, 40, 64, 65, 700]
     win = 64
     rng = np.random.default_rng(7)
     kv = [[] for _ in tiers]
     for b, n in enumerate(lens):
-        kk = np.stack([W.kv_head(cfg, 0, b, h, n) for h in range(hkv)], axis=1).reshape(n, hkv, 128)
-        vv = np.stack([W.kv_head(cfg, 1, b, h, n) for h in range(hkv)], axis=1).reshape(n, hkv, 128)
+        kk = np.stack([W.kv_head(cfg, 0, b, h, n) for h in range(hkv)], axis=1).reshape(n, hkv, d)
+        vv = np.stack([W.kv_head(cfg, 1, b, h, n) for h in range(hkv)], axis=1).reshape(n, hkv, d)
         body = n - min(n, win)  # the window holds the newest tokens; older ones are split
         inner = sorted(int(c) for c in rng.integers(0, body + 1, len(tiers) - 2))  # among the quantised tiers
         cuts = [0] + inner + [body, n]
         for t in range(len(tiers)):
             kv[t].append((kk[cuts[t]:cuts[t + 1]], vv[cuts[t]:cuts[t + 1]]))
     q = W.queries(cfg)
+    chans = np.tile(np.arange(0, d, d // 8, dtype=np.int32), (hkv, 1))  # any valid outlier channel list
     built = gu.build_exact(kvq, torch, list(tiers), kv, W.signs(cfg, 0), W.signs(cfg, 1), 16, 4,
-                           k_qjl=W.qjl_projection(cfg))
+                           k_qjl=W.qjl_projection(cfg), k_outl=chans)
     got = gu.gpu_decode(kvq, torch, built.views, q)
     want = oatt.decode_attention(q, built.ora)
     assert np.all(got[0] == 0)
