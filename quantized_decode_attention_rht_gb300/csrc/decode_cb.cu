@@ -5,6 +5,8 @@
 
 namespace kvq {
 
+constexpr size_t PS_TOKENS = 16;  // tokens per page on the codebook path
+
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
   return (head_dim == 128 || head_dim == 256) && (group == 1 || group == 2 || group == 4) &&
          v_fmt == KVQ_FMT_CODEBOOK &&
@@ -20,6 +22,13 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
   if (e != cudaSuccess) return e;
   const int group = dp.hq / dp.hkv;
   bool projected = false;  // every sketched tier shares the projection and the queries
+  // large caches take the 16-warp tensor-core instances (measured on GB300: ragged, 1.4 GB,
+  // 1118 -> 1056 us; a 138 MB cache with 2 query heads per kv head 85 -> 89 us, slower)
+  size_t cb_bytes = 0;
+  for (int i = 0; i < dp.num_tiers; ++i)
+    if (dp.tier[i].kind == TIER_CB) cb_bytes += (size_t)dp.batch * dp.hkv * dp.tier[i].max_pages * PS_TOKENS *
+                                                (dp.tier[i].k_row_bytes + dp.tier[i].v_row_bytes);
+  const bool wide = cb_bytes >= ((size_t)512 << 20);
   for (int i = 0; i < dp.num_tiers; ++i) {
     const DecTier& t = dp.tier[i];
     if (t.kind != TIER_CB) continue;
@@ -67,6 +76,8 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL) e = cbk::launch_cb_qjl(p, group, t.k_bits, t.v_bits, sms, stream);
     else if (t.k_fmt == KVQ_FMT_CODEBOOK_OUTLIER)
       e = cbk::launch_cb_outlier(p, head_dim, group, t.k_bits, t.v_bits, sms, stream);
+    else if (head_dim == 128 && group >= 2 && wide)
+      e = cbk::launch_cb_wide(p, group, t.k_bits, t.v_bits, sms, stream);
     else if (head_dim == 128) e = cbk::launch_g<128, cbk::kModePlain>(p, group, t.k_bits, t.v_bits, sms, stream);
     else e = cbk::launch_g<256, cbk::kModePlain>(p, group, t.k_bits, t.v_bits, sms, stream);
     if (e != cudaSuccess) return e;

@@ -689,10 +689,12 @@ struct Path1 {
 };
 
 // ================================================================ G = 2, 4: tensor-core path
-template <int D, int G, int KB, int VB, int MODE>
+// WIDE: 16 warps instead of 12 (register-limited to 128, a few spilled bytes): more warps
+// hide more of the path's latency on large caches, fewer items per warp hurt small ones.
+template <int D, int G, int KB, int VB, int MODE, bool WIDE = false>
 struct PathM {
   static constexpr bool QJL = MODE == kModeSketch, OUT = MODE == kModeOutlier;
-  using L = Layout<D, G, KB, VB, D == 128 ? (QJL ? 10 : 12) : 8, MODE>;
+  using L = Layout<D, G, KB, VB, D == 128 ? (QJL ? 10 : (WIDE ? 16 : 12)) : 8, MODE>;
   static constexpr int kD = D, kG = G;
   static constexpr int SKS = KVQ_QJL_DIM / 16;  // sketch mma k-steps
   static constexpr int KS = D / 16;            // key mma k-steps; also value m-tiles
@@ -1101,6 +1103,9 @@ cudaError_t launch_g(const CbParams& p, int g, int kb, int vb, int sms, cudaStre
 cudaError_t launch_cb_qjl(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s);
 // p' = S q' of every query head into p.pq (batch * hkv blocks), before the sketched tiers.
 cudaError_t launch_project_qjl(const CbParams& p, int g, int batch, cudaStream_t s);
+// Plain codes at head_dim 128 with 2 or 4 query heads per kv head on 16 warps (large
+// caches): instantiated in decode_cb_wide.cu.
+cudaError_t launch_cb_wide(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s);
 // Keys with an outlier stream (head_dim 128 or 256): instantiated in decode_cb_outlier.cu.
 cudaError_t launch_cb_outlier(const CbParams& p, int d, int g, int kb, int vb, int sms, cudaStream_t s);
 
