@@ -68,6 +68,8 @@ def parse_args():
     ap.add_argument("--score-gate", action="store_true")
     ap.add_argument("--spike-flags", action="store_true")
     ap.add_argument("--query-scale", type=float, default=1.0)
+    # tokens per sequence of the quantize measurement's prefill chunk (0: the workload's 16384)
+    ap.add_argument("--quant-tokens", type=int, default=0)
     return ap.parse_args()
 
 
@@ -222,14 +224,15 @@ def output_error_vs_fp16(cfg, wl, q_host, out, k_new, v_new, window, samples=4):
                       "unquantised fp16 K/V in float64"}
 
 
-def quantize_throughput(kvq, torch, reps=5):
+def quantize_throughput(kvq, torch, reps=5, tokens=0):
     """Quantise-and-append of the append workload's prefill chunk: 4 sequences x 16384 tokens x
     16 kv heads x (K, V), head_dim 256, 4-bit Lloyd-Max, per-channel std log-uniform in
-    [0.1, 10].  Inputs generated on the device from a fixed seed (2 GiB, larger than L2)."""
+    [0.1, 10].  Inputs generated on the device from a fixed seed (2 GiB, larger than L2).
+    tokens > 0: that many tokens per sequence instead (a smaller chunk for profiling)."""
     import numpy as np
     import workloads as W
     cfg = W.CONFIGS["append"]
-    n = cfg.batch * cfg.prefill_chunk
+    n = cfg.batch * (tokens or cfg.prefill_chunk)
     g = torch.Generator(device="cuda")
     g.manual_seed(cfg.seed)
     sk = torch.from_numpy(W.channel_sigma(cfg, 0)).cuda()
@@ -257,7 +260,7 @@ def quantize_throughput(kvq, torch, reps=5):
     row, aux = kvq.kvq_row_bytes("codebook", 4, cfg.head_dim)
     nbytes = vectors * (2 * cfg.head_dim + row + aux) + 4 * n
     del k, v, cache
-    return {"workload": "append chunk: 4 x 16384 tokens x 16 kv heads x (K,V), D=256, 4-bit LM",
+    return {"workload": f"append chunk: 4 x {n // cfg.batch} tokens x 16 kv heads x (K,V), D=256, 4-bit LM",
             "vectors_per_s": vectors / t, "ms": t * 1e3, "gbps": nbytes / t / 1e9, "bytes": nbytes}
 
 
@@ -526,7 +529,7 @@ def run_ours(args):
         kvq.kvq_decode_attention(views, q_d, out_d, ws_d, 0, stream)  # the step's output, options off
         torch.cuda.synchronize()
         quality = output_error_vs_fp16(cfg, wl, q_host, out_d.cpu().numpy(), k_new, v_new, window)
-    quant = quantize_throughput(kvq, torch) if rank == 0 else None
+    quant = quantize_throughput(kvq, torch, tokens=args.quant_tokens) if rank == 0 else None
     barrier(ws)
     if rank != 0:
         return
