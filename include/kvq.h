@@ -215,7 +215,8 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
  * directly where the fp16 rounding of x~ crosses a decision boundary).  A token whose src
  * or dst slot is negative or out of range is skipped.  src is left unchanged.  A src
  * that is not fp16, or a dst whose keys are KVQ_FMT_CODEBOOK_OUTLIER (its channel split
- * needs the unrotated vector), returns KVQ_ERR_UNSUPPORTED. */
+ * needs the unrotated vector), returns KVQ_ERR_UNSUPPORTED; num_tokens x num_kv_heads above
+ * 2^28 returns KVQ_ERR_INVALID_ARGUMENT (split the move). */
 KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots,
                                   const kvq_cache* dst, const int32_t* dst_slots,
                                   int32_t num_tokens, void* stream);

@@ -315,6 +315,7 @@ KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots
   p.num_kinds = 2;
   p.num_vectors = 2LL * num_tokens * dst->num_kv_heads;
   if (p.num_slots == 0 || p.src_num_slots == 0) return KVQ_OK;
+  if ((long long)num_tokens * dst->num_kv_heads > (1LL << 28)) return KVQ_ERR_INVALID_ARGUMENT;
   cudaError_t e = launch_requantize(p, dst->head_dim, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

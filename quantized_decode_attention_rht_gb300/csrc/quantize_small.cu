@@ -175,14 +175,13 @@ __device__ __forceinline__ void store_fields(uint32_t* buf, uint32_t fields, uin
   if (lane < W / 4) reinterpret_cast<uint4*>(row)[lane] = reinterpret_cast<const uint4*>(buf)[lane];
 }
 
-// Residual sign sketch: z_j = [ (S r)_j >= 0 ], j < KVQ_QJL_DIM, as four 32-bit words.  The
-// lane's partial dot products of 32 rows at a time are reduce-scattered over the warp so
-// lane l ends with row 32k + l, and a ballot gathers the signs.
+// Residual sign sketch: word k of z_j = [ (S r)_j >= 0 ], rows j in [32k, 32k + 32).  The
+// lane's partial dot products of the 32 rows are reduce-scattered over the warp so lane l
+// ends with row 32k + l, and a ballot gathers the signs.  (A key's four words come from
+// four warps: a decode step's few hundred keys then spread over four times the warps.)
 template <int D, int E>
-__device__ __forceinline__ uint4 sketch_words(const float* __restrict__ proj, const float (&r)[E], int lane) {
-  uint32_t zw[KVQ_QJL_DIM / 32];
-#pragma unroll 1
-  for (int k = 0; k < KVQ_QJL_DIM / 32; ++k) {
+__device__ __forceinline__ uint32_t sketch_word(const float* __restrict__ proj, const float (&r)[E], int lane, int k) {
+  {
     float a[32];
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
@@ -209,9 +208,8 @@ __device__ __forceinline__ uint4 sketch_words(const float* __restrict__ proj, co
         a[q] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, msk);
       }
     }
-    zw[k] = __ballot_sync(0xFFFFFFFFu, a[0] >= 0.f);
+    return __ballot_sync(0xFFFFFFFFu, a[0] >= 0.f);
   }
-  return make_uint4(zw[0], zw[1], zw[2], zw[3]);
 }
 
 // FROM_ROWS: the vectors are stored fp16 rows of x~ (src, re-encode) rather than new fp16
@@ -232,8 +230,12 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
 #pragma unroll
     for (int i = 0; i < NB; ++i) bnd[i] = __ldg(side.bounds + i);
   }
-  const int nvec = p.num_tokens * p.hkv;
-  for (int v = blockIdx.x * kWarps + (threadIdx.x >> 5); v < nvec; v += gridDim.x * kWarps) {
+  // keys with a residual sketch: four work units per key, unit u computing sketch word u
+  // (each unit repeats the key's short encode; unit 0 stores the codes and norms)
+  constexpr int UNITS = FMT == F_CBQ ? KVQ_QJL_DIM / 32 : 1;
+  const int nunits = p.num_tokens * p.hkv * UNITS;
+  for (int u = blockIdx.x * kWarps + (threadIdx.x >> 5); u < nunits; u += gridDim.x * kWarps) {
+    const int v = u / UNITS, part = u - v * UNITS;
     const int token = v / p.hkv, h = v - token * p.hkv;
     const int slot = p.slots[token];
     if (slot < 0 || slot >= p.num_slots) continue;  // warp-uniform
@@ -269,7 +271,7 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
         idx[e] = c;
         fields |= (uint32_t)c << (e * BITS);
       }
-      store_fields<D, E, BITS>(buf, fields, row, lane);
+      if (part == 0) store_fields<D, E, BITS>(buf, fields, row, lane);  // warp-uniform
       if constexpr (FMT == F_CB) {
         if (lane == 0) side.aux[prow] = norm16;
       } else if constexpr (FMT == F_CBO) {
@@ -302,10 +304,10 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
           rs = fmaf(y[e], y[e], rs);
         }
         const float rn = sqrtf(warp_sum(rs));
-        const uint4 z = sketch_words<D, E>(side.qjl, y, lane);
+        const uint32_t z = sketch_word<D, E>(side.qjl, y, lane, part);
         if (lane == 0) {
-          *reinterpret_cast<uint4*>(row + D * BITS / 8) = z;
-          reinterpret_cast<__half2*>(side.aux)[prow] = __halves2half2(norm16, __float2half_rn(rn));
+          reinterpret_cast<uint32_t*>(row + D * BITS / 8)[part] = z;
+          if (part == 0) reinterpret_cast<__half2*>(side.aux)[prow] = __halves2half2(norm16, __float2half_rn(rn));
         }
       }
     } else if constexpr (FMT == F_F16) {
@@ -386,7 +388,8 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(const QuantParams p
 
 template <bool FROM_ROWS>
 cudaError_t launch_warp_kernel(const QuantParams& p, int head_dim, int sms, cudaStream_t stream) {
-  const long long nvec = (long long)p.num_tokens * p.hkv;
+  const bool sketch = p.side[0].fmt == KVQ_FMT_CODEBOOK_QJL && p.kind_first == 0;
+  const long long nvec = (long long)p.num_tokens * p.hkv * (sketch ? KVQ_QJL_DIM / 32 : 1);  // work units
   const unsigned blocks =
       (unsigned)std::max<long long>(1, std::min<long long>((nvec + kWarps - 1) / kWarps, (long long)sms * 8));
   const dim3 grid(blocks, p.num_kinds);
@@ -405,7 +408,7 @@ cudaError_t launch_quantize_small(const QuantParams& p, int head_dim, int sms, c
 
 cudaError_t launch_requantize(const QuantParams& p, int head_dim, cudaStream_t stream) {
   if (p.num_tokens == 0) return cudaSuccess;
-  if ((long long)p.num_tokens * p.hkv > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
+  if ((long long)p.num_tokens * p.hkv > (1LL << 28)) return cudaErrorInvalidValue;  // four units per sketched key fit an int
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

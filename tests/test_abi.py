@@ -212,6 +212,7 @@ def test_requantize_checks(kvq):
     assert rq(win, _fake_cache(kvq, k_bounds=None), n=0) == 1
     assert rq(win, dst, n=2, ss=None) == 1
     assert rq(win, dst, n=2, ds=(1 << 43) + 2) == 1
+    assert rq(win, dst, n=(1 << 28) // win.num_kv_heads + 1) == 1  # past 2^28 vectors: split the move
     assert rq(_fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_rows=(1 << 40) + 8), dst, n=0) == 1
 
 
