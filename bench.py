@@ -35,7 +35,7 @@ METRIC = "quantized-KV decode attention GB/s & frac of HBM peak; quantize vector
 # proportion to the batch) and is scaled by 32 / 4.  A changed source reports null.
 TRAFFIC = {
     "gqa32k": {"kernel": "decode_gqa_kernel", "source": "quantized_decode_attention_rht_gb300/csrc/decode_gqa.cu",
-               "sha256": "344f4bbb411b870a", "captured_batch": 4, "bytes": 242750464 + 16719104},
+               "sha256": "11b4d50901ffc752", "captured_batch": 4, "bytes": 242705408 + 15922176},
 }
 
 
@@ -83,52 +83,79 @@ def measured_peak():
 
 # ----------------------------------------------------------------------------- clocks
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_clock_samples(lines, t_begin=None, t_end=None):
+    """Median SM clock, max clock and active throttle reasons of the nvidia-smi samples whose
+    timestamp lies in [t_begin, t_end] (host wall-clock seconds; None: every sample)."""
+    sm, smax, reasons = [], [], set()
+    for line in lines:
+        p = [x.strip() for x in line.split(",")]
+        if len(p) < 10:
+            continue
+        try:
+            ts = time.mktime(time.strptime(p[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            ts += float("0." + p[0].split(".")[1]) if "." in p[0] else 0.0
+            mhz, max_mhz = float(p[2]), float(p[3])
+        except (ValueError, IndexError):
+            continue
+        if (t_begin is not None and ts < t_begin) or (t_end is not None and ts > t_end):
+            continue
+        sm.append(mhz)
+        smax.append(max_mhz)
+        for n, v in zip(REASON_NAMES, p[6:10]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    """nvidia-smi sampling (every 25 ms) of SM clocks and throttle reasons.  The sampler is
+    started, and its first sample awaited, before the timed region; only samples stamped
+    inside the region (host wall clock from the first launch to the final synchronize)
+    are reported."""
 
     def __init__(self, gpu_index: int):
         self.path = tempfile.mktemp(prefix="kvq_clocks_", suffix=".csv")
         self.proc = None
+        self.t_begin = self.t_end = None
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "25"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        deadline = time.time() + 10.0
+        while time.time() < deadline and self.proc.poll() is None and os.path.getsize(self.path) == 0:
+            time.sleep(0.02)
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)  # let the sampler write the line that covers the region's end
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                p = [x.strip() for x in line.split(",")]
-                if len(p) < 9:
-                    continue
-                try:
-                    sm.append(float(p[1]))
-                    smax.append(float(p[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, p[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+            out = parse_clock_samples(f.readlines(), self.t_begin, self.t_end)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return out
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -464,6 +491,8 @@ def run_ours(args):
     t1 = torch.cuda.Event(enable_timing=True)
     launches0 = kvq.kvq_kernel_launches()
     torch.cuda.nvtx.range_push("timed")  # lets a profiler select the timed launches
+    if clocks:
+        clocks.begin()
     t0.record(stream)
     for i in range(args.steps):
         move_oldest()
@@ -475,6 +504,8 @@ def run_ours(args):
     torch.cuda.nvtx.range_pop()
     launches = kvq.kvq_kernel_launches() - launches0
     torch.cuda.synchronize()
+    if clocks:
+        clocks.end()
     barrier(ws)
     clk = clocks.stop() if clocks else None
     total_s = max_over_ranks(t0.elapsed_time(t1) / 1e3, ws, dev)

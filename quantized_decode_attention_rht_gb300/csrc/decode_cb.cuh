@@ -43,8 +43,9 @@
 //    fragments follow that order; the value mma maps its A rows g and g+8 of m-tile mt to
 //    the two coordinates of pair slot g D/16 + mt, so one lookup gives both rows and the
 //    lane's output coordinates come out contiguous.  Value fragments pair two tokens per
-//    register, the table pairs two coordinates of one token: two byte permutes per
-//    register pair swap them.
+//    register, so the value lookups index the same pair table with the codes of two
+//    tokens at one coordinate: per page the lane merges the code runs of its token pairs
+//    (a shift and a bit select per word) and each entry is then a ready A register pair.
 // (Kernel templates shared by decode_cb.cu -- plain codebook keys -- and decode_cb_qjl.cu
 // -- keys with a residual sketch -- so the two instance sets compile in parallel.)
 #pragma once
@@ -255,6 +256,29 @@ __device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int o, u
   } else {
     const uint32_t x = __funnelshift_r(w[i], w[i + 1 < NW ? i + 1 : i], r - 8);
     return (x & mask) | lanebase;
+  }
+}
+
+// Code runs of two tokens a, b (NW words each, VB-bit codes, pair slots of 2 VB bits) merged
+// so that pair slot k of x holds (a's code, b's code) of the slot's first coordinate and
+// slot k of y those of its second: the pair field then indexes a table entry
+// (C[code of a], C[code of b]), i.e. two tokens at one coordinate.
+__host__ __device__ constexpr uint32_t first_code_mask(int vb, int word) {
+  uint32_t m = 0;
+  for (int n = 0; n < 32; ++n)
+    if ((32 * word + n) % (2 * vb) < vb) m |= 1u << n;
+  return m;
+}
+template <int VB, int NW>
+__device__ __forceinline__ void token_pairs(const uint32_t (&a)[NW], const uint32_t (&b)[NW], uint32_t (&x)[NW],
+                                            uint32_t (&y)[NW]) {
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    const uint32_t m = first_code_mask(VB, i);
+    const uint32_t bu = i > 0 ? __funnelshift_l(b[i - 1], b[i], VB) : (b[i] << VB);       // b one code up
+    const uint32_t ad = i + 1 < NW ? __funnelshift_r(a[i], a[i + 1], VB) : (a[i] >> VB);  // a one code down
+    x[i] = (a[i] & m) | (bu & ~m);
+    y[i] = (ad & m) | (b[i] & ~m);
   }
 }
 
@@ -626,10 +650,14 @@ struct Path1 {
       x0 = v0 ? x0 : -INFINITY;
       x1 = v1 ? x1 : -INFINITY;
       // ---- online softmax over the 16 tokens
+      // the page maximum matters only where a score rises above the running maximum (and
+      // for the gate): one vote settles the usual page, whose maximum is below it
       float mt = fmaxf(x0, x1);
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+      if (p.gate || __any_sync(kFull, mt > m)) {
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+      }
       if (mt > m) {
         const float f = exp2f(m - mt);  // m = -inf at first: f = 0
         l *= f;
@@ -885,10 +913,14 @@ struct PathM {
       x0 = v0 ? x0 : -INFINITY;
       x1 = v1 ? x1 : -INFINITY;
       // ---- online softmax of head c over the 16 tokens
+      // the page maximum matters only where a score rises above the running maximum (and
+      // for the gate): one vote settles the usual page, whose maximum is below it
       float mt = fmaxf(x0, x1);
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+      if (p.gate || __any_sync(kFull, mt > m)) {
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+      }
       if (mt > m) {
         const float f = exp2f(m - mt);  // m = -inf at first: f = 0
         l *= f;
@@ -920,17 +952,18 @@ struct PathM {
       const uint32_t A = lo_part ? al : ah, B = lo_part ? bl : bh;
       const uint32_t b0 = live_col ? __byte_perm(A, B, 0x5410) : 0u;
       const uint32_t b1 = live_col ? __byte_perm(A, B, 0x7632) : 0u;
-      // ---- values: m-tile mt covers pair slot g*QPT + mt of the four tokens
+      // ---- values: m-tile mt covers pair slot g*QPT + mt (rows g, g+8: its two
+      // coordinates) of tokens 2c, 2c+1 (columns of a0, a1) and 2c+8, 2c+9 (a2, a3)
+      uint32_t x01[VW], y01[VW], x89[VW], y89[VW];
+      token_pairs<VB, VW>(v[0], v[1], x01, y01);
+      token_pairs<VB, VW>(v[2], v[3], x89, y89);
 #pragma unroll
       for (int mt2 = 0; mt2 < KS; ++mt2) {
-        const uint2 r0 = lut64(field_addr<2 * VB>(v[0], 2 * VB * mt2, vlane));
-        const uint2 r1 = lut64(field_addr<2 * VB>(v[1], 2 * VB * mt2, vlane));
-        const uint2 r2 = lut64(field_addr<2 * VB>(v[2], 2 * VB * mt2, vlane));
-        const uint2 r3 = lut64(field_addr<2 * VB>(v[3], 2 * VB * mt2, vlane));
-        const uint32_t ah4[4] = {__byte_perm(r0.x, r1.x, 0x5410), __byte_perm(r0.x, r1.x, 0x7632),
-                                 __byte_perm(r2.x, r3.x, 0x5410), __byte_perm(r2.x, r3.x, 0x7632)};
-        const uint32_t al4[4] = {__byte_perm(r0.y, r1.y, 0x5410), __byte_perm(r0.y, r1.y, 0x7632),
-                                 __byte_perm(r2.y, r3.y, 0x5410), __byte_perm(r2.y, r3.y, 0x7632)};
+        const uint2 r0 = lut64(field_addr<2 * VB>(x01, 2 * VB * mt2, vlane));
+        const uint2 r1 = lut64(field_addr<2 * VB>(y01, 2 * VB * mt2, vlane));
+        const uint2 r2 = lut64(field_addr<2 * VB>(x89, 2 * VB * mt2, vlane));
+        const uint2 r3 = lut64(field_addr<2 * VB>(y89, 2 * VB * mt2, vlane));
+        const uint32_t ah4[4] = {r0.x, r1.x, r2.x, r3.x}, al4[4] = {r0.y, r1.y, r2.y, r3.y};
         mma16816(acc[mt2], ah4, b0, b1);
         mma16816(acc[mt2], al4, b0, b1);
       }

@@ -301,10 +301,12 @@ struct Far {
     const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
     x0 = v0 ? x0 : -INFINITY;
     x1 = v1 ? x1 : -INFINITY;
-    float mt = fmaxf(x0, x1);
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+    float mt = fmaxf(x0, x1);  // the page maximum: needed only above the running one (or for the gate)
+    if (gate || __any_sync(kFull, mt > s.m)) {
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+    }
     if (mt > s.m) {
       rescale(s, exp2f(s.m - mt));  // first tile: exp2(-inf) = 0
       s.m = mt;
@@ -484,10 +486,12 @@ struct Near {
     const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
     x0 = v0 ? x0 : -INFINITY;
     x1 = v1 ? x1 : -INFINITY;
-    float mt = fmaxf(x0, x1);
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+    float mt = fmaxf(x0, x1);  // the page maximum: needed only above the running one (or for the gate)
+    if (gate || __any_sync(kFull, mt > s.m)) {
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 4));
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+      mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+    }
     if (mt > s.m) {
       const float f = exp2f(s.m - mt);
       s.l *= f;

@@ -63,6 +63,8 @@ __device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
   return r;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr)); }
+
 // ---------------------------------------------------------------- decision table
 // The code index #{i : u > bounds[i]} through cells of width w (a power of two no larger
 // than the smallest gap between boundaries, so a cell holds at most one boundary).  With
@@ -409,6 +411,9 @@ __device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Ta
   const uint16_t* x = p.x[kind];
   for (int v = blockIdx.x * VPB + threadIdx.x / TPV; v < nvec; v += stride) {
     const int token = v / p.hkv, h = v - token * p.hkv;
+    // the thread's 128-byte line of its next vector heads for L2 while this one is worked on
+    // (the loads at the top of each vector otherwise wait a full HBM round trip)
+    if (v + stride < nvec) prefetch_l2(x + (size_t)(v + stride) * D + sub * kE);
     quantize_vector<TPV, kE, FMT, BITS>(p, side, table, x + (size_t)v * D + sub * kE, token, h, sub, gmask);
   }
 }
