@@ -46,6 +46,9 @@
 //    register, so the value lookups index the same pair table with the codes of two
 //    tokens at one coordinate: per page the lane merges the code runs of its token pairs
 //    (a shift and a bit select per word) and each entry is then a ready A register pair.
+//    With 2-bit values a byte of the merged run covers two m-tiles: where shared memory
+//    allows, a quad table (256 byte values x 16 lane copies x 16 bytes) gives both tiles'
+//    registers in one 16-byte lookup addressed by one byte permute.
 // (Kernel templates shared by decode_cb.cu -- plain codebook keys -- and decode_cb_qjl.cu
 // -- keys with a residual sketch -- so the two instance sets compile in parallel.)
 #pragma once
@@ -97,6 +100,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 }
 __device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ uint4 lut128(uint32_t a) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -217,6 +228,15 @@ struct CbParams {
 // outlier stream.
 constexpr int kModePlain = 0, kModeSketch = 1, kModeOutlier = 2;
 
+// Shared memory of a CTA: the table block (quad table if any, pair table, sketch table),
+// aligned to its first table's size, and one area per warp.  The alignment may leave up to
+// that size - 1 bytes before the block; warp areas fill that gap first, so the worst case
+// wastes under one area.
+constexpr int block_smem(int qtab, int table, int skt, int warps, int wsm) {
+  const int align = qtab ? qtab : table, blk = qtab + table + skt;
+  return blk + warps * wsm + wsm > align + blk ? blk + warps * wsm + wsm : align + blk;
+}
+
 template <int D, int G, int KB, int VB, int WARPS_, int MODE_>
 struct Layout {
   static constexpr bool QJL = MODE_ == kModeSketch, OUT = MODE_ == kModeOutlier;
@@ -232,10 +252,12 @@ struct Layout {
   static constexpr int QBUF = G * D * 4;
   static constexpr int QLINES = G * D * 2 / 128;  // fp16 query rows of the group, in lines
   static constexpr int WSM = STAGES * STAGE + QBUF + 16 * ((8 * STAGES + 15) / 16);
-  // the table's alignment may leave up to TABLE - 1 bytes before it; warp areas fill that gap
-  // first, so the worst case wastes under one area
-  static constexpr int SMEM =
-      (TABLE + SKT + WARPS * WSM + WSM > 2 * TABLE + SKT) ? TABLE + SKT + WARPS * WSM + WSM : 2 * TABLE + SKT;
+  // 2-bit values on the tensor-core path: a quad table indexed by a byte of two pair slots
+  // (256 entries x 16 lane copies x 16 bytes) before the pair table, where it fits
+  static constexpr int QTAB =
+      (G > 1 && VB == 2 && block_smem(65536, TABLE, SKT, WARPS, WSM) <= 227 * 1024) ? 65536 : 0;
+  static constexpr int ALIGN = QTAB ? QTAB : TABLE;  // the table block's alignment
+  static constexpr int SMEM = block_smem(QTAB, TABLE, SKT, WARPS, WSM);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
@@ -748,6 +770,16 @@ struct PathM {
       sts64(base + e * 256 + half * 128 + ln * 8, split_pair(c0, c1, 0.f), split_pair(c0, c1, 1.f));
     }
     if (QJL) build_sketch_table<false>(base + L::TABLE);
+    if constexpr (L::QTAB != 0) {  // entry e, lane copy l at base - QTAB + e*256 + l*16: the
+                                   // pair-table entries of e's low and high nibbles
+      for (int i = threadIdx.x; i < 256 * 16; i += blockDim.x) {
+        const int e = i >> 4, ln = i & 15;
+        const float c0 = __ldg(vc + (e & 3)) * kCScale, c1 = __ldg(vc + ((e >> 2) & 3)) * kCScale;
+        const float c2 = __ldg(vc + ((e >> 4) & 3)) * kCScale, c3 = __ldg(vc + (e >> 6)) * kCScale;
+        sts128(base - L::QTAB + e * 256 + ln * 16, split_pair(c0, c1, 0.f), split_pair(c0, c1, 1.f),
+               split_pair(c2, c3, 0.f), split_pair(c2, c3, 1.f));
+      }
+    }
   }
 
   __device__ static void run_item(const CbParams& p, const Item& it, bool has_next, const Item& nx, float* qbuf,
@@ -757,6 +789,9 @@ struct PathM {
     const int t1 = min(it.len, it.t0 + T.chunk);
     const int pg0 = it.t0 / PS, npg = item_pages(T, it);
     const int g = lane >> 2, c = lane & 3;
+    // quad-table lookup base: the table block starts QTAB below the pair table, which is
+    // aligned to its size; lane copy (l & 15) at 16-byte steps
+    const uint32_t qlane = pin(((vlane & ~(uint32_t)(L::TABLE - 1)) - L::QTAB) | ((lane & 15) << 4));
     Feeder<L> fd;
     fd.init(p, it, nx, npg, has_next ? item_pages(T, nx) : 0, rg, lane);
     fd.top_up(rg);
@@ -957,15 +992,33 @@ struct PathM {
       uint32_t x01[VW], y01[VW], x89[VW], y89[VW];
       token_pairs<VB, VW>(v[0], v[1], x01, y01);
       token_pairs<VB, VW>(v[2], v[3], x89, y89);
+      if constexpr (L::QTAB != 0) {
+        // 2-bit values: byte j of a merged run is pair slots 2j, 2j+1, and one quad-table
+        // entry holds the (hi, lo) registers of both m-tiles
 #pragma unroll
-      for (int mt2 = 0; mt2 < KS; ++mt2) {
-        const uint2 r0 = lut64(field_addr<2 * VB>(x01, 2 * VB * mt2, vlane));
-        const uint2 r1 = lut64(field_addr<2 * VB>(y01, 2 * VB * mt2, vlane));
-        const uint2 r2 = lut64(field_addr<2 * VB>(x89, 2 * VB * mt2, vlane));
-        const uint2 r3 = lut64(field_addr<2 * VB>(y89, 2 * VB * mt2, vlane));
-        const uint32_t ah4[4] = {r0.x, r1.x, r2.x, r3.x}, al4[4] = {r0.y, r1.y, r2.y, r3.y};
-        mma16816(acc[mt2], ah4, b0, b1);
-        mma16816(acc[mt2], al4, b0, b1);
+        for (int j = 0; j < KS / 2; ++j) {
+          const uint4 r0 = lut128(field_addr<8>(x01, 8 * j, qlane));
+          const uint4 r1 = lut128(field_addr<8>(y01, 8 * j, qlane));
+          const uint4 r2 = lut128(field_addr<8>(x89, 8 * j, qlane));
+          const uint4 r3 = lut128(field_addr<8>(y89, 8 * j, qlane));
+          const uint32_t ah0[4] = {r0.x, r1.x, r2.x, r3.x}, al0[4] = {r0.y, r1.y, r2.y, r3.y};
+          const uint32_t ah1[4] = {r0.z, r1.z, r2.z, r3.z}, al1[4] = {r0.w, r1.w, r2.w, r3.w};
+          mma16816(acc[2 * j], ah0, b0, b1);
+          mma16816(acc[2 * j], al0, b0, b1);
+          mma16816(acc[2 * j + 1], ah1, b0, b1);
+          mma16816(acc[2 * j + 1], al1, b0, b1);
+        }
+      } else {
+#pragma unroll
+        for (int mt2 = 0; mt2 < KS; ++mt2) {
+          const uint2 r0 = lut64(field_addr<2 * VB>(x01, 2 * VB * mt2, vlane));
+          const uint2 r1 = lut64(field_addr<2 * VB>(y01, 2 * VB * mt2, vlane));
+          const uint2 r2 = lut64(field_addr<2 * VB>(x89, 2 * VB * mt2, vlane));
+          const uint2 r3 = lut64(field_addr<2 * VB>(y89, 2 * VB * mt2, vlane));
+          const uint32_t ah4[4] = {r0.x, r1.x, r2.x, r3.x}, al4[4] = {r0.y, r1.y, r2.y, r3.y};
+          mma16816(acc[mt2], ah4, b0, b1);
+          mma16816(acc[mt2], al4, b0, b1);
+        }
       }
     }
     // ---- partial of head c: sum over the 8 lanes of the head, coordinates 2*QPT*g ..
@@ -996,8 +1049,9 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   // the table sits at a shared address that is a multiple of its size; warp areas fill the
   // space before it first, then follow it
   const uint32_t base = smem_addr(smem);
-  const uint32_t a_t = (base + L::TABLE - 1) & ~(uint32_t)(L::TABLE - 1);
-  const int nfit = min(L::WARPS, (int)((a_t - base) / L::WSM));
+  const uint32_t a_q = (base + L::ALIGN - 1) & ~(uint32_t)(L::ALIGN - 1);  // quad table (if any)
+  const uint32_t a_t = a_q + L::QTAB;                                       // pair table
+  const int nfit = min(L::WARPS, (int)((a_q - base) / L::WSM));
   const uint32_t a_w = a_t + L::TABLE + L::SKT;  // warp areas that do not fit before the tables
   const uint32_t end = nfit == L::WARPS ? a_w : a_w + (L::WARPS - nfit) * L::WSM;
   // A later split-K launch may start on SMs this grid leaves; whatever depends on this
