@@ -48,9 +48,9 @@ cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t str
   // kernel does not carry), take the warp-per-vector kernel
   const bool outl = p.side[0].fmt == KVQ_FMT_CODEBOOK_OUTLIER && p.kind_first == 0;
   if ((long long)p.num_tokens * p.hkv <= kSmallMaxVectors || outl) return launch_quantize_small(p, head_dim, sms, stream);
-  // kCoords coordinates per thread: 2 lanes per vector for head_dim 128, 4 for 256
-  return head_dim == 128 ? launch_tpv<2>(p, sms, stream)
-                         : (head_dim == 256 ? launch_tpv<4>(p, sms, stream) : cudaErrorInvalidValue);
+  // kCoords coordinates per thread: head_dim / kCoords lanes per vector
+  return head_dim == 128 ? launch_tpv<128 / kCoords>(p, sms, stream)
+                         : (head_dim == 256 ? launch_tpv<256 / kCoords>(p, sms, stream) : cudaErrorInvalidValue);
 }
 
 }  // namespace kvq

@@ -1,9 +1,9 @@
 // Quantise-and-append: fp16 K/V vectors -> rotated, encoded rows in the paged pool.
 //
-// Each thread holds 64 coordinates of one vector (D / 64 neighbouring lanes per vector).
+// Each thread holds kCoords = 32 coordinates of one vector (D / 32 neighbouring lanes per vector).
 // Steps per vector, as on the pages:
 //   1. multiply by the Rademacher signs (a flip of the fp16 sign bit), then the
-//      Walsh-Hadamard butterflies in registers with packed f32x2 adds, and log2(D / 64)
+//      Walsh-Hadamard butterflies in registers with packed f32x2 adds, and log2(D / 32)
 //      stages across lanes with shuffles (AdapTQ page, "The Math Fix"; VeloxQuant-MLX page,
 //      "Stage 1");
 //   2. codebook format: norm of the rotated vector, fp16 norm, u = sqrt(D) y / ||y||, the
@@ -29,7 +29,7 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCoords = 64;  // coordinates of one vector held by one thread
+constexpr int kCoords = 32;      // coordinates of one vector held by one thread
 constexpr int kMaxCells = 512;
 typedef unsigned long long u64;
 
@@ -170,14 +170,17 @@ __device__ __forceinline__ void encode_codebook(const Table& tb, float (&y)[E], 
     w[o1 / 32] += i1 * (1u << (o1 % 32));
     if ((o1 % 32) + BITS > 32) w[o1 / 32 + 1] += i1 >> (32 - (o1 % 32));
   }
-  if (store) {
+  if (store) {  // the lane's run is W words at a multiple of its own size (3 words: of 4 bytes)
     if (W % 4 == 0) {
 #pragma unroll
       for (int k = 0; k < W / 4; ++k)
         reinterpret_cast<uint4*>(row)[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-    } else {
+    } else if (W % 2 == 0) {
 #pragma unroll
       for (int k = 0; k < W / 2; ++k) reinterpret_cast<uint2*>(row)[k] = make_uint2(w[2 * k], w[2 * k + 1]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; ++k) reinterpret_cast<uint32_t*>(row)[k] = w[k];
     }
   }
 }
@@ -418,9 +421,15 @@ __device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Ta
   }
 }
 
+// Resident blocks per SM: 4 (64 registers a thread) where the format's path fits them
+// without spills, else 3 (85 registers: the residual sketch, INT4 groups).
+constexpr int blocks_per_sm(int f0, int f1) {
+  return (f0 == F_CBQ || f0 == F_I4 || f1 == F_CBQ || f1 == F_I4) ? 3 : 4;
+}
+
 // Side slot blockIdx.y: (F0, B0) for slot 0, (F1, B1) for slot 1; kind = kind_first + slot.
 template <int TPV, int F0, int B0, int F1, int B1>
-__global__ void __launch_bounds__(kThreads, 2) quantize_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kThreads, blocks_per_sm(F0, F1)) quantize_kernel(const QuantParams p) {
   __shared__ Table table;
   if (blockIdx.y == 0) quantize_side<TPV, F0, B0>(p, p.kind_first, table);
   else quantize_side<TPV, F1, B1>(p, p.kind_first + 1, table);
@@ -431,7 +440,8 @@ cudaError_t launch_q(const QuantParams& p, int sides, int sms, cudaStream_t stre
   constexpr int VPB = kThreads / TPV;
   const long long nvec = (long long)p.num_tokens * p.hkv;
   const long long need = (nvec + VPB - 1) / VPB;
-  const unsigned blocks = (unsigned)std::max<long long>(1, std::min<long long>(need, (long long)sms * 2 / sides));
+  const unsigned blocks =
+      (unsigned)std::max<long long>(1, std::min<long long>(need, (long long)sms * blocks_per_sm(F0, F1) / sides));
   quantize_kernel<TPV, F0, B0, F1, B1><<<dim3(blocks, sides), kThreads, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
