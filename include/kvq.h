@@ -119,7 +119,8 @@ typedef enum kvq_format {
  * Rademacher diagonal, int8 +1/-1 [num_kv_heads][head_dim]; every tier attended in one
  * decode call must use the same K signs and the same V signs. */
 typedef struct kvq_cache {
-  int32_t head_dim;     /* D: 128 or 256 */
+  int32_t head_dim;     /* D: 64, 128 or 256 (keys with a sketch or an outlier stream:
+                           128 or 256; other D return KVQ_ERR_UNSUPPORTED) */
   int32_t num_kv_heads; /* Hkv >= 1 */
   int32_t page_size;    /* tokens per page, 16 */
   int32_t num_pages;    /* pages in the pool */
@@ -244,7 +245,8 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
 /* Decode attention for one new query per sequence over all tiers (a split-K pass, then a
  * combine pass).  Each tier goes to the kernel family that fits its formats: fp16/fp16 and
  * fp8/INT4 tiers (D = 128, 1, 2 or 4 query heads per kv head) share one fused launch,
- * codebook tiers take one launch each, anything else the generic kernel:
+ * codebook tiers (D = 128 or 256, 1, 2 or 4 query heads per kv head) take one launch each,
+ * anything else (D = 64, 8 query heads per kv head, other format pairs) the generic kernel:
  *   out[b][h] = softmax_t( q[b][h] . K[t] / sqrt(D) ) V[t]
  * over every cached token t < seq_lens[b] of every tier of kv head h / (Hq / Hkv), where
  * K[t], V[t] are the dequantised cache rows with the rotation undone; keys stored as

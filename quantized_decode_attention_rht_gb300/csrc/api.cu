@@ -21,7 +21,10 @@ constexpr int kSms = 152;  // GB300; the plan only needs the order of magnitude
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 kvq_status side_bytes(int fmt, int bits, int d, size_t* row, size_t* aux) {
-  if (d != 128 && d != 256) return KVQ_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return KVQ_ERR_UNSUPPORTED;
+  // keys with a sketch or an outlier stream are attended by the codebook kernel only
+  // (head_dim 128 or 256)
+  if ((fmt == KVQ_FMT_CODEBOOK_QJL || fmt == KVQ_FMT_CODEBOOK_OUTLIER) && d == 64) return KVQ_ERR_UNSUPPORTED;
   switch (fmt) {
     case KVQ_FMT_CODEBOOK:
       if (bits < 2 || bits > 4) return KVQ_ERR_UNSUPPORTED;
@@ -70,7 +73,7 @@ kvq_status check_side(const kvq_cache* c, int fmt, int bits, const void* rows, c
 
 kvq_status check_cache(const kvq_cache* c) {
   if (!c) return KVQ_ERR_INVALID_ARGUMENT;
-  if (c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
   if (c->num_kv_heads < 1 || c->page_size < 1 || c->num_pages < 0) return KVQ_ERR_INVALID_ARGUMENT;
   if ((long long)c->num_pages * c->page_size > 0x7FFFFFFFLL) return KVQ_ERR_INVALID_ARGUMENT;
   return KVQ_OK;

@@ -65,7 +65,7 @@ struct Row<Codebook<BITS>, D, DPL> {
       if ((o % 32) + BITS > 32) v |= w[o / 32 + 1] << (32 - (o % 32));
       x[j] = lut[v & ((1u << BITS) - 1u)];
     }
-    constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
+    constexpr float inv_sqrt_d = inv_sqrt_dim(D);
     scale = __half2float(aux[rowid]) * inv_sqrt_d;
   }
 };
@@ -405,14 +405,20 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
 #pragma unroll 4
   for (int s = warp; s < n; s += kCombineWarps) {
     const float f = s_w[s];
-    const float4* src = reinterpret_cast<const float4*>(p.ws_acc + (base + s_part[s]) * D + lane * PER);
+    const float* src = p.ws_acc + (base + s_part[s]) * D + lane * PER;
+    if constexpr (PER % 4 == 0) {
 #pragma unroll
-    for (int k = 0; k < PER / 4; ++k) {
-      const float4 v = src[k];
-      acc[4 * k] = fmaf(v.x, f, acc[4 * k]);
-      acc[4 * k + 1] = fmaf(v.y, f, acc[4 * k + 1]);
-      acc[4 * k + 2] = fmaf(v.z, f, acc[4 * k + 2]);
-      acc[4 * k + 3] = fmaf(v.w, f, acc[4 * k + 3]);
+      for (int k = 0; k < PER / 4; ++k) {
+        const float4 v = reinterpret_cast<const float4*>(src)[k];
+        acc[4 * k] = fmaf(v.x, f, acc[4 * k]);
+        acc[4 * k + 1] = fmaf(v.y, f, acc[4 * k + 1]);
+        acc[4 * k + 2] = fmaf(v.z, f, acc[4 * k + 2]);
+        acc[4 * k + 3] = fmaf(v.w, f, acc[4 * k + 3]);
+      }
+    } else {  // D = 64: two coordinates per lane
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] = fmaf(v.x, f, acc[0]);
+      acc[1] = fmaf(v.y, f, acc[1]);
     }
   }
 #pragma unroll
@@ -452,17 +458,22 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
       acc[k] = (lane & mm) ? (o - acc[k]) : (acc[k] + o);
     }
   }
-  constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
+  constexpr float inv_sqrt_d = inv_sqrt_dim(D);
   const int8_t* sg = p.v_signs + hk * D + lane * PER;
-  float4* dst = reinterpret_cast<float4*>(p.out + ((size_t)b * p.hq + hq) * D + lane * PER);
+  float* dst = p.out + ((size_t)b * p.hq + hq) * D + lane * PER;
+  if constexpr (PER % 4 == 0) {
 #pragma unroll
-  for (int k = 0; k < PER / 4; ++k) {
-    float4 v;
-    v.x = (sg[4 * k] < 0 ? -acc[4 * k] : acc[4 * k]) * inv_sqrt_d;
-    v.y = (sg[4 * k + 1] < 0 ? -acc[4 * k + 1] : acc[4 * k + 1]) * inv_sqrt_d;
-    v.z = (sg[4 * k + 2] < 0 ? -acc[4 * k + 2] : acc[4 * k + 2]) * inv_sqrt_d;
-    v.w = (sg[4 * k + 3] < 0 ? -acc[4 * k + 3] : acc[4 * k + 3]) * inv_sqrt_d;
-    dst[k] = v;
+    for (int k = 0; k < PER / 4; ++k) {
+      float4 v;
+      v.x = (sg[4 * k] < 0 ? -acc[4 * k] : acc[4 * k]) * inv_sqrt_d;
+      v.y = (sg[4 * k + 1] < 0 ? -acc[4 * k + 1] : acc[4 * k + 1]) * inv_sqrt_d;
+      v.z = (sg[4 * k + 2] < 0 ? -acc[4 * k + 2] : acc[4 * k + 2]) * inv_sqrt_d;
+      v.w = (sg[4 * k + 3] < 0 ? -acc[4 * k + 3] : acc[4 * k + 3]) * inv_sqrt_d;
+      reinterpret_cast<float4*>(dst)[k] = v;
+    }
+  } else {
+    *reinterpret_cast<float2*>(dst) = make_float2((sg[0] < 0 ? -acc[0] : acc[0]) * inv_sqrt_d,
+                                                  (sg[1] < 0 ? -acc[1] : acc[1]) * inv_sqrt_d);
   }
 }
 
@@ -529,6 +540,7 @@ bool decode_supports(int k_fmt, int k_bits, int v_fmt, int v_bits) {
 }
 
 cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStream_t stream) {
+  if (head_dim == 64) return launch_decode_d<64>(p, group, stream);
   if (head_dim == 128) return launch_decode_d<128>(p, group, stream);
   if (head_dim == 256) return launch_decode_d<256>(p, group, stream);
   return cudaErrorNotSupported;
@@ -537,7 +549,7 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
 cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
   const int blocks = p.batch * p.hq;
   if (blocks == 0) return cudaSuccess;
-  if (head_dim != 128 && head_dim != 256) return cudaErrorNotSupported;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return cudaErrorNotSupported;
   // programmatic dependent launch: the grid may be set up while the split-K pass drains
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
@@ -549,8 +561,9 @@ cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
-                                        : cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
+  const cudaError_t e = head_dim == 64    ? cudaLaunchKernelEx(&cfg, combine_kernel<64>, p)
+                        : head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
+                                          : cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
   if (e == cudaSuccess) note_launch();
   return e == cudaSuccess ? cudaGetLastError() : e;
 }

@@ -10,6 +10,9 @@
 namespace kvq {
 
 constexpr int kGroup = KVQ_INT4_GROUP;
+// 1 / sqrt(D) and sqrt(D) of the head dims the kernels are built for (64, 128, 256)
+__host__ __device__ constexpr float inv_sqrt_dim(int d) { return d == 256 ? 0.0625f : (d == 128 ? 0.08838834764831845f : 0.125f); }
+__host__ __device__ constexpr float sqrt_dim(int d) { return d == 256 ? 16.0f : (d == 128 ? 11.313708498984760f : 8.0f); }
 
 // Count of kernel launches made by this library (kvq_kernel_launches); every launcher calls
 // note_launch() after a launch that the runtime accepted.

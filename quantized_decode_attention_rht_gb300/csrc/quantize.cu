@@ -49,8 +49,12 @@ cudaError_t launch_quantize(const QuantParams& p, int head_dim, cudaStream_t str
   const bool outl = p.side[0].fmt == KVQ_FMT_CODEBOOK_OUTLIER && p.kind_first == 0;
   if ((long long)p.num_tokens * p.hkv <= kSmallMaxVectors || outl) return launch_quantize_small(p, head_dim, sms, stream);
   // kCoords coordinates per thread: head_dim / kCoords lanes per vector
-  return head_dim == 128 ? launch_tpv<128 / kCoords>(p, sms, stream)
-                         : (head_dim == 256 ? launch_tpv<256 / kCoords>(p, sms, stream) : cudaErrorInvalidValue);
+  switch (head_dim) {
+    case 64: return launch_tpv<64 / kCoords>(p, sms, stream);
+    case 128: return launch_tpv<128 / kCoords>(p, sms, stream);
+    case 256: return launch_tpv<256 / kCoords>(p, sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace kvq

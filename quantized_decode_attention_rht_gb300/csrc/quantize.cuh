@@ -232,8 +232,8 @@ template <int TPV, int kE, int FMT, int BITS>
 __device__ __forceinline__ void quantize_vector(const QuantParams& p, const QuantSide& side, const Table& table,
                                                 const uint16_t* src, int token, int h, int sub, unsigned gmask) {
   constexpr int D = kE * TPV;
-  constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
-  constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
+  constexpr float inv_sqrt_d = inv_sqrt_dim(D);
+  constexpr float sqrt_d = sqrt_dim(D);
   const int slot = p.slots[token];
   const bool store = slot >= 0 && slot < p.num_slots;
 

@@ -1,7 +1,7 @@
 // Quantise-and-append for small appends (a decode step's new token of every sequence): one
-// warp per vector, D / 32 neighbouring coordinates per lane.
+// warp per vector, D / 32 neighbouring coordinates per lane (D = 64, 128 or 256).
 //
-// The per-thread kernel of quantize.cuh keeps 64 coordinates of a vector in one thread's
+// The per-thread kernel of quantize.cuh keeps 32 coordinates of a vector in one thread's
 // registers, which is what a prefill chunk of millions of vectors wants; a few hundred
 // vectors then occupy a handful of SMs whose warps wait on one long, cold instruction
 // stream (and, for keys with a residual sketch, on 16 K multiply-adds per thread).  Here a
@@ -27,8 +27,11 @@ __device__ __forceinline__ float warp_sum(float x) {
 // y = H (s * x) (unnormalised) for the lane's coordinates [lane * E, lane * E + E).
 template <int E>
 __device__ __forceinline__ void load_rotate(const uint16_t* src, const int8_t* sg, int lane, float (&y)[E]) {
-  uint32_t xw[E / 2], sw[E / 4];
-  if constexpr (E == 4) {
+  uint32_t xw[E / 2], sw[(E + 3) / 4];
+  if constexpr (E == 2) {
+    xw[0] = __ldg(reinterpret_cast<const uint32_t*>(src) + lane);
+    sw[0] = __ldg(reinterpret_cast<const uint16_t*>(sg) + lane);
+  } else if constexpr (E == 4) {
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(src) + lane);
     xw[0] = u.x;
     xw[1] = u.y;
@@ -78,7 +81,9 @@ template <int E>
 __device__ __forceinline__ void load_split_rotate(const uint16_t* src, const int8_t* sg, const int32_t* outl, int lane,
                                                   float (&y)[E], float (&xo)[KVQ_OUTLIER_CHANNELS]) {
   uint32_t xw[E / 2];
-  if constexpr (E == 4) {
+  if constexpr (E == 2) {
+    xw[0] = __ldg(reinterpret_cast<const uint32_t*>(src) + lane);
+  } else if constexpr (E == 4) {
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(src) + lane);
     xw[0] = u.x;
     xw[1] = u.y;
@@ -109,8 +114,10 @@ __device__ __forceinline__ void load_split_rotate(const uint16_t* src, const int
     }
     xo[j] = __shfl_sync(0xFFFFFFFFu, mine, (ch[j] / E) & 31);
   }
-  int8_t s8[E];
-  if constexpr (E == 4) {
+  alignas(8) int8_t s8[E < 4 ? 4 : E];
+  if constexpr (E == 2) {
+    *reinterpret_cast<uint16_t*>(s8) = __ldg(reinterpret_cast<const uint16_t*>(sg) + lane);
+  } else if constexpr (E == 4) {
     *reinterpret_cast<uint32_t*>(s8) = __ldg(reinterpret_cast<const uint32_t*>(sg) + lane);
   } else {
     *reinterpret_cast<uint2*>(s8) = __ldg(reinterpret_cast<const uint2*>(sg) + lane);
@@ -140,7 +147,9 @@ __device__ __forceinline__ void load_split_rotate(const uint16_t* src, const int
 template <int E>
 __device__ __forceinline__ void load_row(const uint8_t* row, int lane, float (&y)[E]) {
   uint32_t xw[E / 2];
-  if constexpr (E == 4) {
+  if constexpr (E == 2) {
+    xw[0] = *reinterpret_cast<const uint32_t*>(row + 4 * lane);
+  } else if constexpr (E == 4) {
     const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * lane);
     xw[0] = u.x;
     xw[1] = u.y;
@@ -171,8 +180,12 @@ __device__ __forceinline__ void store_fields(uint32_t* buf, uint32_t fields, uin
   atomicOr(buf + w0, fields << sh);
   if (sh + E * BITS > 32) atomicOr(buf + w0 + 1, fields >> (32 - sh));
   __syncwarp();
-  static_assert(W % 4 == 0, "rows are whole 16-byte units");
-  if (lane < W / 4) reinterpret_cast<uint4*>(row)[lane] = reinterpret_cast<const uint4*>(buf)[lane];
+  if constexpr (W % 4 == 0) {
+    if (lane < W / 4) reinterpret_cast<uint4*>(row)[lane] = reinterpret_cast<const uint4*>(buf)[lane];
+  } else {  // 3-bit rows at D = 64: 24 bytes, 8-byte aligned
+    static_assert(W % 2 == 0, "rows are whole 8-byte units");
+    if (lane < W / 2) reinterpret_cast<uint2*>(row)[lane] = reinterpret_cast<const uint2*>(buf)[lane];
+  }
 }
 
 // Residual sign sketch: word k of z_j = [ (S r)_j >= 0 ], rows j in [32k, 32k + 32).  The
@@ -187,13 +200,18 @@ __device__ __forceinline__ uint32_t sketch_word(const float* __restrict__ proj, 
     for (int t = 0; t < 32; ++t) {
       const float4* srow = reinterpret_cast<const float4*>(proj + (size_t)(32 * k + t) * D + lane * E);
       float s = 0.f;
+      if constexpr (E == 2) {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(srow));
+        s = fmaf(v.y, r[1], v.x * r[0]);
+      } else {
 #pragma unroll
-      for (int q = 0; q < E / 4; ++q) {
-        const float4 v = __ldg(srow + q);
-        s = fmaf(v.x, r[4 * q], s);
-        s = fmaf(v.y, r[4 * q + 1], s);
-        s = fmaf(v.z, r[4 * q + 2], s);
-        s = fmaf(v.w, r[4 * q + 3], s);
+        for (int q = 0; q < E / 4; ++q) {
+          const float4 v = __ldg(srow + q);
+          s = fmaf(v.x, r[4 * q], s);
+          s = fmaf(v.y, r[4 * q + 1], s);
+          s = fmaf(v.z, r[4 * q + 2], s);
+          s = fmaf(v.w, r[4 * q + 3], s);
+        }
       }
       a[t] = s;
     }
@@ -219,8 +237,8 @@ template <int D, int FMT, int BITS, bool FROM_ROWS>
 __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSide& side, const uint16_t* x,
                                             const uint8_t* src, uint32_t* buf) {
   constexpr int E = D / 32;
-  constexpr float inv_sqrt_d = (D == 256) ? 0.0625f : 0.08838834764831845f;
-  constexpr float sqrt_d = (D == 256) ? 16.0f : 11.313708498984760f;
+  constexpr float inv_sqrt_d = inv_sqrt_dim(D);
+  constexpr float sqrt_d = sqrt_dim(D);
   constexpr float ys = FROM_ROWS ? 1.0f : inv_sqrt_d;
   constexpr bool CB = FMT == F_CB || FMT == F_CBQ || FMT == F_CBO;
   constexpr int NB = CB ? (1 << BITS) - 1 : 1;
@@ -317,17 +335,22 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
         const __half2 h2 = __floats2half2_rn(y[2 * k] * ys, y[2 * k + 1] * ys);
         w[k] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      if constexpr (E == 4) reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
+      if constexpr (E == 2) reinterpret_cast<uint32_t*>(row)[lane] = w[0];
+      else if constexpr (E == 4) reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
       else reinterpret_cast<uint4*>(row)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
     } else if constexpr (FMT == F_F8) {
-      uint32_t w[E / 4];
+      if constexpr (E == 2) {
+        reinterpret_cast<uint16_t*>(row)[lane] = (uint16_t)float2_to_fp8x2(y[0] * ys, y[1] * ys);
+      } else {
+        uint32_t w[E / 4];
 #pragma unroll
-      for (int k = 0; k < E / 4; ++k) {
-        const int e = 4 * k;
-        w[k] = float2_to_fp8x2(y[e] * ys, y[e + 1] * ys) | (float2_to_fp8x2(y[e + 2] * ys, y[e + 3] * ys) << 16);
+        for (int k = 0; k < E / 4; ++k) {
+          const int e = 4 * k;
+          w[k] = float2_to_fp8x2(y[e] * ys, y[e + 1] * ys) | (float2_to_fp8x2(y[e + 2] * ys, y[e + 3] * ys) << 16);
+        }
+        if constexpr (E == 4) reinterpret_cast<uint32_t*>(row)[lane] = w[0];
+        else reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
       }
-      if constexpr (E == 4) reinterpret_cast<uint32_t*>(row)[lane] = w[0];
-      else reinterpret_cast<uint2*>(row)[lane] = make_uint2(w[0], w[1]);
     } else {  // F_I4: a group of 32 coordinates spans 32 / E neighbouring lanes
       constexpr int LG = kGroup / E;
       float amax = 0.0f;
@@ -349,7 +372,8 @@ __device__ __forceinline__ void append_side(const QuantParams& p, const QuantSid
         const float q = s > 0.0f ? fminf(fmaxf(rintf(tq), -7.0f), 7.0f) : 0.0f;
         nib |= (uint32_t)((int)q + 8) << (4 * e);
       }
-      if constexpr (E == 4) reinterpret_cast<uint16_t*>(row)[lane] = (uint16_t)nib;
+      if constexpr (E == 2) row[lane] = (uint8_t)nib;
+      else if constexpr (E == 4) reinterpret_cast<uint16_t*>(row)[lane] = (uint16_t)nib;
       else reinterpret_cast<uint32_t*>(row)[lane] = nib;
       if (lane % LG == 0) side.aux[prow * (D / kGroup) + lane / LG] = s16;
     }
@@ -393,7 +417,8 @@ cudaError_t launch_warp_kernel(const QuantParams& p, int head_dim, int sms, cuda
   const unsigned blocks =
       (unsigned)std::max<long long>(1, std::min<long long>((nvec + kWarps - 1) / kWarps, (long long)sms * 8));
   const dim3 grid(blocks, p.num_kinds);
-  if (head_dim == 128) append_kernel<128, FROM_ROWS><<<grid, kWarps * 32, 0, stream>>>(p);
+  if (head_dim == 64) append_kernel<64, FROM_ROWS><<<grid, kWarps * 32, 0, stream>>>(p);
+  else if (head_dim == 128) append_kernel<128, FROM_ROWS><<<grid, kWarps * 32, 0, stream>>>(p);
   else append_kernel<256, FROM_ROWS><<<grid, kWarps * 32, 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();

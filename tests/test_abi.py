@@ -52,15 +52,20 @@ def test_status_strings(kvq):
     assert kvq.kvq_status_string(99) == "KVQ_ERR_UNKNOWN"
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_row_bytes_match_oracle(kvq, d):
     for fmt in ("codebook", "codebook_qjl", "codebook_outlier", "fp16", "fp8_e4m3", "int4_g32"):
         for bits in ((2, 3, 4) if fmt.startswith("codebook") else (0,)):
+            if d == 64 and fmt in ("codebook_qjl", "codebook_outlier"):  # codebook kernel only: D 128, 256
+                with pytest.raises(kvq.KvqError):
+                    kvq.kvq_row_bytes(fmt, bits, d)
+                continue
             assert kvq.kvq_row_bytes(fmt, bits, d) == (ofmt.row_bytes(fmt, bits, d), ofmt.aux_bytes(fmt, d))
     with pytest.raises(kvq.KvqError):
         kvq.kvq_row_bytes("codebook", 5, d)
-    with pytest.raises(kvq.KvqError):
-        kvq.kvq_row_bytes("fp16", 0, 64)
+    for bad in (32, 96, 512):
+        with pytest.raises(kvq.KvqError):
+            kvq.kvq_row_bytes("fp16", 0, bad)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4])
@@ -106,7 +111,8 @@ def _quant(kvq, cache, k=1 << 41, v=1 << 41, n=3, slots=1 << 42):
 def test_quantize_argument_checks(kvq):
     L = kvq.lib()
     assert L.kvq_quantize_append(None, 1 << 41, None, 3, 1 << 42, None) == 1
-    assert _quant(kvq, _fake_cache(kvq, head_dim=64)) == 2
+    assert _quant(kvq, _fake_cache(kvq, head_dim=96)) == 2
+    assert _quant(kvq, _fake_cache(kvq, head_dim=512)) == 2
     assert _quant(kvq, _fake_cache(kvq, k_bits=5)) == 2
     assert _quant(kvq, _fake_cache(kvq, k_format=7)) == 1
     assert _quant(kvq, _fake_cache(kvq, k_rows=None)) == 1
@@ -140,6 +146,9 @@ def _ws(kvq, caches, batch=2, hq=4, split=0, max_pages=8):
 def test_decode_argument_checks(kvq):
     c = _fake_cache(kvq)
     assert _ws(kvq, [c])[0] == 0
+    for hq in (2, 4, 8, 16):  # head_dim 64: the generic kernel, every group size
+        assert _ws(kvq, [_fake_cache(kvq, head_dim=64)], hq=hq)[0] == 0
+    assert _ws(kvq, [_fake_cache(kvq, head_dim=96)])[0] == 2
     assert _ws(kvq, [c], hq=6)[0] == 2  # Hq/Hkv = 3 is not built
     assert _ws(kvq, [c], hq=3)[0] == 1  # Hq not a multiple of Hkv
     assert _ws(kvq, [c] * 5)[0] == 1  # more tiers than KVQ_MAX_TIERS
@@ -184,6 +193,7 @@ def test_qjl_key_checks(kvq):
     assert _ws(kvq, [_qjl_cache(kvq)])[0] == 0
     assert _ws(kvq, [_qjl_cache(kvq)], hq=4 * 2)[0] == 0  # 4 query heads per kv head
     assert _ws(kvq, [_qjl_cache(kvq, head_dim=256)])[0] == 2  # the sketched decode is built for D=128
+    assert _quant(kvq, _qjl_cache(kvq, head_dim=64)) == 2 and _ws(kvq, [_qjl_cache(kvq, head_dim=64)])[0] == 2
     assert _ws(kvq, [_qjl_cache(kvq, v_format=kvq.FMT_FP16, v_bits=0)])[0] == 2
     assert _ws(kvq, [_qjl_cache(kvq), _fake_cache(kvq)])[0] == 0  # with a plain codebook tier
     # a tier of another kernel family runs on its own kernel in the same call

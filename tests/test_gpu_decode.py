@@ -70,7 +70,8 @@ def test_decode_edge_lengths_and_groups(group):
 
 
 CODE_WIDTHS = [(128, 1, 3, 3), (128, 4, 3, 3), (128, 2, 2, 4), (128, 1, 4, 2), (128, 4, 2, 3),
-               (256, 1, 3, 3), (256, 4, 4, 4), (256, 2, 2, 3), (256, 4, 3, 2), (256, 1, 2, 2)]
+               (256, 1, 3, 3), (256, 4, 4, 4), (256, 2, 2, 3), (256, 4, 3, 2), (256, 1, 2, 2),
+               (64, 1, 4, 4), (64, 2, 3, 3), (64, 4, 3, 2), (64, 8, 2, 4)]  # D = 64: the generic kernel
 
 
 @pytest.mark.gpu
@@ -123,6 +124,19 @@ def test_decode_qjl_near_tier_with_codebook_far_tier():
                                              W.Tier("codebook", "codebook", k_bits=2, v_bits=2)))
     lens = [5, 400, 1111]
     got, want, _, _ = run_exact(cfg, lens, split_tokens=64, shuffle=2)
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_decode_head_dim_64_two_tier(group):
+    """head_dim 64 (the generic kernel): fp16 near tier + fp8 keys / INT4 values far tier,
+    every group size, lengths spanning empty, sub-page and multi-chunk."""
+    hkv = 2
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=5, num_q_heads=hkv * group, num_kv_heads=hkv, head_dim=64)
+    lens = [0, 3, 16, 333, 1500]
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=64, shuffle=4)
+    assert np.all(got[0] == 0)
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
 
 

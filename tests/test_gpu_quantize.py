@@ -56,7 +56,7 @@ SIZES = [203, 5600]
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("n", SIZES)
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("fmt,bits", FORMATS)
 def test_quantize_matches_oracle(fmt, bits, d, n):
     torch = gu.torch_cuda()

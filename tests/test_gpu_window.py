@@ -28,9 +28,11 @@ def inputs(n, hkv, d, seed):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("kf,kb,vf,vb", DEST)
 def test_requantize_matches_oracle(kf, kb, vf, vb, d):
+    if kf == "codebook_qjl" and d == 64:
+        pytest.skip("keys with a sketch need head_dim 128 or 256")
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
     hkv, n, ps = 3, 150, 16
