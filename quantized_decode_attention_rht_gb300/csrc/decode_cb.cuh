@@ -259,6 +259,28 @@ struct Layout {
   static constexpr int ALIGN = QTAB ? QTAB : TABLE;  // the table block's alignment
   static constexpr int SMEM = block_smem(QTAB, TABLE, SKT, WARPS, WSM);
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
+
+  // Where things go for a dynamic shared-memory window starting at `base`: the table block
+  // at a multiple of its alignment (quad table at q, pair table at t), the first `nfit`
+  // warp areas in the gap before it, the rest from w on; `end` is one past the last byte.
+  struct Placement {
+    uint32_t q, t, w, end;
+    int nfit;
+  };
+  __host__ __device__ static Placement place(uint32_t base) {
+    Placement pl;
+    pl.q = (base + ALIGN - 1) & ~(uint32_t)(ALIGN - 1);
+    pl.t = pl.q + QTAB;
+    const int gap = (int)((pl.q - base) / WSM);
+    pl.nfit = gap < WARPS ? gap : WARPS;
+    pl.w = pl.t + TABLE + SKT;
+    pl.end = pl.nfit == WARPS ? pl.w : pl.w + (WARPS - pl.nfit) * WSM;
+    return pl;
+  }
+  // Shared address of warp area `warp`.
+  __host__ __device__ static uint32_t area(const Placement& pl, uint32_t base, int warp) {
+    return warp < pl.nfit ? base + warp * WSM : pl.w + (warp - pl.nfit) * WSM;
+  }
 };
 
 // ---------------------------------------------------------------- bit fields
@@ -1049,11 +1071,8 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   // the table sits at a shared address that is a multiple of its size; warp areas fill the
   // space before it first, then follow it
   const uint32_t base = smem_addr(smem);
-  const uint32_t a_q = (base + L::ALIGN - 1) & ~(uint32_t)(L::ALIGN - 1);  // quad table (if any)
-  const uint32_t a_t = a_q + L::QTAB;                                       // pair table
-  const int nfit = min(L::WARPS, (int)((a_q - base) / L::WSM));
-  const uint32_t a_w = a_t + L::TABLE + L::SKT;  // warp areas that do not fit before the tables
-  const uint32_t end = nfit == L::WARPS ? a_w : a_w + (L::WARPS - nfit) * L::WSM;
+  const typename L::Placement pl = L::place(base);
+  const uint32_t a_t = pl.t, end = pl.end;  // pair table (the quad table, if any, just before it)
   // A later split-K launch may start on SMs this grid leaves; whatever depends on this
   // grid's completion also sees the launch before it (the wait at the end).
   if (p.trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1062,7 +1081,7 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t area = warp < nfit ? base + warp * L::WSM : a_w + (warp - nfit) * L::WSM;
+  const uint32_t area = L::area(pl, base, warp);
   Ring rg;
   rg.slots = area;
   rg.bars = area + L::STAGES * L::STAGE + L::QBUF;
