@@ -119,8 +119,9 @@ typedef enum kvq_format {
  * Rademacher diagonal, int8 +1/-1 [num_kv_heads][head_dim]; every tier attended in one
  * decode call must use the same K signs and the same V signs. */
 typedef struct kvq_cache {
-  int32_t head_dim;     /* D: 64, 128 or 256 (keys with a sketch or an outlier stream:
-                           128 or 256; other D return KVQ_ERR_UNSUPPORTED) */
+  int32_t head_dim;     /* D: 64, 128 or 256; keys with an outlier stream 128 or 256, keys
+                           with a sketch are appended at 128 or 256 and decoded at 128;
+                           anything else returns KVQ_ERR_UNSUPPORTED */
   int32_t num_kv_heads; /* Hkv >= 1 */
   int32_t page_size;    /* tokens per page, 16 */
   int32_t num_pages;    /* pages in the pool */
