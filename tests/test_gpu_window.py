@@ -130,3 +130,36 @@ def test_window_tier_decode(name):
     want = oatt.decode_attention(q, built.ora)
     assert np.all(got[0] == 0)
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
+@pytest.mark.gpu
+def test_fp8_encode_every_fp16_pattern():
+    """The fp8 E4M3 encode (round to nearest even, saturating at +-448) on every one of the
+    65,536 fp16 bit patterns, bit-exact against the oracle: the patterns are stored as the
+    rows of an fp16 window tier and moved into an fp8-key tier with kvq_requantize, whose
+    re-encode converts the stored value itself (no rotation in between).  NaN inputs must
+    give a NaN code (0x7F or 0xFF, either sign)."""
+    from oracle import formats as ofmt
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_module()
+    d, hkv, ps = 128, 1, 16
+    n = 65536 // d
+    pages = n // ps
+    pat = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ones = np.ones((hkv, d), dtype=np.int8)
+    signs = torch.from_numpy(ones).cuda()
+    win = kvq.PagedCache(d, hkv, pages, "fp16", "fp16", 0, 0, signs, signs, ps)
+    win.k_rows.copy_(torch.from_numpy(pat.view(np.uint8).reshape(pages, hkv, ps, 2 * d)))
+    win.v_rows.zero_()
+    dst = kvq.PagedCache(d, hkv, pages, "fp8_e4m3", "fp16", 0, 0, signs, signs, ps)
+    slots = torch.arange(n, dtype=torch.int32, device="cuda")
+    kvq.kvq_requantize(win.struct, slots, dst.struct, slots)
+    torch.cuda.synchronize()
+    got = dst.k_rows.cpu().numpy().reshape(-1)
+    vals = pat.view(np.float16).astype(np.float32)
+    with np.errstate(invalid="ignore"):  # NaN patterns
+        want = ofmt.e4m3_encode(vals)
+    nan = np.isnan(vals)
+    assert np.array_equal(got[~nan], want[~nan]), int(np.sum(got[~nan] != want[~nan]))
+    assert np.all((got[nan] & 0x7F) == 0x7F)
+    assert got[np.flatnonzero(vals == np.inf)[0]] == 0x7E and got[np.flatnonzero(vals == -np.inf)[0]] == 0xFE
