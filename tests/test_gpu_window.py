@@ -156,8 +156,8 @@ def test_fp8_encode_every_fp16_pattern():
     kvq.kvq_requantize(win.struct, slots, dst.struct, slots)
     torch.cuda.synchronize()
     got = dst.k_rows.cpu().numpy().reshape(-1)
-    vals = pat.view(np.float16).astype(np.float32)
     with np.errstate(invalid="ignore"):  # NaN patterns
+        vals = pat.view(np.float16).astype(np.float32)
         want = ofmt.e4m3_encode(vals)
     nan = np.isnan(vals)
     assert np.array_equal(got[~nan], want[~nan]), int(np.sum(got[~nan] != want[~nan]))
