@@ -64,6 +64,12 @@ void groups() {
   keys<D, 4, MODE, false>();
 }
 
+// A planted mistake: a layout whose launch window is 4 KB short must be reported.
+template <class L>
+struct Shrunk : L {
+  static constexpr int SMEM = L::SMEM - 4096;
+};
+
 int main() {
   // the instances the library launches: plain codes (D 128, 256; the 16-warp tensor-core
   // variant at D 128), keys with a residual sketch (D 128), keys with an outlier stream
@@ -74,6 +80,11 @@ int main() {
   groups<128, kModeSketch>();
   groups<128, kModeOutlier>();
   groups<256, kModeOutlier>();
+  const int real = failures;
+  check<Shrunk<PathM<128, 4, 3, 2, kModePlain, true>::L>>("planted", 128, 4, 3, 2, kModePlain, 1);
+  const bool caught = failures == real + 1;
+  failures = real;
+  printf("planted mistake %s\n", caught ? "caught" : "MISSED");
   printf("%d failures\n", failures);
-  return failures ? 1 : 0;
+  return (failures || !caught) ? 1 : 0;
 }

@@ -26,6 +26,7 @@ def test_codebook_kernel_shared_memory_placement(tmp_path):
     assert r.returncode == 0, r.stdout[-3000:]
     lines = r.stdout.splitlines()
     assert lines[-1] == "0 failures"
+    assert "planted mistake caught" in lines  # the checker does reject a window that is too small
     assert sum(l.startswith("ok ") for l in lines) == 9 * (3 * 2 + 2 + 3 + 3 * 2)
     # the quad table (2-bit values on the tensor-core path) is placed where it fits
     assert any(" quad 65536 " in l and "V2" in l and "PathM" in l for l in lines)
