@@ -9,6 +9,7 @@ module both sides use is ``workloads`` (seeded inputs, no method arithmetic).
 Everything here is plain numpy in float64 and follows the pages step by step,
 in their order and notation, so that it can be checked against them by eye:
 
+  signs.py      the Rademacher sign vectors (SplitMix64, one draw per sign)
   rotation.py   random signs + Sylvester Walsh-Hadamard, orthonormal scaling
   codebook.py   Lloyd-Max for N(0,1) by trapezoidal quadrature; uniform codebook
   formats.py    fp16 / fp8-E4M3 rounding, INT4 with per-32-group scale, bit packing
@@ -24,4 +25,4 @@ Every function is pinned by ``tests/test_oracle_*.py`` to facts that do not
 come from the oracle itself (closed forms, library routines, the pages' worked
 examples, brute force on tiny inputs).  No function here is "parity unpinned".
 """
-from . import rotation, codebook, formats, cache, attention  # noqa: F401
+from . import signs, rotation, codebook, formats, cache, attention  # noqa: F401
