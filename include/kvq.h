@@ -181,6 +181,21 @@ KVQ_API kvq_status kvq_lloyd_max_codebook(int32_t bits, double* centroids, doubl
  * minimises the N(0,1) mean squared error; boundaries at midpoints.  Host outputs. */
 KVQ_API kvq_status kvq_uniform_codebook(int32_t bits, double* centroids, double* bounds);
 
+/* Rademacher sign vectors of the rotation for one layer (VeloxQuant-MLX page, "Stage 1:
+ * Random Rotation": the random +1/-1 diagonal applied before the Walsh-Hadamard transform;
+ * AdapTQ page, "The Math Fix": the random sign flip).  Host outputs k_signs and v_signs,
+ * int8 [num_kv_heads][head_dim] each, ready to upload as kvq_cache.k_signs / v_signs.
+ * Sign j of kv head h on side s (0 keys, 1 values) is +1 if the lowest bit of the first
+ * output of a SplitMix64 generator whose state starts at
+ *     seed XOR (layer * 2^40 + s * 2^32 + h * 2^16 + j)
+ * is 0, else -1 (SplitMix64: state += 0x9E3779B97F4A7C15; z = state; z = (z ^ z >> 30) *
+ * 0xBF58476D1CE4E5B9; z = (z ^ z >> 27) * 0x94D049BB133111EB; output z ^ z >> 31).  The
+ * same (seed, layer) always gives the same signs.  0 <= layer < 2^24, 1 <= num_kv_heads <=
+ * 2^16 (else KVQ_ERR_INVALID_ARGUMENT); head_dim 64, 128 or 256 (else
+ * KVQ_ERR_UNSUPPORTED); null outputs: KVQ_ERR_INVALID_ARGUMENT. */
+KVQ_API kvq_status kvq_make_signs(uint64_t seed, int32_t layer, int32_t num_kv_heads, int32_t head_dim,
+                                  int8_t* k_signs, int8_t* v_signs);
+
 /* float32 tables for the device: centroids32[i] = (float)centroids[i] and bounds32[i] =
  * (float)(((double)centroids32[i] + centroids32[i+1]) / 2).  All host arrays. */
 KVQ_API kvq_status kvq_codebook_tables(int32_t bits, const double* centroids,

@@ -93,6 +93,7 @@ def lib() -> ctypes.CDLL:
             "kvq_lloyd_max_codebook": [i32, dp, dp],
             "kvq_uniform_codebook": [i32, dp, dp],
             "kvq_codebook_tables": [i32, dp, fp, fp],
+            "kvq_make_signs": [ctypes.c_uint64, i32, i32, i32, vp, vp],
             "kvq_quantize_append": [ctypes.POINTER(KvqCache), vp, vp, i32, vp, vp],
             "kvq_requantize": [ctypes.POINTER(KvqCache), vp, ctypes.POINTER(KvqCache), vp, i32, vp],
             "kvq_outlier_calibrate": [vp, i32, i32, i32, vp, vp],
@@ -179,6 +180,16 @@ def kvq_codebook_tables(bits: int, centroids: np.ndarray):
                                      c32.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
                                      b32.ctypes.data_as(ctypes.POINTER(ctypes.c_float))), "kvq_codebook_tables")
     return c32, b32
+
+
+def kvq_make_signs(seed: int, layer: int, num_kv_heads: int, head_dim: int):
+    """int8 [num_kv_heads, head_dim] +1/-1 sign vectors for keys and values of one layer
+    (numpy arrays, computed on the host by the library)."""
+    k = np.zeros((num_kv_heads, head_dim), dtype=np.int8)
+    v = np.zeros((num_kv_heads, head_dim), dtype=np.int8)
+    _check(lib().kvq_make_signs(seed & ((1 << 64) - 1), layer, num_kv_heads, head_dim, k.ctypes.data, v.ctypes.data),
+           "kvq_make_signs")
+    return k, v
 
 
 # ----------------------------------------------------------------------------- GPU entry points

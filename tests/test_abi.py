@@ -259,3 +259,22 @@ def test_outlier_calibrate_checks(kvq):
     assert L.kvq_outlier_calibrate(1 << 41, 10, 0, 128, 1 << 42, None) == 1
     assert L.kvq_outlier_calibrate(1 << 41, 10, 2, 64, 1 << 42, None) == 2
     assert L.kvq_outlier_calibrate(1 << 41, 10, 2, 128, (1 << 42) + 2, None) == 1
+
+
+@pytest.mark.parametrize("seed,layer,hkv,d", [(0, 0, 1, 64), (12345, 3, 8, 128), ((1 << 64) - 1, 31, 2, 256),
+                                              (0x9E3779B97F4A7C15, 1000, 16, 128)])
+def test_make_signs_matches_oracle(kvq, seed, layer, hkv, d):
+    from oracle import signs as osg
+    k, v = kvq.kvq_make_signs(seed, layer, hkv, d)
+    ok, ov = osg.make_signs(seed, layer, hkv, d)
+    assert np.array_equal(k, ok) and np.array_equal(v, ov)
+
+
+def test_make_signs_argument_checks(kvq):
+    lib = kvq.lib()
+    buf = np.zeros(256, dtype=np.int8)
+    assert lib.kvq_make_signs(0, 0, 1, 128, None, buf.ctypes.data) == 1
+    assert lib.kvq_make_signs(0, -1, 1, 128, buf.ctypes.data, buf.ctypes.data) == 1
+    assert lib.kvq_make_signs(0, 1 << 24, 1, 128, buf.ctypes.data, buf.ctypes.data) == 1
+    assert lib.kvq_make_signs(0, 0, 0, 128, buf.ctypes.data, buf.ctypes.data) == 1
+    assert lib.kvq_make_signs(0, 0, 1, 96, buf.ctypes.data, buf.ctypes.data) == 2
