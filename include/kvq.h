@@ -280,8 +280,21 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
                                         float* out, void* workspace,
                                         size_t workspace_bytes, void* stream);
 
+/* Device-side error bits of a decode call.  The kernels check what only the device can see
+ * (lengths and block-table entries live in device memory) and never read outside a buffer
+ * because of it; a call that raised a bit has a wrong result for the sequences concerned.
+ * They reach the caller through kvq_decode_options.status. */
+#define KVQ_DEVERR_COPY_TIMEOUT 1 /* a wait for one of the kernel's own bulk copies gave up
+                                     after its iteration limit: the work items of that warp
+                                     contribute nothing to the result */
+#define KVQ_DEVERR_PAGE_INDEX 2   /* a block-table entry outside [0, num_pages): the page is
+                                     skipped (its tokens contribute nothing) */
+#define KVQ_DEVERR_SEQ_LEN 4      /* a seq_lens entry outside [0, max_pages * page_size]: it is
+                                     clamped into that range */
+
 /* Options of kvq_decode_attention_ex: two features of the FoveatedKV page's fused kernel
- * ("Making it fast").  All zero is the plain computation of kvq_decode_attention. */
+ * ("Making it fast"), and the device error report.  All zero is the plain computation of
+ * kvq_decode_attention. */
 #define KVQ_SCORE_GATE_NATS 16.0f
 typedef struct kvq_decode_options {
   /* Nonzero: score-gated value loading.  A token whose score is more than
@@ -300,11 +313,15 @@ typedef struct kvq_decode_options {
    * page's spike detection), else 0; 0 when tier 0 or the later tiers hold no token of the
    * sequence.  Scores are compared as the kernels compute them (float32). */
   int32_t* spike_flags;
+  /* Optional device int32 (4-byte aligned), written when non-NULL by the call's last kernel
+   * (stream-ordered, like the output): the OR of the KVQ_DEVERR_* bits the call's kernels
+   * raised, 0 when none.  Not written by a call with batch 0 (it launches nothing). */
+  int32_t* status;
 } kvq_decode_options;
 
 /* kvq_decode_attention with options (NULL options: identical to kvq_decode_attention).
- * Same arguments, workspace and errors, plus: a misaligned spike_flags buffer returns
- * KVQ_ERR_INVALID_ARGUMENT. */
+ * Same arguments, workspace and errors, plus: a misaligned spike_flags or status buffer
+ * returns KVQ_ERR_INVALID_ARGUMENT. */
 KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t num_tiers,
                                            const uint16_t* q, int32_t batch,
                                            int32_t num_q_heads, int32_t split_tokens,
@@ -322,8 +339,12 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
  * is fixed at start-up and forbids later allocations.  This entry point allocates nothing.
  *
  * The first call made while a given device is current looks up that device's scratch
- * address (cudaGetSymbolAddress) and remembers it; make that first call before any stream
- * capture.  Shapes needing more than KVQ_NOALLOC_SCRATCH_BYTES of scratch (see
+ * address (cudaGetSymbolAddress) and remembers it.  Under CUDA's lazy module loading that
+ * lookup is also what loads the library's device code on that device, and with it the
+ * array: the first call may therefore allocate the KVQ_NOALLOC_SCRATCH_BYTES of device
+ * memory, and can fail where none is left.  Make one warm-up call per device at start-up,
+ * before any stream capture and before the memory budget is fixed.  The remembered address
+ * belongs to the device's primary context (the one the CUDA runtime uses).  Shapes needing more than KVQ_NOALLOC_SCRATCH_BYTES of scratch (see
  * kvq_decode_workspace_size) return KVQ_ERR_WORKSPACE_TOO_SMALL and launch nothing.
  * Every call on a device shares the one array and it keeps the last call's contents (each
  * call clears, on its stream, the part that must start at zero); calls whose work overlaps

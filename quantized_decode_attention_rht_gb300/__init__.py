@@ -65,10 +65,12 @@ class KvqTierView(ctypes.Structure):
 class KvqDecodeOptions(ctypes.Structure):
     """Mirror of ``struct kvq_decode_options``."""
 
-    _fields_ = [("score_gate", ctypes.c_int32), ("spike_flags", ctypes.c_void_p)]
+    _fields_ = [("score_gate", ctypes.c_int32), ("spike_flags", ctypes.c_void_p), ("status", ctypes.c_void_p)]
 
 
 SCORE_GATE_NATS = 16.0
+# device-side error bits of a decode call (kvq_decode_options.status)
+DEVERR_COPY_TIMEOUT, DEVERR_PAGE_INDEX, DEVERR_SEQ_LEN = 1, 2, 4
 
 _lib_handle = None
 
@@ -239,19 +241,20 @@ def kvq_decode_workspace_size(tiers, batch: int, num_q_heads: int, split_tokens:
 
 
 def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream=None, score_gate: bool = False,
-                         spike_flags=None) -> None:
+                         spike_flags=None, status=None) -> None:
     """q: fp16 [B, Hq, D]; out: fp32 [B, Hq, D]; workspace: uint8 CUDA tensor.
-    score_gate / spike_flags (int32 [B, Hq] CUDA tensor): the options of
-    kvq_decode_attention_ex (FoveatedKV score-gated value loading and spike detection)."""
-    _dense(q, out, workspace, spike_flags)
+    score_gate / spike_flags (int32 [B, Hq] CUDA tensor) / status (int32 CUDA tensor of one
+    element, receives the call's DEVERR_* bits): the options of kvq_decode_attention_ex
+    (FoveatedKV score-gated value loading and spike detection, the device error report)."""
+    _dense(q, out, workspace, spike_flags, status)
     arr = _views(tiers)
     b, hq, _ = q.shape
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    if not score_gate and spike_flags is None:
+    if not score_gate and spike_flags is None and status is None:
         _check(lib().kvq_decode_attention(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out),
                                           _ptr(workspace), ws_bytes, _stream(stream)), "kvq_decode_attention")
         return
-    opts = KvqDecodeOptions(1 if score_gate else 0, _ptr(spike_flags))
+    opts = KvqDecodeOptions(1 if score_gate else 0, _ptr(spike_flags), _ptr(status))
     _check(lib().kvq_decode_attention_ex(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out), _ptr(workspace),
                                          ws_bytes, ctypes.byref(opts), _stream(stream)), "kvq_decode_attention_ex")
 

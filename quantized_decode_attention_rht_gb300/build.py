@@ -3,7 +3,12 @@
 Every translation unit under csrc/ is compiled in parallel, then linked into
 ``quantized_decode_attention_rht_gb300/libkvq.so``.  Objects live in ``_build/``
 next to this file; a unit is recompiled only when it or a header is newer than
-its object.  Run ``python -m quantized_decode_attention_rht_gb300.build``."""
+its object.  Run ``python -m quantized_decode_attention_rht_gb300.build``.
+
+``build(variant="spintest")`` makes a TEST-ONLY library, ``libkvq_spintest.so`` (objects in
+``_build_spintest/``), whose codebook decode kernel gives up a wait for its own bulk copies
+after two non-blocking polls: the GPU test of the give-up path loads it to see the error
+report on valid data.  The product never loads it."""
 from __future__ import annotations
 
 import concurrent.futures
@@ -41,8 +46,11 @@ def _stale(src: str, obj: str, newest_header: float) -> bool:
     return os.path.getmtime(src) > t or newest_header > t
 
 
-def _compile(nvcc: str, src: str, obj: str, verbose: bool):
-    cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
+VARIANTS = {None: ([], "_build", "libkvq.so"), "spintest": (["-DKVQ_SPIN_TEST"], "_build_spintest", "libkvq_spintest.so")}
+
+
+def _compile(nvcc: str, src: str, obj: str, verbose: bool, defines=()):
+    cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defines, "-I", os.path.join(ROOT, "include"), "-c", src, "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -51,8 +59,11 @@ def _compile(nvcc: str, src: str, obj: str, verbose: bool):
     return src, r.stderr
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, variant=None) -> str:
     nvcc = _nvcc()
+    defines, build_dir, lib_name = VARIANTS[variant]
+    BUILD = os.path.join(HERE, build_dir)
+    LIB = os.path.join(HERE, lib_name)
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     newest_header = max(os.path.getmtime(h) for h in _headers())
@@ -66,7 +77,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     workers = max(1, min(len(jobs), os.cpu_count() or 4))
     if jobs:
         with concurrent.futures.ThreadPoolExecutor(workers) as ex:
-            for src, log in ex.map(lambda j: _compile(nvcc, j[0], j[1], verbose), jobs):
+            for src, log in ex.map(lambda j: _compile(nvcc, j[0], j[1], verbose, defines), jobs):
                 if verbose and log:
                     sys.stderr.write(f"== {os.path.basename(src)}\n{log}")
     if force or jobs or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):

@@ -16,7 +16,18 @@ namespace {
 
 using namespace kvq;
 
-constexpr int kSms = 152;  // GB300; the plan only needs the order of magnitude
+// Streaming multiprocessors of the current device (the split plan sizes its items from
+// it), queried once per device; 152 (GB300) if the query fails.
+int device_sms() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -118,6 +129,7 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
   const kvq_cache* c0 = tiers[0].cache;
   const int ps = c0->page_size, hkv = c0->num_kv_heads, group = hq / hkv;
   if (split_tokens < 0 || split_tokens % ps) return KVQ_ERR_INVALID_ARGUMENT;
+  const int kSms = device_sms();
   // fused kernels: items of about equal bytes, several per warp of a full GPU, sized from
   // the bytes of the tiers their launch covers (a small recent-token window gets small items)
   size_t family_bytes[3] = {0, 0, 0};
@@ -362,9 +374,16 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t
   if (!bytes) return KVQ_ERR_INVALID_ARGUMENT;
   kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
   if (st != KVQ_OK) return st;
-  Plan plan;
-  if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, true, &plan)) != KVQ_OK) return st;
-  *bytes = workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total, has_sketch(tiers, num_tiers));
+  // the plan depends on whether q is 16-byte aligned (the fused fp16 / fp8 kernel loads it in
+  // 16-byte pieces): size for the larger of the two, so any valid q fits
+  size_t most = 0;
+  for (const bool q16 : {true, false}) {
+    Plan plan;
+    if ((st = make_plan(tiers, num_tiers, batch, num_q_heads, split_tokens, q16, &plan)) != KVQ_OK) return st;
+    most = std::max(most, workspace_bytes(batch, num_q_heads, tiers[0].cache->head_dim, plan.total,
+                                          has_sketch(tiers, num_tiers)));
+  }
+  *bytes = most;
   return KVQ_OK;
 }
 
@@ -382,6 +401,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
   kvq_status st = check_tiers(tiers, num_tiers, batch, num_q_heads);
   if (st != KVQ_OK) return st;
   if (options && options->spike_flags && !aligned(options->spike_flags, 4)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (options && options->status && !aligned(options->status, 4)) return KVQ_ERR_INVALID_ARGUMENT;
   if (batch == 0) return KVQ_OK;
   if (!q || !out || !aligned(q, 4) || !aligned(out, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   const kvq_cache* c0 = tiers[0].cache;
@@ -417,6 +437,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
     t.v_bits = c->v_bits;
     t.k_row_bytes = side_row_bytes(c->k_format, c->k_bits, d);
     t.v_row_bytes = side_row_bytes(c->v_format, c->v_bits, d);
+    t.num_pages = c->num_pages;
     t.max_pages = tiers[i].max_pages;
     t.split_begin = at;
     t.num_splits = plan.splits[i];
@@ -435,6 +456,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
   p.ws_pq = sketch ? reinterpret_cast<float*>(reinterpret_cast<char*>(p.ws_min) + align_up(parts * sizeof(float), 256))
                    : nullptr;
   p.spike = options ? options->spike_flags : nullptr;
+  p.status = options ? options->status : nullptr;
   p.gate = options && options->score_gate ? 1 : 0;
   p.batch = batch;
   p.hq = num_q_heads;
@@ -445,6 +467,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
   // all its tiers at once, the codebook and generic kernels one launch per tier), all
   // writing partials into the one workspace, then the combine pass over every tier
   int* counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + need - 256);
+  p.err = counters + kErrorWord;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool fam[3] = {false, false, false};
   for (int i = 0; i < num_tiers; ++i) fam[plan.kind[i]] = true;

@@ -148,7 +148,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
   constexpr int DPL = S::DPL, LPT = S::LPT, TPS = S::TPS;
   const DecTier& T = p.tier[tier_index];
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  const int len = T.seq_lens[b];
+  int bits = 0;
+  const int len = checked_len(T.seq_lens[b], T.max_pages, p.page_size, &bits);
+  if (bits && split == 0 && hk == 0 && threadIdx.x == 0) atomicOr(p.err, bits);
   const int t_begin = split * T.chunk;
   if (t_begin >= len) return;  // the combine pass only reads splits that hold tokens
   const int t_end = min(len, t_begin + T.chunk);
@@ -196,6 +198,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
   const int p_begin = t_begin / p.page_size, p_end = (t_end + p.page_size - 1) / p.page_size;
   for (int lp = p_begin + warp; lp < p_end; lp += kWarps) {
     const int phys = T.block_table[(size_t)b * T.max_pages + lp];
+    int pbits = 0;
+    if (!page_in_pool(phys, T.num_pages, &pbits)) {  // warp-uniform: skip the page
+      if (lane == 0) atomicOr(p.err, pbits);
+      continue;
+    }
     const size_t row_base = ((size_t)phys * p.hkv + hk) * p.page_size;
     for (int s0 = 0; s0 < p.page_size; s0 += TPS) {
       const int off = s0 + gi;
@@ -334,6 +341,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
   __shared__ float s_red[kCombineWarps][2];
   __shared__ float s_spk[kCombineWarps][2];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // partials of the split-K pass are complete
+  // every split-K kernel of the call has completed: its error bits are final
+  if (p.status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = *reinterpret_cast<volatile int*>(p.err);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = blockIdx.x;
   const int b = pair / p.hq, hq = pair % p.hq;
@@ -343,7 +352,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
   int n = 0, n0 = 0;  // splits holding tokens; the first n0 are tier 0's
   for (int ti = 0; ti < p.num_tiers; ++ti) {
     const DecTier& T = p.tier[ti];
-    const int nt = (T.seq_lens[b] + T.chunk - 1) / T.chunk;
+    int bits = 0;  // the split-K kernels raised any bit already
+    const int nt = splits_holding_tokens(checked_len(T.seq_lens[b], T.max_pages, p.page_size, &bits), T.chunk,
+                                         T.num_splits);
     for (int s = threadIdx.x; s < nt && n + s < kCombineMaxSplits; s += blockDim.x)
       s_part[n + s] = T.split_begin + s;
     n += nt;

@@ -42,6 +42,7 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.t.v_norm = t.v_aux;
     p.t.block_table = t.block_table;
     p.t.seq_lens = t.seq_lens;
+    p.t.num_pages = t.num_pages;
     p.t.max_pages = t.max_pages;
     p.t.chunk = t.chunk;
     p.t.nchunks = t.num_splits;
@@ -57,7 +58,7 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.gate = dp.gate;
     p.track = dp.spike != nullptr && i == 0;
     p.counter = counters + i;
-    p.err = counters + kCbErrorWord;
+    p.t.err = dp.err;
     p.hq = dp.hq;
     p.hkv = dp.hkv;
     p.total_splits = dp.total_splits;

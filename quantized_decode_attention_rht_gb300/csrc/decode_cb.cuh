@@ -69,6 +69,14 @@ constexpr float kQScale = 64.0f;   // the rotated queries hold 2^6 q'
 constexpr float kWScale = 8.0f;    // weight fragments hold 2^3 p norm / sqrt(D); with p <= 1
                                    // every fp16 norm stays below the fp16 maximum
 constexpr int kSpinLimit = 1 << 22;  // try_wait rounds before a slot counts as lost
+// KVQ_SPIN_TEST (a test-only build, never the library's): the slot wait polls with the
+// non-blocking test_wait and gives up after two rounds, so the give-up path runs on valid
+// data; the drain after a give-up keeps the full limit, so every issued copy lands first.
+#ifdef KVQ_SPIN_TEST
+constexpr int kSlotSpinLimit = 2;
+#else
+constexpr int kSlotSpinLimit = kSpinLimit;
+#endif
 typedef unsigned long long u64;
 
 // ---------------------------------------------------------------- PTX helpers
@@ -158,6 +166,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of a phase (test builds' slot wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Plain arrival: completes the phase of a barrier that expects no bytes (a skipped page).
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(mbar)
@@ -200,7 +222,8 @@ struct CbTier {
   const int32_t* outl;   // keys with an outlier stream: channels [Hkv][KVQ_OUTLIER_CHANNELS]
   const int32_t* block_table;
   const int32_t* seq_lens;
-  int max_pages, chunk, nchunks, split_begin;
+  int* err;  // the call's error word (KVQ_DEVERR_* bits)
+  int num_pages, max_pages, chunk, nchunks, split_begin;
 };
 
 struct CbParams {
@@ -214,7 +237,6 @@ struct CbParams {
   float* pq;     // keys with a residual sketch: p' = S q' per query head, [B][Hq][KVQ_QJL_DIM]
   float* ws_min; // lowest score per split, written when `track` (tier 0, spike flags asked for)
   int* counter;  // this launch's work counter
-  int* err;      // error word: set when a wait for a bulk copy gives up
   int hq, hkv, total_splits, total_items, smem_bytes;
   int gate, track;  // score-gated value loading; record the lowest score
   int pdl;          // launched as a programmatic dependent of the previous split-K launch
@@ -390,7 +412,9 @@ __device__ __forceinline__ Item fetch_item(const CbParams& p, int item, int lane
   it.hk = rem % p.hkv;
   it.b = rem / p.hkv;
   it.t0 = it.chunk * T.chunk;
-  it.len = __ldg(T.seq_lens + it.b);
+  int bits = 0;
+  it.len = checked_len(__ldg(T.seq_lens + it.b), T.max_pages, PS, &bits);
+  if (bits && lane == 0 && it.chunk == 0) atomicOr(T.err, bits);
   const int pg = it.t0 / PS + lane;
   it.btw = pg < T.max_pages ? (uint32_t)__ldg(T.block_table + (size_t)it.b * T.max_pages + pg) : 0u;
   return it;
@@ -405,39 +429,76 @@ __device__ __forceinline__ int item_pages(const CbTier& T, const Item& it) {
 struct Ring {
   uint32_t slots, bars;  // shared addresses
   int issued, consumed;  // stream positions (pages)
+  uint32_t bad;          // bit (position % 8): the page at that position lay outside the pool
+                         // and was not copied (at most STAGES positions are in flight)
   bool lost;             // a slot wait gave up
 };
+
+// The page at the ring's next consumed position was skipped (out of the pool): its slot holds
+// nothing of it and must not be read.
+__device__ __forceinline__ bool ring_page_bad(const Ring& rg) { return (rg.bad >> (rg.consumed & 7)) & 1u; }
 
 template <class L>
 __device__ __forceinline__ void ring_issue(const CbTier& T, int hkv, Ring& rg, uint32_t phys, int hk, int lane) {
   const int slot = rg.issued % L::STAGES;
+  int bits = 0;
+  const bool ok = page_in_pool((int)phys, T.num_pages, &bits);  // warp-uniform
+  const uint32_t bit = 1u << (rg.issued & 7);
+  rg.bad = ok ? (rg.bad & ~bit) : (rg.bad | bit);
   if (lane == 0) {
     const uint32_t dst = rg.slots + slot * L::STAGE, bar = rg.bars + 8 * slot;
-    const size_t blk = (size_t)phys * hkv + hk;
-    fence_proxy_async();  // the slot's previous page was read through the generic proxy
-    mbar_expect_tx(bar, L::STAGE);
-    bulk_g2s(dst, T.k_rows + blk * L::KBLK, L::KBLK, bar);
-    bulk_g2s(dst + L::KBLK, T.v_rows + blk * L::VBLK, L::VBLK, bar);
-    bulk_g2s(dst + L::KBLK + L::VBLK, T.k_norm + blk * (L::KNORM / 2), L::KNORM, bar);
-    bulk_g2s(dst + L::KBLK + L::VBLK + L::KNORM, T.v_norm + blk * PS, 32, bar);
+    if (ok) {
+      const size_t blk = (size_t)phys * hkv + hk;
+      fence_proxy_async();  // the slot's previous page was read through the generic proxy
+      mbar_expect_tx(bar, L::STAGE);
+      bulk_g2s(dst, T.k_rows + blk * L::KBLK, L::KBLK, bar);
+      bulk_g2s(dst + L::KBLK, T.v_rows + blk * L::VBLK, L::VBLK, bar);
+      bulk_g2s(dst + L::KBLK + L::VBLK, T.k_norm + blk * (L::KNORM / 2), L::KNORM, bar);
+      bulk_g2s(dst + L::KBLK + L::VBLK + L::KNORM, T.v_norm + blk * PS, 32, bar);
+    } else {
+      atomicOr(T.err, bits);
+      mbar_arrive(bar);  // no copy: the phase completes at once, the consumer skips the page
+    }
   }
   ++rg.issued;
 }
 
 // Wait until the next page of the stream has landed; returns its slot address.
 template <class L>
-__device__ __forceinline__ uint32_t ring_wait(Ring& rg, int* err) {
+__device__ __forceinline__ uint32_t ring_wait(Ring& rg, int* err, int lane) {
   const int slot = rg.consumed % L::STAGES;
   const uint32_t parity = (rg.consumed / L::STAGES) & 1;
   int n = 0;
+#ifdef KVQ_SPIN_TEST
+  while (!mbar_test_wait(rg.bars + 8 * slot, parity)) {
+#else
   while (!mbar_try_wait(rg.bars + 8 * slot, parity)) {
-    if (++n >= kSpinLimit) {
+#endif
+    if (++n >= kSlotSpinLimit) {
       rg.lost = true;
-      atomicExch(err, 1);
       break;
     }
   }
+  // lanes may disagree on when the phase completed: the warp is lost if any lane gave up
+  rg.lost = __any_sync(kFull, rg.lost);
+  if (rg.lost && lane == 0) atomicOr(err, KVQ_DEVERR_COPY_TIMEOUT);
   return rg.slots + slot * L::STAGE;
+}
+
+// A partial that contributes nothing (running max -inf, sum 0): written for every work item
+// a warp took but could not finish after a slot wait gave up, so the combine pass never
+// reads a stale partial.
+template <int D, int G>
+__device__ void empty_partial(const CbParams& p, const Item& it, int lane) {
+  for (int h = 0; h < G; ++h) {
+    const size_t part = ((size_t)it.b * p.hq + it.hk * G + h) * p.total_splits + p.t.split_begin + it.chunk;
+    for (int j = lane; j < D; j += 32) p.ws_acc[part * D + j] = 0.f;
+    if (lane == 0) {
+      p.ws_ml[2 * part] = -INFINITY;
+      p.ws_ml[2 * part + 1] = 0.f;
+      if (p.track) p.ws_min[part] = INFINITY;
+    }
+  }
 }
 
 // Feeds the pages of an item (and the first pages of the next one) into the ring, STAGES
@@ -619,8 +680,17 @@ struct Path1 {
     constexpr float sscale = kInvD / kQScale;
 #pragma unroll 1
     for (int i = 0; i < npg; ++i) {
-      const uint32_t st = ring_wait<L>(rg, p.err);
-      if (rg.lost) return;
+      const uint32_t st = ring_wait<L>(rg, T.err, lane);
+      if (rg.lost) {
+        empty_partial<D, 1>(p, it, lane);
+        return;
+      }
+      if (ring_page_bad(rg)) {  // a page outside the pool: nothing was copied, skip it
+        __syncwarp();
+        ++rg.consumed;
+        fd.top_up(rg);
+        continue;
+      }
       uint32_t k[2][KW], v[2][VW];
       lds_run<KBYTES>(st + t * L::KROW + c * KBYTES, k[0]);
       lds_run<KBYTES>(st + (t + 8) * L::KROW + c * KBYTES, k[1]);
@@ -872,8 +942,17 @@ struct PathM {
     const bool lo_part = g & 1, live_col = hB < G;
 #pragma unroll 1
     for (int i = 0; i < npg; ++i) {
-      const uint32_t st = ring_wait<L>(rg, p.err);
-      if (rg.lost) return;
+      const uint32_t st = ring_wait<L>(rg, T.err, lane);
+      if (rg.lost) {
+        empty_partial<D, G>(p, it, lane);
+        return;
+      }
+      if (ring_page_bad(rg)) {  // a page outside the pool: nothing was copied, skip it
+        __syncwarp();
+        ++rg.consumed;
+        fd.top_up(rg);
+        continue;
+      }
       uint32_t k[2][KW], v[4][VW];
       lds_run<KBYTES>(st + g * L::KROW + c * KBYTES, k[0]);
       lds_run<KBYTES>(st + (g + 8) * L::KROW + c * KBYTES, k[1]);
@@ -1086,6 +1165,7 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   rg.slots = area;
   rg.bars = area + L::STAGES * L::STAGE + L::QBUF;
   rg.issued = rg.consumed = 0;
+  rg.bad = 0u;
   rg.lost = false;
   float* qbuf = reinterpret_cast<float*>(smem + (area + L::STAGES * L::STAGE - base));
   if (lane == 0) {
@@ -1107,9 +1187,11 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   item = __shfl_sync(kFull, item, 0);
   next = __shfl_sync(kFull, next, 0);
   Item cur = fetch_item(p, item < p.total_items ? item : 0, lane);
-  while (item < p.total_items && !rg.lost) {
-    int after = 0;
-    if (lane == 0) after = atomicAdd(p.counter, 1);
+  while (item < p.total_items) {
+    // a warp whose slot wait gave up takes no new items; the ones it already holds get
+    // empty partials
+    int after = p.total_items;
+    if (lane == 0 && !rg.lost) after = atomicAdd(p.counter, 1);
     const bool has_next = next < p.total_items;
     Item nx = cur;
     if (has_next) {
@@ -1117,7 +1199,10 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
       const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q + ((size_t)nx.b * p.hq + nx.hk * P::kG) * P::kD);
       if (lane < L::QLINES) prefetch_l2(qrow + 128 * lane);
     }
-    if (cur.len > cur.t0) P::run_item(p, cur, has_next, nx, qbuf, rg, klane, vlane, slane, lane);
+    if (cur.len > cur.t0) {
+      if (rg.lost) empty_partial<P::kD, P::kG>(p, cur, lane);
+      else P::run_item(p, cur, has_next, nx, qbuf, rg, klane, vlane, slane, lane);
+    }
     item = next;
     next = __shfl_sync(kFull, after, 0);
     cur = nx;

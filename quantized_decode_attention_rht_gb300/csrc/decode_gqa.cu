@@ -130,6 +130,7 @@ struct GqaTier {
   const __half* v_aux;
   const int32_t* block_table;
   const int32_t* seq_lens;
+  int num_pages;  // pages in the pool: block-table entries at or above are skipped
   int far;    // 1: fp8 K + INT4-g32 V; 0: fp16 K + fp16 V
   int first;  // tier 0 of the call (the near tier of spike detection)
   int max_pages, chunk, nchunks, split_begin, item_begin;
@@ -144,6 +145,7 @@ struct GqaParams {
   float* ws_ml;
   float* ws_min;  // lowest score per tier-0 split, when spike flags are asked for
   int* counter;
+  int* err;       // the call's error word (KVQ_DEVERR_* bits)
   int hq, hkv, total_splits, total_items;
   int group;        // query heads per kv head (1, 2 or 4); heads group.. of an item are idle
   int trigger;      // a codebook split-K launch follows (as a programmatic dependent)
@@ -554,7 +556,12 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
   int* btab = reinterpret_cast<int*>(wsm + kBtab);
   const int pg0 = t0 / PS, npg = (t1 + PS - 1) / PS - pg0;
   const int32_t* bt = T.block_table + (size_t)b * T.max_pages + pg0;
-  for (int i = lane; i < npg; i += 32) btab[i] = __ldg(bt + i);
+  int bits = 0;
+  for (int i = lane; i < npg; i += 32) {
+    const int e = __ldg(bt + i);
+    btab[i] = page_in_pool(e, T.num_pages, &bits) ? e : -1;  // -1: skipped below
+  }
+  if (__any_sync(kFull, bits != 0) && lane == 0) atomicOr(p.err, KVQ_DEVERR_PAGE_INDEX);
   rotate_query(p, b, hk, qbuf, lane);
   __syncwarp();
   uint32_t qf[8][2];
@@ -565,7 +572,7 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
   const uint32_t ring = smem_addr(wsm);
 #pragma unroll 1
   for (int s = 0; s < TT::S; ++s) {
-    if (s < npg) TT::issue(T, pl, btab[s], hk, p.hkv, ring + s * TT::STAGE, lane);
+    if (s < npg && btab[s] >= 0) TT::issue(T, pl, btab[s], hk, p.hkv, ring + s * TT::STAGE, lane);
     cp_commit();
   }
   typename TT::State st;
@@ -576,9 +583,10 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
     __syncwarp();
     const int slot = i % TT::S;
     const int nvalid = min(PS, t1 - (pg0 + i) * PS);
-    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.group);
+    if (btab[i] >= 0) TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.group);
     __syncwarp();
-    if (i + TT::S < npg) TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
+    if (i + TT::S < npg && btab[i + TT::S] >= 0)
+      TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
     cp_commit();
   }
   cp_wait<0>();
@@ -607,7 +615,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
     const int chunk = rem % T.nchunks;
     rem /= T.nchunks;
     const int hk = rem % p.hkv, b = rem / p.hkv;
-    const int len = T.seq_lens[b];
+    int bits = 0;
+    const int len = checked_len(T.seq_lens[b], T.max_pages, PS, &bits);
+    if (bits && chunk == 0 && lane == 0) atomicOr(p.err, bits);
     const int t0 = chunk * T.chunk;
     if (t0 < len) {
       const int t1 = min(len, t0 + T.chunk);
@@ -654,6 +664,7 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
     g.v_aux = t.v_aux;
     g.block_table = t.block_table;
     g.seq_lens = t.seq_lens;
+    g.num_pages = t.num_pages;
     g.far = t.k_fmt == KVQ_FMT_FP8_E4M3;
     g.max_pages = t.max_pages;
     g.chunk = t.chunk;
@@ -673,6 +684,7 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
   p.gate = dp.gate;
   p.spike = dp.spike != nullptr;
   p.counter = counter;
+  p.err = dp.err;
   p.hq = dp.hq;
   p.hkv = dp.hkv;
   p.total_splits = dp.total_splits;

@@ -55,9 +55,39 @@ cudaError_t launch_requantize(const QuantParams& p, int head_dim, cudaStream_t s
 // Kernel family of a decode tier (chosen per tier on the host).
 enum TierKind { TIER_GENERIC = 0, TIER_GQA = 1, TIER_CB = 2 };
 // The 256-byte counter block at the end of the decode workspace (cleared once per call):
-// ints [0, KVQ_MAX_TIERS) codebook work counters, kCbErrorWord the codebook kernel's error
-// word, kGqaCounter the fused fp16 / fp8 + INT4 kernel's work counter.
-constexpr int kCbErrorWord = 32, kGqaCounter = 40;
+// ints [0, KVQ_MAX_TIERS) codebook work counters, kErrorWord the call's device error word
+// (the OR of the KVQ_DEVERR_* bits any of its kernels raised), kGqaCounter the fused fp16 /
+// fp8 + INT4 kernel's work counter.
+constexpr int kErrorWord = 32, kGqaCounter = 40;
+
+// ------------------------------------------------------------------------ index checks
+// Every decode kernel reads lengths and block-table entries from device memory the host
+// never sees, so it checks them itself before using them: a length outside
+// [0, max_pages * page_size] is clamped into it, a page outside [0, num_pages) is skipped,
+// and either raises its KVQ_DEVERR_* bit in *bits (the kernels OR the bits into the call's
+// error word).  Host-callable, so a CPU test can drive them with out-of-range values.
+__host__ __device__ __forceinline__ int checked_len(int len, int max_pages, int page_size, int* bits) {
+  const long long cap = (long long)max_pages * page_size;
+  if (len < 0 || (long long)len > cap) {
+    *bits |= KVQ_DEVERR_SEQ_LEN;
+    return len < 0 ? 0 : (int)cap;
+  }
+  return len;
+}
+// true when the page may be read; false (and the bit raised) when it lies outside the pool
+__host__ __device__ __forceinline__ bool page_in_pool(int phys, int num_pages, int* bits) {
+  if (phys < 0 || phys >= num_pages) {
+    *bits |= KVQ_DEVERR_PAGE_INDEX;
+    return false;
+  }
+  return true;
+}
+// Split-K chunks of one sequence that hold tokens (len already checked), never more than
+// the plan made for the tier.
+__host__ __device__ __forceinline__ int splits_holding_tokens(int len, int chunk, int num_splits) {
+  const int n = (len + chunk - 1) / chunk;
+  return n < num_splits ? n : num_splits;
+}
 
 struct DecTier {
   const uint8_t* k_rows;
@@ -72,6 +102,7 @@ struct DecTier {
   const int32_t* seq_lens;
   int k_fmt, v_fmt, k_bits, v_bits, k_row_bytes, v_row_bytes;
   int kind;  // TierKind
+  int num_pages;  // pages in the pool (block-table entries must lie below)
   int max_pages, split_begin, num_splits, chunk;
 };
 
@@ -87,6 +118,8 @@ struct DecParams {
   float* ws_pq;   // [B][Hq][KVQ_QJL_DIM] projected queries when a tier's keys carry a sketch
   float* ws_min;  // [B][Hq][S] lowest score of each tier-0 split (written when spike != null)
   int* spike;     // [B][Hq] spike flags, or null
+  int* err;       // the call's device error word (KVQ_DEVERR_* bits), zero at launch
+  int* status;    // where the combine pass copies the error word, or null
   int gate;       // score-gated value loading
   int batch, hq, hkv, page_size, total_splits;
 };
@@ -106,8 +139,7 @@ cudaError_t launch_decode_gqa(const DecParams& p, int* counter, cudaStream_t str
 // Fused tensor-core decode over codebook tiers (codebook K and V), head_dim 128 or 256,
 // 1, 2 or 4 query heads per kv head; one launch per tier (after one projection launch when
 // a tier's keys carry a sketch).  `counters`: the 256-byte counter block, zero at launch
-// (ints [0, KVQ_MAX_TIERS) work counters, kCbErrorWord set when a wait for one of the
-// kernel's own bulk copies gives up).
+// (ints [0, KVQ_MAX_TIERS) work counters; the error word is DecParams::err).
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt);
 // after_split_k: a split-K launch of this call precedes; the codebook grids then run as its
 // programmatic dependents (overlapping its tail) and complete only after it.

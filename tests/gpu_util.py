@@ -273,12 +273,42 @@ def build_exact(kvq, torch, tier_specs, tier_kv, k_signs, v_signs, page_size=16,
     return Built(ora_tiers, gpu, views, k_signs, v_signs)
 
 
+# ----------------------------------------------------------------------------- guard bands
+
+GUARD_BYTES = 4096  # canary bytes before and after a guarded buffer (keeps 256-byte alignment)
+GUARD_FRONT, GUARD_BACK = 0xA5, 0x5A
+
+
+def guarded_empty(torch, shape, dtype):
+    """(backing uint8 buffer, view of `shape` / `dtype` inside it) with GUARD_BYTES of canary
+    pattern on each side, for checking that a kernel writes nothing outside its buffer."""
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    buf = torch.empty(n + 2 * GUARD_BYTES, dtype=torch.uint8, device="cuda")
+    buf[:GUARD_BYTES].fill_(GUARD_FRONT)
+    buf[GUARD_BYTES + n:].fill_(GUARD_BACK)
+    view = buf[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+    return buf, view
+
+
+def assert_guards(buf, view):
+    n = view.numel() * view.element_size()
+    front, back = buf[:GUARD_BYTES].cpu().numpy(), buf[GUARD_BYTES + n:].cpu().numpy()
+    assert (front == GUARD_FRONT).all(), "write before the buffer"
+    assert (back == GUARD_BACK).all(), "write after the buffer"
+
+
 def gpu_decode(kvq, torch, views, q16, split_tokens=0):
+    """Decode through the C ABI with guard bands around the output and the workspace and the
+    device error report on; both are checked after the call."""
     q = torch.from_numpy(q16).cuda()
     b, hq, d = q16.shape
-    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(1, kvq.kvq_decode_workspace_size(views, b, hq, split_tokens)), dtype=torch.uint8,
-                     device="cuda")
-    kvq.kvq_decode_attention(views, q, out, ws, split_tokens)
+    out_buf, out = guarded_empty(torch, (b, hq, d), torch.float32)
+    ws_buf, ws = guarded_empty(torch, (max(1, kvq.kvq_decode_workspace_size(views, b, hq, split_tokens)),),
+                               torch.uint8)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvq.kvq_decode_attention(views, q, out, ws, split_tokens, status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device error bits {int(status.item())}"
+    assert_guards(out_buf, out)
+    assert_guards(ws_buf, ws)
     return out.cpu().numpy()

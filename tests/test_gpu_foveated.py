@@ -35,12 +35,17 @@ OUTLIER_LIST = np.tile(np.array([0, 5, 17, 40, 64, 99, 100, 127], dtype=np.int32
 def decode_ex(kvq, torch, views, q16, split_tokens=0, score_gate=False, spikes=False):
     q = torch.from_numpy(q16).cuda()
     b, hq, d = q16.shape
-    out = torch.empty((b, hq, d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(max(1, kvq.kvq_decode_workspace_size(views, b, hq, split_tokens)), dtype=torch.uint8,
-                     device="cuda")
+    out_buf, out = gu.guarded_empty(torch, (b, hq, d), torch.float32)
+    ws_buf, ws = gu.guarded_empty(torch, (max(1, kvq.kvq_decode_workspace_size(views, b, hq, split_tokens)),),
+                                  torch.uint8)
     flags = torch.full((b, hq), -1, dtype=torch.int32, device="cuda") if spikes else None
-    kvq.kvq_decode_attention(views, q, out, ws, split_tokens, score_gate=score_gate, spike_flags=flags)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    kvq.kvq_decode_attention(views, q, out, ws, split_tokens, score_gate=score_gate, spike_flags=flags,
+                             status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    gu.assert_guards(out_buf, out)
+    gu.assert_guards(ws_buf, ws)
     return out.cpu().numpy(), (flags.cpu().numpy() if spikes else None)
 
 

@@ -3,8 +3,6 @@ device memory (plugins inside a framework that owns all device memory, serving l
 memory budget fixed at start-up): it uses the library's static device scratch instead of a
 caller-provided workspace.  Its results must match kvq_decode_attention's on the same inputs,
 on consecutive calls (the scratch keeps the previous call's contents)."""
-import ctypes
-
 import numpy as np
 import pytest
 
@@ -54,20 +52,25 @@ def test_noalloc_matches_workspace_entry_point():
 
 @pytest.mark.gpu
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    gu.torch_cuda()
+    """A shape whose split-K scratch exceeds the static array is refused before any launch.
+    Every pointer handed over is a real allocation (a 4-page cache, a zeroed block table,
+    zero lengths, real queries and outputs), so even a launch could read nothing invalid."""
+    torch = gu.torch_cuda()
     kvq = gu.kvq_module()
-    s = kvq.KvqCache()
-    s.head_dim, s.num_kv_heads, s.page_size, s.num_pages = 128, 8, 16, 4
-    s.k_format = s.v_format = kvq.FMT_CODEBOOK
-    s.k_bits = s.v_bits = 4
-    for i, f in enumerate(("k_rows", "v_rows", "k_aux", "v_aux", "k_centroids", "k_bounds", "v_centroids",
-                           "v_bounds", "k_signs", "v_signs")):
-        setattr(s, f, (1 << 40) + 4096 * i)  # never dereferenced: the size check comes first
-    views = (kvq.KvqTierView * 1)()
-    views[0].cache = ctypes.pointer(s)
-    views[0].block_table = 1 << 43
-    views[0].seq_lens = 1 << 44
-    views[0].max_pages = 1 << 16  # 1M tokens in 1024-token splits: 1024 splits per output,
-    # within the split limit but ~1 GB of partials, far more scratch than it has
-    st = kvq.lib().kvq_decode_attention_noalloc(views, 1, 1 << 45, 64, 32, 1024, 1 << 46, None)
+    ks = torch.ones((8, 128), dtype=torch.int8, device="cuda")
+    cache = kvq.PagedCache(128, 8, 4, "codebook", "codebook", 4, 4, ks, ks)
+    batch, hq, max_pages = 64, 32, 1 << 16  # 1M tokens in 1024-token splits: 1024 splits per
+    # output, within the split limit but ~1 GB of partials, far more scratch than it has
+    bt = torch.zeros((batch, max_pages), dtype=torch.int32, device="cuda")
+    lens = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    q = torch.zeros((batch, hq, 128), dtype=torch.float16, device="cuda")
+    out = torch.full((batch, hq, 128), 7.0, dtype=torch.float32, device="cuda")
+    views = [kvq.TierView(cache, bt, lens)]
+    assert kvq.kvq_decode_workspace_size(views, batch, hq, 1024) > kvq.NOALLOC_SCRATCH_BYTES
+    launches = kvq.kvq_kernel_launches()
+    st = kvq.lib().kvq_decode_attention_noalloc(kvq._views(views), 1, q.data_ptr(), batch, hq, 1024,
+                                                out.data_ptr(), None)
+    torch.cuda.synchronize()
     assert st == 3  # KVQ_ERR_WORKSPACE_TOO_SMALL
+    assert kvq.kvq_kernel_launches() == launches  # nothing was launched
+    assert (out == 7.0).all().item()  # nothing was written
