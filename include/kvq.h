@@ -287,10 +287,13 @@ KVQ_API kvq_status kvq_decode_attention(const kvq_tier_view* tiers, int32_t num_
 #define KVQ_DEVERR_COPY_TIMEOUT 1 /* a wait for one of the kernel's own bulk copies gave up
                                      after its iteration limit: the work items of that warp
                                      contribute nothing to the result */
-#define KVQ_DEVERR_PAGE_INDEX 2   /* a block-table entry outside [0, num_pages): the page is
-                                     skipped (its tokens contribute nothing) */
-#define KVQ_DEVERR_SEQ_LEN 4      /* a seq_lens entry outside [0, max_pages * page_size]: it is
-                                     clamped into that range */
+#define KVQ_DEVERR_PAGE_INDEX 2   /* a block-table entry outside [0, num_pages): no read is made
+                                     through it -- the fused fp16 / fp8 kernel leaves out the
+                                     split-K chunk holding it, the codebook kernel reads page 0
+                                     in its place, the generic kernel leaves out the page */
+#define KVQ_DEVERR_SEQ_LEN 4      /* a seq_lens entry outside [0, max_pages * page_size] (a pool
+                                     with num_pages 0 has no room: any length above 0): it is
+                                     cut into that range */
 
 /* Options of kvq_decode_attention_ex: two features of the FoveatedKV page's fused kernel
  * ("Making it fast"), and the device error report.  All zero is the plain computation of

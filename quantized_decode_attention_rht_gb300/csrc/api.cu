@@ -104,6 +104,10 @@ struct Plan {
   int total;
 };
 
+// Pages of the block table a call may use: none for a pool without pages (every length
+// above 0 is then out of range: the kernels see an empty tier and the report says so).
+int usable_pages(const kvq_tier_view& t) { return t.cache->num_pages > 0 ? t.max_pages : 0; }
+
 size_t token_bytes(const kvq_cache* c) {
   size_t rk, ak, rv, av;
   side_bytes(c->k_format, c->k_bits, c->head_dim, &rk, &ak);
@@ -135,11 +139,11 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
   size_t family_bytes[3] = {0, 0, 0};
   for (int i = 0; i < n; ++i) {
     plan->kind[i] = tier_kind(tiers[i].cache, group, split_tokens, q16);
-    family_bytes[plan->kind[i]] += (size_t)batch * hkv * tiers[i].max_pages * ps * token_bytes(tiers[i].cache);
+    family_bytes[plan->kind[i]] += (size_t)batch * hkv * usable_pages(tiers[i]) * ps * token_bytes(tiers[i].cache);
   }
   plan->total = 0;
   for (int i = 0; i < n; ++i) {
-    const long long max_len = (long long)tiers[i].max_pages * ps;
+    const long long max_len = (long long)usable_pages(tiers[i]) * ps;
     const int kind = plan->kind[i];
     int chunk = split_tokens;
     if (chunk == 0 && kind != TIER_GENERIC) {
@@ -438,7 +442,7 @@ KVQ_API kvq_status kvq_decode_attention_ex(const kvq_tier_view* tiers, int32_t n
     t.k_row_bytes = side_row_bytes(c->k_format, c->k_bits, d);
     t.v_row_bytes = side_row_bytes(c->v_format, c->v_bits, d);
     t.num_pages = c->num_pages;
-    t.max_pages = tiers[i].max_pages;
+    t.max_pages = usable_pages(tiers[i]);
     t.split_begin = at;
     t.num_splits = plan.splits[i];
     t.chunk = plan.chunk[i];

@@ -148,9 +148,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
   constexpr int DPL = S::DPL, LPT = S::LPT, TPS = S::TPS;
   const DecTier& T = p.tier[tier_index];
   const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-  int bits = 0;
+  int bits = 0;  // a length out of range is cut into it here and reported by the combine pass
   const int len = checked_len(T.seq_lens[b], T.max_pages, p.page_size, &bits);
-  if (bits && split == 0 && hk == 0 && threadIdx.x == 0) atomicOr(p.err, bits);
   const int t_begin = split * T.chunk;
   if (t_begin >= len) return;  // the combine pass only reads splits that hold tokens
   const int t_end = min(len, t_begin + T.chunk);
@@ -341,9 +340,25 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
   __shared__ float s_red[kCombineWarps][2];
   __shared__ float s_spk[kCombineWarps][2];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // partials of the split-K pass are complete
-  // every split-K kernel of the call has completed: its error bits are final
-  if (p.status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = *reinterpret_cast<volatile int*>(p.err);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (p.status && blockIdx.x == 0) {
+    // every split-K kernel of the call has completed: their bits are final; block 0 adds
+    // the lengths out of range (every kernel cut them into range) and reports
+    int bits = 0;
+    for (int i = threadIdx.x; i < p.batch * p.num_tiers; i += blockDim.x) {
+      const DecTier& T = p.tier[i % p.num_tiers];
+      checked_len(T.seq_lens[i / p.num_tiers], T.max_pages, p.page_size, &bits);
+    }
+    bits = __reduce_or_sync(0xFFFFFFFFu, bits);
+    if (lane == 0) s_part[warp] = bits;  // s_part is free until the split list below
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int all = *reinterpret_cast<volatile int*>(p.err);
+      for (int w = 0; w < kCombineWarps; ++w) all |= s_part[w];
+      *p.status = all;
+    }
+    __syncthreads();
+  }
   const int pair = blockIdx.x;
   const int b = pair / p.hq, hq = pair % p.hq;
   const int hk = hq / (p.hq / p.hkv);

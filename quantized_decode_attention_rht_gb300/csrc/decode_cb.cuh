@@ -69,11 +69,13 @@ constexpr float kQScale = 64.0f;   // the rotated queries hold 2^6 q'
 constexpr float kWScale = 8.0f;    // weight fragments hold 2^3 p norm / sqrt(D); with p <= 1
                                    // every fp16 norm stays below the fp16 maximum
 constexpr int kSpinLimit = 1 << 22;  // try_wait rounds before a slot counts as lost
-// KVQ_SPIN_TEST (a test-only build, never the library's): the slot wait polls with the
-// non-blocking test_wait and gives up after two rounds, so the give-up path runs on valid
-// data; the drain after a give-up keeps the full limit, so every issued copy lands first.
+// KVQ_SPIN_TEST (a test-only build, never the library's): the slot wait polls once with the
+// non-blocking test_wait, and a warp polls the first slot of its stream before the copies
+// of that slot are issued -- a poll that cannot succeed -- then issues them: the give-up
+// path runs on valid data every time, with copies in flight; the drain after a give-up
+// keeps the full limit, so every issued copy lands before the CTA exits.
 #ifdef KVQ_SPIN_TEST
-constexpr int kSlotSpinLimit = 2;
+constexpr int kSlotSpinLimit = 1;
 #else
 constexpr int kSlotSpinLimit = kSpinLimit;
 #endif
@@ -175,10 +177,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t a, uint32_t parity) {
       : "r"(a), "r"(parity)
       : "memory");
   return ok != 0;
-}
-// Plain arrival: completes the phase of a barrier that expects no bytes (a skipped page).
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -412,9 +410,9 @@ __device__ __forceinline__ Item fetch_item(const CbParams& p, int item, int lane
   it.hk = rem % p.hkv;
   it.b = rem / p.hkv;
   it.t0 = it.chunk * T.chunk;
-  int bits = 0;
-  it.len = checked_len(__ldg(T.seq_lens + it.b), T.max_pages, PS, &bits);
-  if (bits && lane == 0 && it.chunk == 0) atomicOr(T.err, bits);
+  // a length past the block table is cut there (the combine pass reports it); a negative
+  // one leaves the item empty
+  it.len = min(__ldg(T.seq_lens + it.b), T.max_pages * PS);
   const int pg = it.t0 / PS + lane;
   it.btw = pg < T.max_pages ? (uint32_t)__ldg(T.block_table + (size_t)it.b * T.max_pages + pg) : 0u;
   return it;
@@ -429,36 +427,28 @@ __device__ __forceinline__ int item_pages(const CbTier& T, const Item& it) {
 struct Ring {
   uint32_t slots, bars;  // shared addresses
   int issued, consumed;  // stream positions (pages)
-  uint32_t bad;          // bit (position % 8): the page at that position lay outside the pool
-                         // and was not copied (at most STAGES positions are in flight)
   bool lost;             // a slot wait gave up
 };
 
-// The page at the ring's next consumed position was skipped (out of the pool): its slot holds
-// nothing of it and must not be read.
-__device__ __forceinline__ bool ring_page_bad(const Ring& rg) { return (rg.bad >> (rg.consumed & 7)) & 1u; }
-
+// Issues the copies of page `phys`.  A block-table entry outside the pool (warp-uniform
+// test, which also catches negative entries) is never read through: page 0 is copied in its
+// place (the host gives a pool without pages no work) and the call reports the entry.
 template <class L>
 __device__ __forceinline__ void ring_issue(const CbTier& T, int hkv, Ring& rg, uint32_t phys, int hk, int lane) {
+  if (__builtin_expect(phys >= (uint32_t)T.num_pages, 0)) {
+    if (lane == 0) atomicOr(T.err, KVQ_DEVERR_PAGE_INDEX);
+    phys = 0;
+  }
   const int slot = rg.issued % L::STAGES;
-  int bits = 0;
-  const bool ok = page_in_pool((int)phys, T.num_pages, &bits);  // warp-uniform
-  const uint32_t bit = 1u << (rg.issued & 7);
-  rg.bad = ok ? (rg.bad & ~bit) : (rg.bad | bit);
   if (lane == 0) {
     const uint32_t dst = rg.slots + slot * L::STAGE, bar = rg.bars + 8 * slot;
-    if (ok) {
-      const size_t blk = (size_t)phys * hkv + hk;
-      fence_proxy_async();  // the slot's previous page was read through the generic proxy
-      mbar_expect_tx(bar, L::STAGE);
-      bulk_g2s(dst, T.k_rows + blk * L::KBLK, L::KBLK, bar);
-      bulk_g2s(dst + L::KBLK, T.v_rows + blk * L::VBLK, L::VBLK, bar);
-      bulk_g2s(dst + L::KBLK + L::VBLK, T.k_norm + blk * (L::KNORM / 2), L::KNORM, bar);
-      bulk_g2s(dst + L::KBLK + L::VBLK + L::KNORM, T.v_norm + blk * PS, 32, bar);
-    } else {
-      atomicOr(T.err, bits);
-      mbar_arrive(bar);  // no copy: the phase completes at once, the consumer skips the page
-    }
+    const size_t blk = (size_t)phys * hkv + hk;
+    fence_proxy_async();  // the slot's previous page was read through the generic proxy
+    mbar_expect_tx(bar, L::STAGE);
+    bulk_g2s(dst, T.k_rows + blk * L::KBLK, L::KBLK, bar);
+    bulk_g2s(dst + L::KBLK, T.v_rows + blk * L::VBLK, L::VBLK, bar);
+    bulk_g2s(dst + L::KBLK + L::VBLK, T.k_norm + blk * (L::KNORM / 2), L::KNORM, bar);
+    bulk_g2s(dst + L::KBLK + L::VBLK + L::KNORM, T.v_norm + blk * PS, 32, bar);
   }
   ++rg.issued;
 }
@@ -467,6 +457,7 @@ __device__ __forceinline__ void ring_issue(const CbTier& T, int hkv, Ring& rg, u
 template <class L>
 __device__ __forceinline__ uint32_t ring_wait(Ring& rg, int* err, int lane) {
   const int slot = rg.consumed % L::STAGES;
+  if (rg.lost) return rg.slots;  // a warp that gave up waits for nothing more
   const uint32_t parity = (rg.consumed / L::STAGES) & 1;
   int n = 0;
 #ifdef KVQ_SPIN_TEST
@@ -479,27 +470,16 @@ __device__ __forceinline__ uint32_t ring_wait(Ring& rg, int* err, int lane) {
       break;
     }
   }
-  // lanes may disagree on when the phase completed: the warp is lost if any lane gave up
-  rg.lost = __any_sync(kFull, rg.lost);
-  if (rg.lost && lane == 0) atomicOr(err, KVQ_DEVERR_COPY_TIMEOUT);
+  // A phase seen complete at the first poll is complete for every lane.  After a longer
+  // wait, lanes that kept polling agree through a vote: the warp is lost if any gave up.
+  if (__builtin_expect(n > 0, 0)) {
+    rg.lost = __any_sync(__activemask(), rg.lost);
+    if (rg.lost && lane == 0) atomicOr(err, KVQ_DEVERR_COPY_TIMEOUT);
+  }
   return rg.slots + slot * L::STAGE;
 }
 
-// A partial that contributes nothing (running max -inf, sum 0): written for every work item
-// a warp took but could not finish after a slot wait gave up, so the combine pass never
-// reads a stale partial.
-template <int D, int G>
-__device__ void empty_partial(const CbParams& p, const Item& it, int lane) {
-  for (int h = 0; h < G; ++h) {
-    const size_t part = ((size_t)it.b * p.hq + it.hk * G + h) * p.total_splits + p.t.split_begin + it.chunk;
-    for (int j = lane; j < D; j += 32) p.ws_acc[part * D + j] = 0.f;
-    if (lane == 0) {
-      p.ws_ml[2 * part] = -INFINITY;
-      p.ws_ml[2 * part + 1] = 0.f;
-      if (p.track) p.ws_min[part] = INFINITY;
-    }
-  }
-}
+
 
 // Feeds the pages of an item (and the first pages of the next one) into the ring, STAGES
 // ahead of consumption.  Block-table entries of pages [wbase, wbase + 32) and
@@ -530,7 +510,7 @@ struct Feeder {
     if (npg > 32 && pg0 + 32 + lane < T->max_pages) btw1 = (uint32_t)__ldg(bt + 32 + lane);
   }
   __device__ __forceinline__ void top_up(Ring& rg) {
-    while (rg.issued < rg.consumed + L::STAGES && rg.issued - start < npg + n_next) {
+    while (rg.issued < rg.consumed + L::STAGES && rg.issued - start < npg + n_next && !rg.lost) {
       const int o = rg.issued - start;
       if (o < npg) {
         if (o - wbase >= 32) {  // slide the window by 32 pages
@@ -645,6 +625,14 @@ struct Path1 {
     const int t = lane >> 2, c = lane & 3;
     Feeder<L> fd;
     fd.init(p, it, nx, npg, has_next ? item_pages(T, nx) : 0, rg, lane);
+#ifdef KVQ_SPIN_TEST
+    if (rg.issued == 0) {  // test build: poll the first slot before its copies exist, then
+      ring_wait<L>(rg, T.err, lane);  // issue them so that the drain has copies to wait for
+      rg.lost = false;
+      fd.top_up(rg);
+      rg.lost = true;
+    }
+#endif
     fd.top_up(rg);
     rotate_query<D, 1>(p, b, hk, qbuf, lane);
     __syncwarp();
@@ -681,16 +669,7 @@ struct Path1 {
 #pragma unroll 1
     for (int i = 0; i < npg; ++i) {
       const uint32_t st = ring_wait<L>(rg, T.err, lane);
-      if (rg.lost) {
-        empty_partial<D, 1>(p, it, lane);
-        return;
-      }
-      if (ring_page_bad(rg)) {  // a page outside the pool: nothing was copied, skip it
-        __syncwarp();
-        ++rg.consumed;
-        fd.top_up(rg);
-        continue;
-      }
+      if (rg.lost) break;  // nothing more is read: the item's partial is written empty below
       uint32_t k[2][KW], v[2][VW];
       lds_run<KBYTES>(st + t * L::KROW + c * KBYTES, k[0]);
       lds_run<KBYTES>(st + (t + 8) * L::KROW + c * KBYTES, k[1]);
@@ -799,6 +778,13 @@ struct Path1 {
 #pragma unroll
       for (int j = 0; j < NP; ++j) acc[j] = fma2(W1, lut64x(field_addr<2 * VB>(v[1], 2 * VB * j, vlane)), acc[j]);
     }
+    if (rg.lost) {  // a wait gave up: the item contributes nothing (its partial says so)
+#pragma unroll
+      for (int j = 0; j < NP; ++j) acc[j] = 0ull;
+      m = -INFINITY;
+      l = 0.f;
+      mn = INFINITY;
+    }
     // ---- sums over the 8 token lanes of a coordinate block: reduce-scatter on lane bits 4, 3, 2
     float a[DL];
 #pragma unroll
@@ -886,6 +872,14 @@ struct PathM {
     const uint32_t qlane = pin(((vlane & ~(uint32_t)(L::TABLE - 1)) - L::QTAB) | ((lane & 15) << 4));
     Feeder<L> fd;
     fd.init(p, it, nx, npg, has_next ? item_pages(T, nx) : 0, rg, lane);
+#ifdef KVQ_SPIN_TEST
+    if (rg.issued == 0) {  // test build: poll the first slot before its copies exist, then
+      ring_wait<L>(rg, T.err, lane);  // issue them so that the drain has copies to wait for
+      rg.lost = false;
+      fd.top_up(rg);
+      rg.lost = true;
+    }
+#endif
     fd.top_up(rg);
     rotate_query<D, G>(p, b, hk, qbuf, lane);
     __syncwarp();
@@ -943,16 +937,7 @@ struct PathM {
 #pragma unroll 1
     for (int i = 0; i < npg; ++i) {
       const uint32_t st = ring_wait<L>(rg, T.err, lane);
-      if (rg.lost) {
-        empty_partial<D, G>(p, it, lane);
-        return;
-      }
-      if (ring_page_bad(rg)) {  // a page outside the pool: nothing was copied, skip it
-        __syncwarp();
-        ++rg.consumed;
-        fd.top_up(rg);
-        continue;
-      }
+      if (rg.lost) break;  // nothing more is read: the item's partial is written empty below
       uint32_t k[2][KW], v[4][VW];
       lds_run<KBYTES>(st + g * L::KROW + c * KBYTES, k[0]);
       lds_run<KBYTES>(st + (g + 8) * L::KROW + c * KBYTES, k[1]);
@@ -1122,6 +1107,13 @@ struct PathM {
         }
       }
     }
+    if (rg.lost) {  // a wait gave up: the item contributes nothing (its partial says so)
+#pragma unroll
+      for (int i = 0; i < KS; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+      m = -INFINITY;
+      l = 0.f;
+      mn = INFINITY;
+    }
     // ---- partial of head c: sum over the 8 lanes of the head, coordinates 2*QPT*g ..
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(kFull, l, o);
@@ -1165,7 +1157,6 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   rg.slots = area;
   rg.bars = area + L::STAGES * L::STAGE + L::QBUF;
   rg.issued = rg.consumed = 0;
-  rg.bad = 0u;
   rg.lost = false;
   float* qbuf = reinterpret_cast<float*>(smem + (area + L::STAGES * L::STAGE - base));
   if (lane == 0) {
@@ -1188,10 +1179,10 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   next = __shfl_sync(kFull, next, 0);
   Item cur = fetch_item(p, item < p.total_items ? item : 0, lane);
   while (item < p.total_items) {
-    // a warp whose slot wait gave up takes no new items; the ones it already holds get
-    // empty partials
-    int after = p.total_items;
-    if (lane == 0 && !rg.lost) after = atomicAdd(p.counter, 1);
+    // a warp whose slot wait gave up keeps taking items but writes empty partials for
+    // them: every item gets a partial even if every warp gave up
+    int after = 0;
+    if (lane == 0) after = atomicAdd(p.counter, 1);
     const bool has_next = next < p.total_items;
     Item nx = cur;
     if (has_next) {
@@ -1199,10 +1190,8 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
       const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q + ((size_t)nx.b * p.hq + nx.hk * P::kG) * P::kD);
       if (lane < L::QLINES) prefetch_l2(qrow + 128 * lane);
     }
-    if (cur.len > cur.t0) {
-      if (rg.lost) empty_partial<P::kD, P::kG>(p, cur, lane);
-      else P::run_item(p, cur, has_next, nx, qbuf, rg, klane, vlane, slane, lane);
-    }
+    // after a wait gave up, the items the warp still takes run to an empty partial at once
+    if (cur.len > cur.t0) P::run_item(p, cur, has_next, nx, qbuf, rg, klane, vlane, slane, lane);
     item = next;
     next = __shfl_sync(kFull, after, 0);
     cur = nx;

@@ -547,6 +547,21 @@ struct Near {
   }
 };
 
+// The partial of an item that contributes nothing (running max -inf, sum 0): what an item
+// with a block-table entry outside the pool leaves, so the combine pass reads no stale data.
+__device__ __noinline__ void empty_partial(const GqaParams& p, const GqaTier& T, int b, int hk, int chunk, int lane,
+                                           bool track) {
+  for (int h = 0; h < p.group; ++h) {
+    const size_t part = ((size_t)b * p.hq + hk * p.group + h) * p.total_splits + T.split_begin + chunk;
+    for (int j = lane; j < D; j += 32) p.ws_acc[part * D + j] = 0.f;
+    if (lane == 0) {
+      p.ws_ml[2 * part] = -INFINITY;
+      p.ws_ml[2 * part + 1] = 0.f;
+      if (track) p.ws_min[part] = INFINITY;
+    }
+  }
+}
+
 // One work item: pages [t0, t1) of sequence b, kv head hk in tier T.
 template <class TT>
 __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, int b, int hk, int chunk, int t0,
@@ -559,20 +574,25 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
   int bits = 0;
   for (int i = lane; i < npg; i += 32) {
     const int e = __ldg(bt + i);
-    btab[i] = page_in_pool(e, T.num_pages, &bits) ? e : -1;  // -1: skipped below
+    page_in_pool(e, T.num_pages, &bits);
+    btab[i] = e;
   }
-  if (__any_sync(kFull, bits != 0) && lane == 0) atomicOr(p.err, KVQ_DEVERR_PAGE_INDEX);
-  rotate_query(p, b, hk, qbuf, lane);
+  rotate_query(p, b, hk, qbuf, lane);  // its loads overlap the block-table loads above
   __syncwarp();
   uint32_t qf[8][2];
   TT::qfrag(qbuf, qf, g, c);
   typename TT::Plan pl;
   TT::plan(pl, lane);
   __syncwarp();  // the ring is reused for stages below
+  if (__any_sync(kFull, bits != 0)) {  // a page outside the pool: the item reads nothing
+    if (lane == 0) atomicOr(p.err, KVQ_DEVERR_PAGE_INDEX);
+    empty_partial(p, T, b, hk, chunk, lane, track);
+    return;
+  }
   const uint32_t ring = smem_addr(wsm);
 #pragma unroll 1
   for (int s = 0; s < TT::S; ++s) {
-    if (s < npg && btab[s] >= 0) TT::issue(T, pl, btab[s], hk, p.hkv, ring + s * TT::STAGE, lane);
+    if (s < npg) TT::issue(T, pl, btab[s], hk, p.hkv, ring + s * TT::STAGE, lane);
     cp_commit();
   }
   typename TT::State st;
@@ -583,10 +603,9 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
     __syncwarp();
     const int slot = i % TT::S;
     const int nvalid = min(PS, t1 - (pg0 + i) * PS);
-    if (btab[i] >= 0) TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.group);
+    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.group);
     __syncwarp();
-    if (i + TT::S < npg && btab[i + TT::S] >= 0)
-      TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
+    if (i + TT::S < npg) TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
     cp_commit();
   }
   cp_wait<0>();
@@ -615,9 +634,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
     const int chunk = rem % T.nchunks;
     rem /= T.nchunks;
     const int hk = rem % p.hkv, b = rem / p.hkv;
-    int bits = 0;
+    int bits = 0;  // a length out of range is cut into it here and reported by the combine pass
     const int len = checked_len(T.seq_lens[b], T.max_pages, PS, &bits);
-    if (bits && chunk == 0 && lane == 0) atomicOr(p.err, bits);
     const int t0 = chunk * T.chunk;
     if (t0 < len) {
       const int t1 = min(len, t0 + T.chunk);

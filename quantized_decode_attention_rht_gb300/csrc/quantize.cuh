@@ -30,7 +30,11 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCoords = 32;      // coordinates of one vector held by one thread
-constexpr int kMaxCells = 512;
+constexpr int kMaxCells = 160;   // decision cells a table holds (more: count the boundaries)
+constexpr int kCellCopies = 16;  // lane copies of every cell: the 16 lanes of a half-warp, which
+                                 // one 64-bit shared load serves together, hit 16 different
+                                 // bank pairs whatever cells they look up
+constexpr int kCellBytes = kMaxCells * kCellCopies * 8;  // dynamic shared memory of a block
 typedef unsigned long long u64;
 
 // ---------------------------------------------------------------- packed fp32 helpers
@@ -73,16 +77,19 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr) { asm volatile("pre
 // count[k] = boundaries below the cell, beta[k] = the boundary inside it (in units of w) or
 // +inf.  When t sits exactly between two cells rint may pick either, and both give the same
 // index.  |u| <= sqrt(D), so the table spans every reachable cell and needs no clamping.
+// The cells {count (int bits), beta} live in the block's dynamic shared memory, cell k's
+// kCellCopies copies in one 128-byte row.
 struct Table {
   float inv_w;
   int k0, ncells, nb;  // k0 = lowest cell
   int linear;
+  uint32_t cells;      // shared address of the cell rows
   float bounds[16];
-  float cent[16];          // centroids (the residual sketch needs the decoded values)
-  float2 cell[kMaxCells];  // {count (int bits), beta}
+  float cent[16];      // centroids (the residual sketch needs the decoded values)
 };
 
-__device__ void build_table(Table& t, const float* bounds, const float* cent, int nb, int head_dim) {
+__device__ void build_table(Table& t, float2* cells, const float* bounds, const float* cent, int nb,
+                            int head_dim) {
   // every thread of the block calls this
   if (threadIdx.x < 16) t.bounds[threadIdx.x] = threadIdx.x < nb ? bounds[threadIdx.x] : INFINITY;
   if (threadIdx.x < 16) t.cent[threadIdx.x] = (cent && threadIdx.x <= nb) ? cent[threadIdx.x] : 0.0f;
@@ -100,18 +107,20 @@ __device__ void build_table(Table& t, const float* bounds, const float* cent, in
   const int kmax = (int)ceilf(sqrtf((float)head_dim) * inv_w) + 1;
   const int ncells = 2 * kmax + 1;
   ok = ok && ncells <= kMaxCells;
-  for (int c = threadIdx.x; ok && c < ncells; c += blockDim.x) {
+  for (int i = threadIdx.x; ok && i < ncells * kCellCopies; i += blockDim.x) {
+    const int c = i / kCellCopies;
     const float k = (float)(c - kmax);
     const float lo = (k - 0.5f) * w, hi = (k + 0.5f) * w;  // exact: w a power of two
     int cnt = 0;
     float beta = INFINITY;
-    for (int i = 0; i < nb; ++i) {
-      if (t.bounds[i] < lo) ++cnt;
-      else if (t.bounds[i] < hi) beta = t.bounds[i] * inv_w;
+    for (int b = 0; b < nb; ++b) {
+      if (t.bounds[b] < lo) ++cnt;
+      else if (t.bounds[b] < hi) beta = t.bounds[b] * inv_w;
     }
-    t.cell[c] = make_float2(__int_as_float(cnt), beta);
+    cells[i] = make_float2(__int_as_float(cnt), beta);
   }
   if (threadIdx.x == 0) {
+    t.cells = static_cast<uint32_t>(__cvta_generic_to_shared(cells));
     t.inv_w = ok ? inv_w : 1.0f;  // the fallback compares u against the bounds directly
     t.k0 = -kmax;
     t.ncells = ncells;
@@ -136,9 +145,9 @@ __device__ __forceinline__ void encode_codebook(const Table& tb, float (&y)[E], 
 #pragma unroll
   for (int k = 0; k < W; ++k) w[k] = 0;
   const u64 sc2 = pk(scale, scale), mg2 = pk(kMagic, kMagic);
-  // cell address = base + 8 * (bits - kMagicBits - k0), in 32-bit shared-space arithmetic
-  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(tb.cell)) -
-                        8u * (kMagicBits + static_cast<uint32_t>(tb.k0));
+  // cell address = row of cell (bits - kMagicBits - k0), the copy of this lane's half-warp
+  // position, in 32-bit shared-space arithmetic
+  const uint32_t base = tb.cells - 128u * (kMagicBits + static_cast<uint32_t>(tb.k0)) + 8u * (threadIdx.x & 15u);
   const bool lin = tb.linear;
 #pragma unroll
   for (int e = 0; e < E; e += 2) {
@@ -148,8 +157,8 @@ __device__ __forceinline__ void encode_codebook(const Table& tb, float (&y)[E], 
     uint32_t i0, i1;
     if (!lin) {
       float2 c0, c1;
-      asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(c0.x), "=f"(c0.y) : "r"(base + 8u * __float_as_uint(f0)));
-      asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(c1.x), "=f"(c1.y) : "r"(base + 8u * __float_as_uint(f1)));
+      asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(c0.x), "=f"(c0.y) : "r"(base + 128u * __float_as_uint(f0)));
+      asm("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(c1.x), "=f"(c1.y) : "r"(base + 128u * __float_as_uint(f1)));
       i0 = __float_as_uint(c0.x) + (t0 > c0.y ? 1u : 0u);
       i1 = __float_as_uint(c1.x) + (t1 > c1.y ? 1u : 0u);
     } else {  // no table: count the boundaries (in units of w = 1)
@@ -403,10 +412,11 @@ constexpr long long kSmallMaxVectors = 1 << 14;
 
 // Every vector of one side (kind) that falls to this block (grid-stride over vectors).
 template <int TPV, int FMT, int BITS>
-__device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Table& table) {
+__device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Table& table, float2* cells) {
   constexpr int kE = kCoords, D = kE * TPV, VPB = kThreads / TPV;
   const QuantSide& side = p.side[kind];
-  if constexpr (FMT == F_CB || FMT == F_CBQ) build_table(table, side.bounds, side.centroids, (1 << BITS) - 1, D);
+  if constexpr (FMT == F_CB || FMT == F_CBQ)
+    build_table(table, cells, side.bounds, side.centroids, (1 << BITS) - 1, D);
   const int lane = threadIdx.x & 31, sub = lane % TPV;
   const unsigned gmask = (TPV == 32 ? 0xFFFFFFFFu : ((1u << TPV) - 1u)) << (lane - sub);
   const int nvec = p.num_tokens * p.hkv;
@@ -431,8 +441,9 @@ constexpr int blocks_per_sm(int f0, int f1) {
 template <int TPV, int F0, int B0, int F1, int B1>
 __global__ void __launch_bounds__(kThreads, blocks_per_sm(F0, F1)) quantize_kernel(const QuantParams p) {
   __shared__ Table table;
-  if (blockIdx.y == 0) quantize_side<TPV, F0, B0>(p, p.kind_first, table);
-  else quantize_side<TPV, F1, B1>(p, p.kind_first + 1, table);
+  extern __shared__ float2 cells[];  // kCellBytes when a side is coded, else none
+  if (blockIdx.y == 0) quantize_side<TPV, F0, B0>(p, p.kind_first, table, cells);
+  else quantize_side<TPV, F1, B1>(p, p.kind_first + 1, table, cells);
 }
 
 template <int TPV, int F0, int B0, int F1, int B1>
@@ -442,7 +453,8 @@ cudaError_t launch_q(const QuantParams& p, int sides, int sms, cudaStream_t stre
   const long long need = (nvec + VPB - 1) / VPB;
   const unsigned blocks =
       (unsigned)std::max<long long>(1, std::min<long long>(need, (long long)sms * blocks_per_sm(F0, F1) / sides));
-  quantize_kernel<TPV, F0, B0, F1, B1><<<dim3(blocks, sides), kThreads, 0, stream>>>(p);
+  constexpr bool coded = F0 == F_CB || F0 == F_CBQ || F1 == F_CB || F1 == F_CBQ;
+  quantize_kernel<TPV, F0, B0, F1, B1><<<dim3(blocks, sides), kThreads, coded ? kCellBytes : 0, stream>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;

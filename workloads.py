@@ -9,6 +9,9 @@ Every random draw comes from a numpy PCG64 stream keyed by
 ``SeedSequence([config seed, stream id, *indices])``, so that the K/V of one
 (sequence, kv head) can be regenerated on its own: the oracle recomputes a few
 sampled heads of a multi-gigabyte workload without materialising the rest.
+(Timing runs that never meet the oracle may instead fill a cache with draws of
+the same distributions from a seeded torch generator on the GPU:
+``GpuWorkload(cfg, fill="device")``.)
 
 Workload shapes follow the pages' own workloads:
   * "Shrinking the LLM KV Cache by 8x on CPU: AdapTQ" (The Results): 4-bit
@@ -346,7 +349,11 @@ class GpuWorkload:
     sequence at a time (host fp16 -> device -> kvq_quantize_append).  Holds one PagedCache
     and block table per tier, sized for `capacity(cfg)` tokens per sequence."""
 
-    def __init__(self, cfg: Config, device: str = "cuda", fill: bool = True):
+    def __init__(self, cfg: Config, device: str = "cuda", fill=True):
+        """fill: True -- every sequence's K/V drawn on the host (the PCG64 streams above, the
+        same values the oracle sees); "device" -- drawn on the GPU from a seeded torch
+        generator with the same distributions (single-tier configs; for timing runs whose
+        result is not compared with the oracle); False -- left empty."""
         import torch
         import quantized_decode_attention_rht_gb300 as kvq
 
@@ -388,11 +395,46 @@ class GpuWorkload:
         self.block_tables = [torch.from_numpy(np.maximum(m.block_table, 0)).to(device) for m in self.maps]
         self.seq_lens_dev = [torch.from_numpy(l.astype(np.int32)).to(device) for l in self.tier_len]
         self.device = device
-        if fill:
+        if fill == "device":
+            self.fill_on_device()
+        elif fill:
             for b in range(cfg.batch):
                 for t, (k, v) in enumerate(sequence_tiers(cfg, b, int(self.lens[b]))):
                     self.append(t, b, np.arange(k.shape[0]), k, v)
             torch.cuda.synchronize()
+
+    def device_draw(self, gen, which: int, h_count: int, n: int):
+        """fp16 [n, Hkv, D] draws on the device with the config's distribution: N(0,1) or
+        Student-t(4)/sqrt(2), times the per-channel std or the outlier multipliers."""
+        import torch
+        cfg = self.cfg
+        shape = (n, h_count, cfg.head_dim)
+        if cfg.kv_dist == "student_t4":  # t = z / sqrt(chi2_4 / 4), chi2_4 a sum of 4 squared normals
+            z = torch.randn(shape, generator=gen, device=self.device)
+            chi = sum(torch.randn(shape, generator=gen, device=self.device) ** 2 for _ in range(4))
+            x = z / torch.sqrt(chi / 4.0) / math.sqrt(2.0)
+        else:
+            x = torch.randn(shape, generator=gen, device=self.device)
+        if cfg.kv_dist == "normal_channel_sigma":
+            x *= torch.from_numpy(channel_sigma(cfg, which)).to(self.device)
+        x *= torch.from_numpy(outlier_multipliers(cfg)).to(self.device)
+        return x.half()
+
+    def fill_on_device(self, chunk: int = 16384):
+        import torch
+        cfg = self.cfg
+        assert len(cfg.tiers) == 1, "device fill: single-tier configs"
+        gen = torch.Generator(device=self.device)
+        gen.manual_seed(1000003 * cfg.seed + 17)
+        for b in range(cfg.batch):
+            n = int(self.lens[b])
+            for t0 in range(0, n, chunk):
+                m = min(chunk, n - t0)
+                k = self.device_draw(gen, 0, cfg.num_kv_heads, m)
+                v = self.device_draw(gen, 1, cfg.num_kv_heads, m)
+                slots = torch.from_numpy(self.maps[0].slots(b, np.arange(t0, t0 + m))).to(self.device)
+                self.caches[0].append(k, v, slots)
+        torch.cuda.synchronize()
 
     def append(self, tier: int, b: int, positions, k: np.ndarray, v: np.ndarray, stream=None):
         """Quantise-and-append host fp16 K/V [n, Hkv, D] at `positions` of sequence b."""
