@@ -182,6 +182,13 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// log2 of a page size that is a power of two, else -1 (the quantize kernels then divide)
+int page_shift_of(int page_size) {
+  for (int s = 0; s < 31; ++s)
+    if ((1 << s) == page_size) return s;
+  return -1;
+}
+
 kvq_status check_tiers(const kvq_tier_view* tiers, int n, int batch, int hq) {
   if (!tiers || n < 1 || n > KVQ_MAX_TIERS || batch < 0 || hq < 1) return KVQ_ERR_INVALID_ARGUMENT;
   const kvq_cache* c0 = tiers[0].cache;
@@ -329,6 +336,7 @@ KVQ_API kvq_status kvq_requantize(const kvq_cache* src, const int32_t* src_slots
   p.num_tokens = num_tokens;
   p.hkv = dst->num_kv_heads;
   p.page_size = dst->page_size;
+  p.page_shift = page_shift_of(dst->page_size);
   p.num_slots = dst->num_pages * dst->page_size;
   p.kind_first = 0;
   p.num_kinds = 2;
@@ -364,6 +372,7 @@ KVQ_API kvq_status kvq_quantize_append(const kvq_cache* cache, const uint16_t* k
   p.num_tokens = num_tokens;
   p.hkv = c->num_kv_heads;
   p.page_size = c->page_size;
+  p.page_shift = page_shift_of(c->page_size);
   p.num_slots = c->num_pages * c->page_size;
   p.kind_first = k ? 0 : 1;
   p.num_kinds = (k && v) ? 2 : 1;

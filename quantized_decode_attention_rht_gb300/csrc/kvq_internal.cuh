@@ -35,6 +35,7 @@ struct QuantParams {
   QuantSide side[2];
   const int32_t* slots;
   int num_tokens, hkv, page_size, num_slots;
+  int page_shift;             // log2(page_size) when it is a power of two, else -1
   int kind_first, num_kinds;  // kinds present: [kind_first, kind_first + num_kinds)
   long long num_vectors;      // num_kinds * num_tokens * hkv
   // re-encode of stored fp16 rows (kvq_requantize) instead of new vectors: the source

@@ -3,9 +3,9 @@
 // Each thread holds kCoords = 32 coordinates of one vector (D / 32 neighbouring lanes per vector).
 // Steps per vector, as on the pages:
 //   1. multiply by the Rademacher signs (a flip of the fp16 sign bit), then the
-//      Walsh-Hadamard butterflies in registers with packed f32x2 adds, and log2(D / 32)
-//      stages across lanes with shuffles (AdapTQ page, "The Math Fix"; VeloxQuant-MLX page,
-//      "Stage 1");
+//      Walsh-Hadamard butterflies, all in registers with packed f32x2 adds: five stages on
+//      strided runs of the vector, one transpose through shared memory, the remaining
+//      log2(D / 32) stages (AdapTQ page, "The Math Fix"; VeloxQuant-MLX page, "Stage 1");
 //   2. codebook format: norm of the rotated vector, fp16 norm, u = sqrt(D) y / ||y||, the
 //      index of u's centroid cell, little-endian bit packing (VeloxQuant-MLX page, "Stage 2"
 //      and "The Bit-Packing Problem"); fp16 / fp8 E4M3 / INT4-g32 formats: the rotated vector
@@ -22,6 +22,7 @@
 // it launches.)
 #pragma once
 #include <algorithm>
+#include <atomic>
 
 #include "kvq_internal.cuh"
 
@@ -235,55 +236,94 @@ __device__ __forceinline__ void residual_sketch(const float* __restrict__ proj, 
   }
 }
 
-// One vector's TPV lanes: sub-part `sub` holds coordinates [sub * kE, (sub + 1) * kE) of
-// the vector, read from src (fp16).  Rotates, encodes and stores it.
-template <int TPV, int kE, int FMT, int BITS>
-__device__ __forceinline__ void quantize_vector(const QuantParams& p, const QuantSide& side, const Table& table,
-                                                const uint16_t* src, int token, int h, int sub, unsigned gmask) {
-  constexpr int D = kE * TPV;
-  constexpr float inv_sqrt_d = inv_sqrt_dim(D);
-  constexpr float sqrt_d = sqrt_dim(D);
-  const int slot = p.slots[token];
-  const bool store = slot >= 0 && slot < p.num_slots;
+// ---------------------------------------------------------------- rotation
+// The Walsh-Hadamard transform of D = 32 TPV points is a product of one butterfly stage per
+// index bit, and the stages commute, so they may run in any order.  Thread `sub` of a
+// vector first loads the runs of R = 32 / TPV coordinates at 32k + R sub (k < TPV): its 32
+// values then span every value of index bits 0 .. log2(R) - 1 and log2(R) + log2(TPV) .. ,
+// i.e. five of the stages run in its registers.  One transpose through shared memory hands
+// thread `sub` the 32 neighbouring coordinates [32 sub, 32 sub + 32), which span the
+// remaining log2(TPV) bits: their stages run in registers too, and the result sits where the
+// encoders expect it.  No cross-lane shuffle is involved.
+//
+// The transpose area of a vector is D floats in 16-byte chunks, 8 chunks to a 128-byte row
+// (row = index bits 5.., chunk column = bits 2..4).  Column c of row r is stored at column
+// c ^ swz(r, v) (v: the vector's position in its warp), which keeps both the writes (one row,
+// TPV threads) and the reads (TPV rows, one column each) of every quarter-warp on eight
+// different 16-byte bank groups.
+template <int TPV>
+__device__ __forceinline__ uint32_t swz(int row, int v) {
+  if constexpr (TPV == 8) return (uint32_t)row;                  // one vector per quarter-warp
+  else if constexpr (TPV == 4) return (uint32_t)(row ^ (5 * (v & 1)));  // two
+  else return (uint32_t)((4 * row) ^ (v & 3));                   // four (TPV == 2)
+}
 
-  // ---- kE fp16 coordinates and their signs; y = s * x
-  float y[kE];
-  {
-    const uint4* sg = reinterpret_cast<const uint4*>(side.signs + (size_t)h * D + sub * kE);
-    uint32_t xw[kE / 2];
-    uint4 ss[kE / 16];
+// Sign bytes of the thread's 32 coordinates, in the order the loads below use (32 bytes:
+// run k, offset r at byte k R + r).
+template <int TPV>
+__device__ __forceinline__ void load_signs(const int8_t* signs_h, int sub, uint32_t (&sw)[8]) {
+  constexpr int R = 32 / TPV;
 #pragma unroll
-    for (int i = 0; i < kE / 8; ++i) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + i);
-      xw[4 * i] = u.x;
-      xw[4 * i + 1] = u.y;
-      xw[4 * i + 2] = u.z;
-      xw[4 * i + 3] = u.w;
-    }
-#pragma unroll
-    for (int i = 0; i < kE / 16; ++i) ss[i] = __ldg(sg + i);
-    const uint32_t* sw = reinterpret_cast<const uint32_t*>(ss);
-#pragma unroll
-    for (int k = 0; k < kE / 2; ++k) {
-      // sign bytes 2k, 2k+1 (int8 +-1: bit 7 set for -1) -> fp16 sign bits 15, 31
-      const uint32_t m = __byte_perm(sw[k >> 1], 0, (k & 1) ? 0x3424 : 0x1404) & 0x80008000u;
-      const uint32_t xv = xw[k] ^ m;
-      const __half2 h2 = *reinterpret_cast<const __half2*>(&xv);
-      y[2 * k] = __low2float(h2);
-      y[2 * k + 1] = __high2float(h2);
+  for (int k = 0; k < TPV; ++k) {
+    const int8_t* src = signs_h + 32 * k + R * sub;
+    if constexpr (R == 4) {
+      sw[k] = __ldg(reinterpret_cast<const uint32_t*>(src));
+    } else if constexpr (R == 8) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+      sw[2 * k] = u.x;
+      sw[2 * k + 1] = u.y;
+    } else {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+      sw[4 * k] = u.x;
+      sw[4 * k + 1] = u.y;
+      sw[4 * k + 2] = u.z;
+      sw[4 * k + 3] = u.w;
     }
   }
-  // ---- Walsh-Hadamard: stage 1 in scalar, stages 2.. on f32x2 pairs, then across lanes
+}
+
+// y = H (s * x) (unnormalised) of one vector: thread `sub` ends with coordinates
+// [32 sub, 32 sub + 32) in y.  xv: the vector's fp16 coordinates; area: the vector's shared
+// transpose area; vw: the vector's position in its warp.
+template <int TPV>
+__device__ __forceinline__ void load_rotate(const uint16_t* xv, const uint32_t (&sw)[8], uint32_t area, int sub,
+                                            int vw, unsigned gmask, float (&y)[32]) {
+  constexpr int R = 32 / TPV;
+  uint32_t xw[16];
 #pragma unroll
-  for (int e = 0; e < kE; e += 2) {
-    const float a = y[e], c = y[e + 1];
-    y[e] = a + c;
-    y[e + 1] = a - c;
+  for (int k = 0; k < TPV; ++k) {
+    const uint16_t* src = xv + 32 * k + R * sub;
+    if constexpr (R == 4) {
+      const uint2 u = __ldcs(reinterpret_cast<const uint2*>(src));
+      xw[2 * k] = u.x;
+      xw[2 * k + 1] = u.y;
+    } else {
+#pragma unroll
+      for (int i = 0; i < R / 8; ++i) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+        xw[(k * R) / 2 + 4 * i] = u.x;
+        xw[(k * R) / 2 + 4 * i + 1] = u.y;
+        xw[(k * R) / 2 + 4 * i + 2] = u.z;
+        xw[(k * R) / 2 + 4 * i + 3] = u.w;
+      }
+    }
   }
+  // signs: bytes 2j, 2j+1 (int8 +-1, bit 7 set for -1) -> fp16 sign bits 15, 31 of pair j;
+  // the first stage (index bit 0, a pair's two halves) in scalar
 #pragma unroll
-  for (int hs = 2; hs < kE; hs <<= 1) {
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t m = __byte_perm(sw[j >> 1], 0, (j & 1) ? 0x3424 : 0x1404) & 0x80008000u;
+    const uint32_t xs = xw[j] ^ m;
+    const __half2 h2 = *reinterpret_cast<const __half2*>(&xs);
+    const float a = __low2float(h2), c = __high2float(h2);
+    y[2 * j] = a + c;
+    y[2 * j + 1] = a - c;
+  }
+  // the other four register stages on f32x2 pairs
 #pragma unroll
-    for (int e = 0; e < kE; e += 2) {
+  for (int hs = 2; hs < 32; hs <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
       if ((e & hs) == 0) {
         const u64 a = pk(y[e], y[e + 1]), c = pk(y[e + hs], y[e + hs + 1]);
         upk(add2(a, c), y[e], y[e + 1]);
@@ -291,15 +331,57 @@ __device__ __forceinline__ void quantize_vector(const QuantParams& p, const Quan
       }
     }
   }
+  // transpose: run k (coordinates 32k + R sub ..) to row k, columns (R/4) sub ..; then read
+  // row sub
+  __syncwarp(gmask);  // the group's reads of the previous vector are done
 #pragma unroll
-  for (int m = 1; m < TPV; m <<= 1) {
-    const float sgn = (sub & m) ? -1.0f : 1.0f;  // upper lane keeps partner - own
+  for (int k = 0; k < TPV; ++k) {
 #pragma unroll
-    for (int e = 0; e < kE; ++e) y[e] = fmaf(sgn, y[e], __shfl_xor_sync(gmask, y[e], m, TPV));
+    for (int q = 0; q < R / 4; ++q) {
+      const uint32_t col = ((uint32_t)((R / 4) * sub + q)) ^ swz<TPV>(k, vw);
+      const int e = k * R + 4 * q;
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(area + 16u * (8u * k + col)), "f"(y[e]),
+                   "f"(y[e + 1]), "f"(y[e + 2]), "f"(y[e + 3])
+                   : "memory");
+    }
   }
+  __syncwarp(gmask);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t col = (uint32_t)j ^ swz<TPV>(sub, vw);
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(y[4 * j]), "=f"(y[4 * j + 1]), "=f"(y[4 * j + 2]), "=f"(y[4 * j + 3])
+                 : "r"(area + 16u * (8u * sub + col))
+                 : "memory");
+  }
+  // stages of index bits log2(R) .. 4 (the vector's TPV rows)
+#pragma unroll
+  for (int hs = R; hs < 32; hs <<= 1) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      if ((e & hs) == 0) {
+        const u64 a = pk(y[e], y[e + 1]), c = pk(y[e + hs], y[e + hs + 1]);
+        upk(add2(a, c), y[e], y[e + 1]);
+        upk(sub2(a, c), y[e + hs], y[e + hs + 1]);
+      }
+    }
+  }
+}
+
+// One vector's TPV lanes: y holds coordinates [sub * kE, (sub + 1) * kE) of the rotated
+// vector H s x (unnormalised).  Encodes and stores it.
+template <int TPV, int kE, int FMT, int BITS>
+__device__ __forceinline__ void quantize_vector(const QuantParams& p, const QuantSide& side, const Table& table,
+                                                float (&y)[kE], int token, int h, int sub, unsigned gmask) {
+  constexpr int D = kE * TPV;
+  constexpr float inv_sqrt_d = inv_sqrt_dim(D);
+  constexpr float sqrt_d = sqrt_dim(D);
+  const int slot = __ldg(p.slots + token);
+  const bool store = slot >= 0 && slot < p.num_slots;
   // y = H s x (unnormalised); the rotated vector is x~ = y / sqrt(D)
   const int slot_c = store ? slot : 0;
-  const size_t prow = ((size_t)(slot_c / p.page_size) * p.hkv + h) * p.page_size + (slot_c % p.page_size);
+  const int page = p.page_shift >= 0 ? slot_c >> p.page_shift : slot_c / p.page_size;
+  const size_t prow = ((size_t)page * p.hkv + h) * p.page_size + (slot_c - page * p.page_size);
   uint8_t* row = side.rows + prow * side.row_bytes;
 
   if constexpr (FMT == F_CB || FMT == F_CBQ) {
@@ -412,22 +494,36 @@ constexpr long long kSmallMaxVectors = 1 << 14;
 
 // Every vector of one side (kind) that falls to this block (grid-stride over vectors).
 template <int TPV, int FMT, int BITS>
-__device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Table& table, float2* cells) {
+__device__ __forceinline__ void quantize_side(const QuantParams& p, int kind, Table& table, float2* cells,
+                                              uint32_t xpose) {
   constexpr int kE = kCoords, D = kE * TPV, VPB = kThreads / TPV;
   const QuantSide& side = p.side[kind];
   if constexpr (FMT == F_CB || FMT == F_CBQ)
     build_table(table, cells, side.bounds, side.centroids, (1 << BITS) - 1, D);
-  const int lane = threadIdx.x & 31, sub = lane % TPV;
+  const int lane = threadIdx.x & 31, sub = lane % TPV, vw = lane / TPV;
   const unsigned gmask = (TPV == 32 ? 0xFFFFFFFFu : ((1u << TPV) - 1u)) << (lane - sub);
+  const uint32_t area = xpose + (uint32_t)(threadIdx.x / TPV) * (D * 4);
   const int nvec = p.num_tokens * p.hkv;
   const int stride = gridDim.x * VPB;
   const uint16_t* x = p.x[kind];
-  for (int v = blockIdx.x * VPB + threadIdx.x / TPV; v < nvec; v += stride) {
-    const int token = v / p.hkv, h = v - token * p.hkv;
-    // the thread's 128-byte line of its next vector heads for L2 while this one is worked on
-    // (the loads at the top of each vector otherwise wait a full HBM round trip)
+  // with a stride that is a multiple of the kv heads the head stays fixed and the token
+  // advances by stride / hkv: no division in the loop
+  const bool fixed = stride % p.hkv == 0;
+  const int v0 = blockIdx.x * VPB + threadIdx.x / TPV, dt = stride / p.hkv;
+  int token = v0 / p.hkv, h = v0 - token * p.hkv;
+  for (int v = v0; v < nvec; v += stride) {
+    if (!fixed) {
+      token = v / p.hkv;
+      h = v - token * p.hkv;
+    }
+    // the thread's part of its next vector heads for L2 while this one is worked on
     if (v + stride < nvec) prefetch_l2(x + (size_t)(v + stride) * D + sub * kE);
-    quantize_vector<TPV, kE, FMT, BITS>(p, side, table, x + (size_t)v * D + sub * kE, token, h, sub, gmask);
+    uint32_t sw[8];  // (reloaded per vector, from L1: holding them across the loop spills)
+    load_signs<TPV>(side.signs + (size_t)h * D, sub, sw);
+    float y[kE];
+    load_rotate<TPV>(x + (size_t)v * D, sw, area, sub, vw, gmask, y);
+    quantize_vector<TPV, kE, FMT, BITS>(p, side, table, y, token, h, sub, gmask);
+    token += dt;
   }
 }
 
@@ -438,24 +534,55 @@ constexpr int blocks_per_sm(int f0, int f1) {
 }
 
 // Side slot blockIdx.y: (F0, B0) for slot 0, (F1, B1) for slot 1; kind = kind_first + slot.
+// Dynamic shared memory of a block: the decision cells (when a side is coded), then the
+// transpose areas of its vectors (32 floats a thread).
+constexpr int kXposeBytes = kThreads * kCoords * 4;
+template <int F0, int F1>
+__host__ __device__ constexpr int quant_smem() {
+  return ((F0 == F_CB || F0 == F_CBQ || F1 == F_CB || F1 == F_CBQ) ? kCellBytes : 0) + kXposeBytes;
+}
+
 template <int TPV, int F0, int B0, int F1, int B1>
 __global__ void __launch_bounds__(kThreads, blocks_per_sm(F0, F1)) quantize_kernel(const QuantParams p) {
   __shared__ Table table;
-  extern __shared__ float2 cells[];  // kCellBytes when a side is coded, else none
-  if (blockIdx.y == 0) quantize_side<TPV, F0, B0>(p, p.kind_first, table, cells);
-  else quantize_side<TPV, F1, B1>(p, p.kind_first + 1, table, cells);
+  extern __shared__ __align__(16) float2 cells[];
+  const uint32_t xpose =
+      static_cast<uint32_t>(__cvta_generic_to_shared(cells)) + (uint32_t)(quant_smem<F0, F1>() - kXposeBytes);
+  if (blockIdx.y == 0) quantize_side<TPV, F0, B0>(p, p.kind_first, table, cells, xpose);
+  else quantize_side<TPV, F1, B1>(p, p.kind_first + 1, table, cells, xpose);
 }
 
 template <int TPV, int F0, int B0, int F1, int B1>
 cudaError_t launch_q(const QuantParams& p, int sides, int sms, cudaStream_t stream) {
   constexpr int VPB = kThreads / TPV;
+  constexpr int smem = quant_smem<F0, F1>();
+  auto kern = quantize_kernel<TPV, F0, B0, F1, B1>;
+  static std::atomic<bool> configured[64];  // shared-memory limit raised on this device (a racing
+                                           // second raise is harmless)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev].store(true, std::memory_order_relaxed);
+  }
   const long long nvec = (long long)p.num_tokens * p.hkv;
   const long long need = (nvec + VPB - 1) / VPB;
-  const unsigned blocks =
-      (unsigned)std::max<long long>(1, std::min<long long>(need, (long long)sms * blocks_per_sm(F0, F1) / sides));
-  constexpr bool coded = F0 == F_CB || F0 == F_CBQ || F1 == F_CB || F1 == F_CBQ;
-  quantize_kernel<TPV, F0, B0, F1, B1><<<dim3(blocks, sides), kThreads, coded ? kCellBytes : 0, stream>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  long long blocks = std::max<long long>(1, std::min<long long>(need, (long long)sms * blocks_per_sm(F0, F1) / sides));
+  // a grid stride (blocks * VPB vectors) that is a multiple of the kv heads keeps every
+  // thread on one head, so it loads that head's signs once
+  long long per = p.hkv;
+  for (long long a = VPB, b = per; b;) {  // per = hkv / gcd(VPB, hkv)
+    const long long t = a % b;
+    a = b;
+    b = t;
+    if (!b) per = p.hkv / a;
+  }
+  if (blocks >= per) blocks = blocks / per * per;
+  kern<<<dim3((unsigned)blocks, sides), kThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }
