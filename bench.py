@@ -38,24 +38,26 @@ sys.path.insert(0, ROOT)
 METRIC = "quantized-KV decode attention GB/s & frac of HBM peak; quantize vectors/s"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
-# kernel, from one ncu capture of the same kernel source (sha256 prefix).  The gqa32k
-# capture ran at batch 4 (every sequence has the same length, so traffic grows in
-# proportion to the batch) and is scaled by 32 / 4.  A changed source reports null.
+# kernel, from one ncu capture of the same kernel source (sha256 prefix) on the full-size
+# workload.  Reported only for that source and that batch: the split-K partials (the write
+# side) do not grow with the batch, so the figure does not scale to other sizes.
 TRAFFIC = {
     "gqa32k": {"kernel": "decode_gqa_kernel", "source": "quantized_decode_attention_rht_gb300/csrc/decode_gqa.cu",
-               "sha256": "11b4d50901ffc752", "captured_batch": 4, "bytes": 242705408 + 15922176},
+               "sha256": "418fede5a25264f9", "captured_batch": 32, "bytes": 1941790208 + 21282304},
 }
 
 
 def kernel_traffic(config: str, batch: int):
     import hashlib
     t = TRAFFIC.get(config)
-    if t is None:
+    if t is None or batch != t["captured_batch"]:
         return None
     with open(os.path.join(ROOT, t["source"]), "rb") as f:
         if hashlib.sha256(f.read()).hexdigest()[:16] != t["sha256"]:
             return None
-    return t["bytes"] * batch / t["captured_batch"]
+    return t["bytes"]
+
+
 PEAK_FALLBACK_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth (the ~8 TB/s the targets are quoted against)
 
