@@ -24,6 +24,14 @@ constexpr int kWarps = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- storage formats
+// 2^x, x <= 0 or -inf (scores in base-2 units relative to a maximum): the hardware
+// approximation (relative error below 2^-22), results below 2^-126 flushed to 0.
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int BITS>
 struct Codebook {
   static constexpr int bits = BITS;
@@ -230,13 +238,13 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 #pragma unroll
         for (int o = LPT; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
         if (mx > m[g]) {
-          const float f = exp2f(m[g] - mx);  // m = -inf first: f = 0
+          const float f = exp2_fast(m[g] - mx);  // m = -inf first: f = 0
           l[g] *= f;
 #pragma unroll
           for (int j = 0; j < DPL; ++j) acc[g][j] *= f;
           m[g] = mx;
         }
-        pr[g] = valid ? exp2f(sc[g] - m[g]) : 0.f;
+        pr[g] = valid ? exp2_fast(sc[g] - m[g]) : 0.f;
         l[g] += pr[g];
         if (track && valid) mn[g] = fminf(mn[g], sc[g]);
       }
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       if (w_m[w][g] == -INFINITY) continue;  // a warp that saw no token
-      const float f = exp2f(w_m[w][g] - mx);
+      const float f = exp2_fast(w_m[w][g] - mx);
       a += w_acc[w][g][j] * f;
       s += w_l[w][g] * f;
     }
@@ -416,7 +424,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecPa
   __syncthreads();  // s_red is reused below
   for (int s = threadIdx.x; s < n; s += blockDim.x) {
     const float m = s_w[s];
-    const float f = m == -INFINITY ? 0.f : exp2f(m - mx);  // a split that saw no token: 0
+    const float f = m == -INFINITY ? 0.f : exp2_fast(m - mx);  // a split that saw no token: 0
     lsum = fmaf(p.ws_ml[2 * (base + s_part[s]) + 1], f, lsum);
     s_w[s] = f;
   }

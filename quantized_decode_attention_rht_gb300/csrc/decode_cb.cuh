@@ -430,6 +430,14 @@ struct Ring {
   bool lost;             // a slot wait gave up
 };
 
+// 2^x, x <= 0 or -inf (scores in base-2 units relative to the running maximum): the
+// hardware approximation (relative error below 2^-22), results below 2^-126 flushed to 0.
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Issues the copies of page `phys`.  A block-table entry outside the pool (warp-uniform
 // test, which also catches negative entries) is never read through: page 0 is copied in its
 // place (the host gives a pool without pages no work) and the call reports the entry.
@@ -752,15 +760,15 @@ struct Path1 {
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
       }
       if (mt > m) {
-        const float f = exp2f(m - mt);  // m = -inf at first: f = 0
+        const float f = exp2_fast(m - mt);  // m = -inf at first: f = 0
         l *= f;
         const u64 f2 = pk2(f, f);
 #pragma unroll
         for (int j = 0; j < NP; ++j) acc[j] = mul2(acc[j], f2);
         m = mt;
       }
-      const float p0 = v0 ? exp2f(x0 - m) : 0.f;
-      const float p1 = v1 ? exp2f(x1 - m) : 0.f;
+      const float p0 = v0 ? exp2_fast(x0 - m) : 0.f;
+      const float p1 = v1 ? exp2_fast(x1 - m) : 0.f;
       l += p0 + p1;
       if (p.track) {
         float lo = fminf(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY);
@@ -1043,7 +1051,7 @@ struct PathM {
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
       }
       if (mt > m) {
-        const float f = exp2f(m - mt);  // m = -inf at first: f = 0
+        const float f = exp2_fast(m - mt);  // m = -inf at first: f = 0
         l *= f;
 #pragma unroll
         for (int a = 0; a < KS; ++a)
@@ -1051,8 +1059,8 @@ struct PathM {
           for (int kk = 0; kk < 4; ++kk) acc[a][kk] *= f;
         m = mt;
       }
-      const float p0 = v0 ? exp2f(x0 - m) : 0.f;
-      const float p1 = v1 ? exp2f(x1 - m) : 0.f;
+      const float p0 = v0 ? exp2_fast(x0 - m) : 0.f;
+      const float p1 = v1 ? exp2_fast(x1 - m) : 0.f;
       l += p0 + p1;
       if (p.track) {
         float lo = fminf(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY);

@@ -115,6 +115,14 @@ __device__ __forceinline__ uint32_t split_pair(float x, float y, float hl) {
   return pack_f16x2(rx, ry);
 }
 
+// 2^x, x <= 0 or -inf (scores in base-2 units relative to the running maximum): the
+// hardware approximation (relative error below 2^-22), results below 2^-126 flushed to 0.
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Lowest score of head c over the page's 16 tokens (lanes g = 0..7 of the same c).
 __device__ __forceinline__ float page_min(float a, float b) {
   float v = fminf(a, b);
@@ -310,11 +318,11 @@ struct Far {
       mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
     }
     if (mt > s.m) {
-      rescale(s, exp2f(s.m - mt));  // first tile: exp2(-inf) = 0
+      rescale(s, exp2_fast(s.m - mt));  // first tile: exp2(-inf) = 0
       s.m = mt;
     }
-    const float p0 = v0 ? exp2f(x0 - s.m) : 0.f;
-    const float p1 = v1 ? exp2f(x1 - s.m) : 0.f;
+    const float p0 = v0 ? exp2_fast(x0 - s.m) : 0.f;
+    const float p1 = v1 ? exp2_fast(x1 - s.m) : 0.f;
     s.l += p0 + p1;
     if (track) s.mn = fminf(s.mn, page_min(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY));
     // score gate: every token of the page, for every live head, far below the running max
@@ -495,7 +503,7 @@ struct Near {
       mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
     }
     if (mt > s.m) {
-      const float f = exp2f(s.m - mt);
+      const float f = exp2_fast(s.m - mt);
       s.l *= f;
 #pragma unroll
       for (int a = 0; a < 8; ++a)
@@ -503,8 +511,8 @@ struct Near {
         for (int k = 0; k < 4; ++k) s.acc[a][k] *= f;
       s.m = mt;
     }
-    const float p0 = v0 ? exp2f(x0 - s.m) : 0.f;
-    const float p1 = v1 ? exp2f(x1 - s.m) : 0.f;
+    const float p0 = v0 ? exp2_fast(x0 - s.m) : 0.f;
+    const float p1 = v1 ? exp2_fast(x1 - s.m) : 0.f;
     s.l += p0 + p1;
     if (track) s.mn = fminf(s.mn, page_min(v0 ? x0 : INFINITY, v1 ? x1 : INFINITY));
     if (gate && __all_sync(kFull, !live || mt - s.m < -kGateLog2)) return;  // score gate (see Far)
