@@ -71,6 +71,8 @@ def parse_args():
     ap.add_argument("--config", default="gqa32k")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per GPU (default: the workload's); smaller cases for profiling")
+    ap.add_argument("--head-dim", type=int, default=0, help="reshape the workload's layer (64, 128 or 256)")
+    ap.add_argument("--num-kv-heads", type=int, default=0, help="reshape the workload's kv heads (query heads kept)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-configs", action="store_true",
                     help="skip the llama7b / ragged / append measurements added to the line")
@@ -281,12 +283,18 @@ def barrier(ws: int):
 # ----------------------------------------------------------------------------- workload
 
 
-def rank_config(name: str, rank: int, batch: int = 0):
-    """Each rank holds its own batch of sequences (weak scaling): same shapes, its own seed."""
+def rank_config(name: str, rank: int, batch: int = 0, head_dim: int = 0, num_kv_heads: int = 0):
+    """Each rank holds its own batch of sequences (weak scaling): same shapes, its own seed.
+    head_dim / num_kv_heads (0: the workload's) reshape the layer, e.g. to time the shapes
+    the fused kernels leave to the generic one (head_dim 64, 8 query heads per kv head)."""
     import workloads as W
     cfg = W.CONFIGS[name]
     if batch:
         cfg = cfg.scaled(batch=batch)
+    if head_dim:
+        cfg = cfg.scaled(head_dim=head_dim)
+    if num_kv_heads:
+        cfg = cfg.scaled(num_kv_heads=num_kv_heads)
     return cfg if rank == 0 else cfg.scaled(seed=cfg.seed + 1000 * rank)
 
 
@@ -797,7 +805,7 @@ def run_ours(args):
     kvq.lib()
     if args.config == "append":
         return run_append_main(args, kvq, torch, ws, rank)
-    cfg = rank_config(args.config, rank, args.batch)
+    cfg = rank_config(args.config, rank, args.batch, args.head_dim, args.num_kv_heads)
     wl = W.GpuWorkload(cfg)
     views = wl.views()
     last = len(cfg.tiers) - 1

@@ -153,13 +153,17 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
       // best at 72 items per SM, 3/2-bit G = 4 at 288, the fp16 / fp8 kernel at 64)
       const size_t fb = family_bytes[kind];
       const size_t per_sm = kind == TIER_GQA ? 64 : (group >= 2 ? 288 : 72);
-      const size_t item_bytes = std::max<size_t>(16 << 10, fb / (kSms * per_sm));
+      // a group of 8 on the fused kernels makes two items per chunk (heads 0-3 and 4-7):
+      // chunks twice as long keep the item count
+      const size_t halves = group == 8 ? 2 : 1;
+      const size_t item_bytes = std::max<size_t>(16 << 10, halves * fb / (kSms * per_sm));
       size_t tok = item_bytes / token_bytes(tiers[i].cache);
       // the tensor-core path's time per token hardly depends on the code width, so its small
       // caches get items of a fixed token count rather than bytes (measured on GB300 for
       // 4/4- and 3/2-bit codes: 96-112 tokens best for 4 query heads per kv head, 192 for 2)
       if (kind == TIER_CB && group >= 2)
-        tok = std::max<size_t>(group == 4 ? 112 : 192, fb / (kSms * per_sm) / token_bytes(tiers[i].cache));
+        tok = std::max<size_t>(group >= 4 ? 112 * halves : 192,
+                               halves * fb / (kSms * per_sm) / token_bytes(tiers[i].cache));
       const size_t cap = kind == TIER_GQA ? (size_t)gqa_max_chunk_tokens() : (size_t)1 << 20;
       chunk = (int)std::min<size_t>(cap, std::max<size_t>(ps, tok / ps * ps));
     } else if (chunk == 0) {

@@ -8,6 +8,8 @@ namespace kvq {
 constexpr size_t PS_TOKENS = 16;  // tokens per page on the codebook path
 
 bool cb_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
+  if (group == 8)  // plain codes: the 4-head instances, two items per chunk
+    return (head_dim == 128 || head_dim == 256) && v_fmt == KVQ_FMT_CODEBOOK && k_fmt == KVQ_FMT_CODEBOOK;
   return (head_dim == 128 || head_dim == 256) && (group == 1 || group == 2 || group == 4) &&
          v_fmt == KVQ_FMT_CODEBOOK &&
          (k_fmt == KVQ_FMT_CODEBOOK || k_fmt == KVQ_FMT_CODEBOOK_OUTLIER ||
@@ -28,7 +30,7 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
   for (int i = 0; i < dp.num_tiers; ++i)
     if (dp.tier[i].kind == TIER_CB) cb_bytes += (size_t)dp.batch * dp.hkv * dp.tier[i].max_pages * PS_TOKENS *
                                                 (dp.tier[i].k_row_bytes + dp.tier[i].v_row_bytes);
-  const bool wide = cb_bytes >= ((size_t)512 << 20);
+  const bool wide = cb_bytes >= ((size_t)512 << 20);  // (8 heads per kv head: the same rule)
   for (int i = 0; i < dp.num_tiers; ++i) {
     const DecTier& t = dp.tier[i];
     if (t.kind != TIER_CB) continue;
@@ -62,7 +64,7 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
     p.hq = dp.hq;
     p.hkv = dp.hkv;
     p.total_splits = dp.total_splits;
-    p.total_items = dp.batch * dp.hkv * t.num_splits;
+    p.total_items = dp.batch * dp.hkv * t.num_splits * (group == 8 ? 2 : 1);
     if (p.total_items == 0) continue;
     // run alongside the previous split-K grid, unless the projection (whose output this
     // launch reads) is what precedes it
@@ -74,7 +76,8 @@ cudaError_t launch_decode_cb(const DecParams& dp, int head_dim, int* counters, c
       projected = true;
       p.pdl = 0;
     }
-    if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL) e = cbk::launch_cb_qjl(p, group, t.k_bits, t.v_bits, sms, stream);
+    if (group == 8) e = cbk::launch_cb_g8(p, head_dim, wide, t.k_bits, t.v_bits, sms, stream);
+    else if (t.k_fmt == KVQ_FMT_CODEBOOK_QJL) e = cbk::launch_cb_qjl(p, group, t.k_bits, t.v_bits, sms, stream);
     else if (t.k_fmt == KVQ_FMT_CODEBOOK_OUTLIER)
       e = cbk::launch_cb_outlier(p, head_dim, group, t.k_bits, t.v_bits, sms, stream);
     else if (head_dim == 128 && group >= 2 && wide)

@@ -348,11 +348,12 @@ __device__ __forceinline__ void token_pairs(const uint32_t (&a)[NW], const uint3
 
 // ---------------------------------------------------------------- query rotation
 
-// q' = H (s_K * q) * log2(e) / D * 2^6 for the G heads of kv head hk into qbuf[G][D].
+// q' = H (s_K * q) * log2(e) / D * 2^6 for heads h0 .. h0 + G - 1 of kv head hk (GQ query heads
+// per kv head) into qbuf[G][D].
 // Lane l holds coordinates [l*D/32, (l+1)*D/32) of one head at a time: in-register
 // butterfly stages, then five across lanes.
-template <int D, int G>
-__device__ __forceinline__ void rotate_query(const CbParams& p, int b, int hk, float* qbuf, int lane) {
+template <int D, int G, int GQ = G>
+__device__ __forceinline__ void rotate_query(const CbParams& p, int b, int hk, int h0, float* qbuf, int lane) {
   constexpr int E = D / 32;
   const int d0 = lane * E;
   const int8_t* sg = p.k_signs + hk * D + d0;
@@ -361,7 +362,7 @@ __device__ __forceinline__ void rotate_query(const CbParams& p, int b, int hk, f
   for (int e = 0; e < E; ++e) s[e] = sg[e];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const __half* qs = p.q + ((size_t)b * p.hq + hk * G + h) * D + d0;
+    const __half* qs = p.q + ((size_t)b * p.hq + hk * GQ + h0 + h) * D + d0;
     float y[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -398,15 +399,21 @@ __device__ __forceinline__ void rotate_query(const CbParams& p, int b, int hk, f
 // A work item: chunk `chunk` of sequence b, kv head hk.  `len` is loaded one item ahead and
 // `btw` holds the block-table entry of page t0/16 + lane of the item.
 struct Item {
-  int b, hk, chunk, t0, len;
+  int b, hk, h0, chunk, t0, len;  // h0: the item's first query head within the kv head's group
   uint32_t btw;
 };
 
+// H8: a group of 8 query heads, two items (heads 0-3, 4-7) per chunk.
+template <bool H8>
 __device__ __forceinline__ Item fetch_item(const CbParams& p, int item, int lane) {
   const CbTier& T = p.t;
   Item it;
   it.chunk = item % T.nchunks;
-  const int rem = item / T.nchunks;
+  int rem = item / T.nchunks;
+  // a group of 8: every chunk of heads 0-3, then every chunk of heads 4-7, so the second
+  // pass over a chunk comes a few items later and finds its pages in L2
+  it.h0 = H8 ? 4 * (rem & 1) : 0;
+  rem = H8 ? rem >> 1 : rem;
   it.hk = rem % p.hkv;
   it.b = rem / p.hkv;
   it.t0 = it.chunk * T.chunk;
@@ -561,7 +568,7 @@ __global__ void __launch_bounds__(128) project_kernel(const __grid_constant__ Cb
   __shared__ __align__(16) float qs[4][G * D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x / p.hkv, hk = blockIdx.x - b * p.hkv;
-  rotate_query<D, G>(p, b, hk, qs[warp], lane);
+  rotate_query<D, G>(p, b, hk, 0, qs[warp], lane);
   __syncwarp();
   const int j = 32 * warp + lane;
   const float4* srow = reinterpret_cast<const float4*>(p.t.qjl + (size_t)j * D);
@@ -600,7 +607,8 @@ template <int D, int KB, int VB, int MODE>
 struct Path1 {
   static constexpr bool QJL = MODE == kModeSketch, OUT = MODE == kModeOutlier;
   using L = Layout<D, 1, KB, VB, D == 128 ? (QJL ? 12 : 16) : 8, MODE>;
-  static constexpr int kD = D, kG = 1;
+  static constexpr int kD = D, kG = 1, kGQ = 1;
+  static constexpr bool kH8 = false;
   static constexpr int SNP = KVQ_QJL_DIM / 8;  // sketch sign pairs per lane and token (a quarter of m)
   static constexpr int DL = D / 4;  // coordinates per lane and token
   static constexpr int NP = DL / 2;  // pair slots per lane and token
@@ -642,7 +650,7 @@ struct Path1 {
     }
 #endif
     fd.top_up(rg);
-    rotate_query<D, 1>(p, b, hk, qbuf, lane);
+    rotate_query<D, 1>(p, b, hk, 0, qbuf, lane);
     __syncwarp();
     u64 q2[NP], acc[NP], p2[QJL ? SNP : 1];
     {
@@ -827,11 +835,14 @@ struct Path1 {
 // ================================================================ G = 2, 4: tensor-core path
 // WIDE: 16 warps instead of 12 (register-limited to 128, a few spilled bytes): more warps
 // hide more of the path's latency on large caches, fewer items per warp hurt small ones.
-template <int D, int G, int KB, int VB, int MODE, bool WIDE = false>
+// H8 (G = 4 only): 8 query heads per kv head, two items per chunk, heads 0-3 and 4-7.
+template <int D, int G, int KB, int VB, int MODE, bool WIDE = false, bool H8 = false>
 struct PathM {
+  static_assert(!H8 || G == 4, "a group of 8 runs as two items of 4 heads");
   static constexpr bool QJL = MODE == kModeSketch, OUT = MODE == kModeOutlier;
   using L = Layout<D, G, KB, VB, D == 128 ? (QJL ? 10 : (WIDE ? 16 : 12)) : 8, MODE>;
-  static constexpr int kD = D, kG = G;
+  static constexpr int kD = D, kG = G, GQ = H8 ? 8 : G, kGQ = GQ;
+  static constexpr bool kH8 = H8;
   static constexpr int SKS = KVQ_QJL_DIM / 16;  // sketch mma k-steps
   static constexpr int KS = D / 16;            // key mma k-steps; also value m-tiles
   static constexpr int PPT = D / 8;            // key pair slots per lane (index c)
@@ -875,6 +886,7 @@ struct PathM {
     const int t1 = min(it.len, it.t0 + T.chunk);
     const int pg0 = it.t0 / PS, npg = item_pages(T, it);
     const int g = lane >> 2, c = lane & 3;
+    const int h0 = H8 ? it.h0 : 0;  // the item's first query head within its kv head's group
     // quad-table lookup base: the table block starts QTAB below the pair table, which is
     // aligned to its size; lane copy (l & 15) at 16-byte steps
     const uint32_t qlane = pin(((vlane & ~(uint32_t)(L::TABLE - 1)) - L::QTAB) | ((lane & 15) << 4));
@@ -889,7 +901,7 @@ struct PathM {
     }
 #endif
     fd.top_up(rg);
-    rotate_query<D, G>(p, b, hk, qbuf, lane);
+    rotate_query<D, G, GQ>(p, b, hk, h0, qbuf, lane);
     __syncwarp();
     // query B fragments: column g = (head g/2, part g%2); pair slots c*PPT + 2ks (+1)
     uint32_t qf[KS][2];
@@ -913,7 +925,7 @@ struct PathM {
       if (hB < G) {
         const float hl = (float)(g & 1);
         const float4* src =
-            reinterpret_cast<const float4*>(p.pq + ((size_t)b * p.hq + hk * G + hB) * KVQ_QJL_DIM + 32 * c);
+            reinterpret_cast<const float4*>(p.pq + ((size_t)b * p.hq + hk * GQ + h0 + hB) * KVQ_QJL_DIM + 32 * c);
 #pragma unroll
         for (int ks = 0; ks < SKS; ++ks) {
           const float4 v = src[ks];
@@ -928,7 +940,7 @@ struct PathM {
     float qo[OUT ? KVQ_OUTLIER_CHANNELS : 1];  // outlier stream: q[c_j] of head c, score units
     if constexpr (OUT) {
       const int32_t* ch = T.outl + hk * KVQ_OUTLIER_CHANNELS;
-      const __half* qrow = p.q + ((size_t)b * p.hq + hk * G + (c < G ? c : 0)) * D;
+      const __half* qrow = p.q + ((size_t)b * p.hq + hk * GQ + h0 + (c < G ? c : 0)) * D;
 #pragma unroll
       for (int j = 0; j < KVQ_OUTLIER_CHANNELS; ++j)
         qo[j] = c < G ? __half2float(qrow[__ldg(ch + j) & (D - 1)]) * OutlierScale<D>::v : 0.f;
@@ -1126,7 +1138,7 @@ struct PathM {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(kFull, l, o);
     if (c < G) {
-      const size_t part = ((size_t)b * p.hq + hk * G + c) * p.total_splits + T.split_begin + it.chunk;
+      const size_t part = ((size_t)b * p.hq + hk * GQ + h0 + c) * p.total_splits + T.split_begin + it.chunk;
       constexpr float unw = 1.0f / (kWScale * kCScale);
       float4* dst = reinterpret_cast<float4*>(p.ws_acc + part * D + 2 * QPT * g);
 #pragma unroll
@@ -1185,7 +1197,7 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
   }
   item = __shfl_sync(kFull, item, 0);
   next = __shfl_sync(kFull, next, 0);
-  Item cur = fetch_item(p, item < p.total_items ? item : 0, lane);
+  Item cur = fetch_item<P::kH8>(p, item < p.total_items ? item : 0, lane);
   while (item < p.total_items) {
     // a warp whose slot wait gave up keeps taking items but writes empty partials for
     // them: every item gets a partial even if every warp gave up
@@ -1194,8 +1206,9 @@ __global__ void __launch_bounds__(P::L::WARPS * 32, 1) decode_cb_kernel(const __
     const bool has_next = next < p.total_items;
     Item nx = cur;
     if (has_next) {
-      nx = fetch_item(p, next, lane);
-      const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q + ((size_t)nx.b * p.hq + nx.hk * P::kG) * P::kD);
+      nx = fetch_item<P::kH8>(p, next, lane);
+      const uint8_t* qrow =
+          reinterpret_cast<const uint8_t*>(p.q + ((size_t)nx.b * p.hq + nx.hk * P::kGQ + nx.h0) * P::kD);
       if (lane < L::QLINES) prefetch_l2(qrow + 128 * lane);
     }
     // after a wait gave up, the items the warp still takes run to an empty partial at once
@@ -1278,6 +1291,7 @@ cudaError_t launch_kb(const CbParams& p, int kb, int vb, int sms, cudaStream_t s
   }
 }
 
+// A group of 8 runs the 4-head instances, two items per chunk (CbParams::halves).
 template <int D, int MODE>
 cudaError_t launch_g(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s) {
   switch (g) {
@@ -1287,6 +1301,9 @@ cudaError_t launch_g(const CbParams& p, int g, int kb, int vb, int sms, cudaStre
   }
 }
 
+// Plain codes with 8 query heads per kv head (head_dim 128 or 256; `wide`: the 16-warp
+// instances at head_dim 128): instantiated in decode_cb_g8.cu.
+cudaError_t launch_cb_g8(const CbParams& p, int d, bool wide, int kb, int vb, int sms, cudaStream_t s);
 // Keys with a residual sketch (head_dim 128): instantiated in decode_cb_qjl.cu.
 cudaError_t launch_cb_qjl(const CbParams& p, int g, int kb, int vb, int sms, cudaStream_t s);
 // p' = S q' of every query head into p.pq (batch * hkv blocks), before the sketched tiers.

@@ -1,4 +1,4 @@
-// Fused decode attention for groups of 1, 2 or 4 query heads per kv head, head_dim 128, over
+// Fused decode attention for groups of 1, 2, 4 or 8 query heads per kv head, head_dim 128, over
 // fp16 tiers (FoveatedKV near tier, or a recent-token window) and fp8-E4M3-key /
 // INT4-g32-value tiers (far tier), all of them in one launch ("Making it fast", FoveatedKV
 // page: both tiers and the decode buffer in a single dispatch).
@@ -9,7 +9,9 @@
 // by 16 bytes so every fragment load below is free of bank conflicts), and writes one
 // split-K partial (running max, sum, rotated-domain accumulator) per item.
 //
-// The query heads of a kv head (up to G = 4; smaller groups leave zero columns) form a real
+// The query heads of an item (up to G = 4; smaller groups leave zero columns; a group of 8 is
+// two items per chunk, heads 0-3 and 4-7, whose second pass reads the chunk's pages from
+// L2) form a real
 // contraction with every key and value row, done with mma.sync.m16n8k16 (fp16 inputs, fp32
 // accumulation):
 //   scores  S[16 tokens x 8] = K[16 tokens x 128] . Qt[128 x 8]
@@ -34,7 +36,7 @@
 namespace kvq {
 namespace {
 
-constexpr int D = 128, G = 4, PS = 16;  // G: query heads one item can carry (a group of 1, 2 or 4)
+constexpr int D = 128, G = 4, PS = 16;  // G: query heads one item can carry
 constexpr int kWarps = 12;
 constexpr int kWarpSmem = 19360;               // per warp: stage ring + block-table slice
 constexpr int kMaxPagesPerItem = 128;
@@ -155,20 +157,23 @@ struct GqaParams {
   int* counter;
   int* err;       // the call's error word (KVQ_DEVERR_* bits)
   int hq, hkv, total_splits, total_items;
-  int group;        // query heads per kv head (1, 2 or 4); heads group.. of an item are idle
+  int group;        // query heads per kv head (1, 2, 4 or 8)
+  int halves;       // items per chunk: 2 for a group of 8 (heads 0-3, 4-7), else 1
+  int igroup;       // query heads an item carries: min(group, 4); heads igroup.. are idle
   int trigger;      // a codebook split-K launch follows (as a programmatic dependent)
   int gate, spike;  // score-gated value loading; track tier 0's lowest scores
 };
 
 // ---------------------------------------------------------------- per-warp pieces
 
-// q' = H (s_K * q) * log2(e) / D for the 4 heads of kv head hk, into qbuf[4][128] (fp32).
+// q' = H (s_K * q) * log2(e) / D for heads h0 .. h0 + 3 of kv head hk, into qbuf[4][128] (fp32).
 // Lane l holds head l/8, coordinates (l%8)*16 .. +16: four butterfly stages in registers,
 // three across the 8 lanes of the head.
-__device__ __forceinline__ void rotate_query(const GqaParams& p, int b, int hk, float* qbuf, int lane) {
+__device__ __forceinline__ void rotate_query(const GqaParams& p, int b, int hk, int h0, float* qbuf, int lane) {
   const int hh = lane >> 3, d0 = (lane & 7) * 16;
-  const bool live = hh < p.group;  // idle heads get a zero query (zero B columns)
-  const uint4* qs = reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.hq + hk * p.group + (live ? hh : 0)) * D + d0);
+  const bool live = hh < p.igroup;  // idle heads get a zero query (zero B columns)
+  const uint4* qs =
+      reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.hq + hk * p.group + h0 + (live ? hh : 0)) * D + d0);
   uint4 q0 = __ldg(qs), q1 = __ldg(qs + 1);
   if (!live) q0 = q1 = make_uint4(0u, 0u, 0u, 0u);
   const uint4 sg = __ldg(reinterpret_cast<const uint4*>(p.k_signs + hk * D + d0));
@@ -557,9 +562,9 @@ struct Near {
 
 // The partial of an item that contributes nothing (running max -inf, sum 0): what an item
 // with a block-table entry outside the pool leaves, so the combine pass reads no stale data.
-__device__ __noinline__ void empty_partial(const GqaParams& p, const GqaTier& T, int b, int hk, int chunk, int lane,
-                                           bool track) {
-  for (int h = 0; h < p.group; ++h) {
+__device__ __noinline__ void empty_partial(const GqaParams& p, const GqaTier& T, int b, int hk, int h0, int chunk,
+                                           int lane, bool track) {
+  for (int h = h0; h < h0 + p.igroup; ++h) {
     const size_t part = ((size_t)b * p.hq + hk * p.group + h) * p.total_splits + T.split_begin + chunk;
     for (int j = lane; j < D; j += 32) p.ws_acc[part * D + j] = 0.f;
     if (lane == 0) {
@@ -572,8 +577,8 @@ __device__ __noinline__ void empty_partial(const GqaParams& p, const GqaTier& T,
 
 // One work item: pages [t0, t1) of sequence b, kv head hk in tier T.
 template <class TT>
-__device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, int b, int hk, int chunk, int t0,
-                                         int t1, uint8_t* wsm, int lane, bool track) {
+__device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, int b, int hk, int h0, int chunk,
+                                         int t0, int t1, uint8_t* wsm, int lane, bool track) {
   const int g = lane >> 2, c = lane & 3;
   float* qbuf = reinterpret_cast<float*>(wsm);  // the ring is idle between items
   int* btab = reinterpret_cast<int*>(wsm + kBtab);
@@ -585,7 +590,7 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
     page_in_pool(e, T.num_pages, &bits);
     btab[i] = e;
   }
-  rotate_query(p, b, hk, qbuf, lane);  // its loads overlap the block-table loads above
+  rotate_query(p, b, hk, h0, qbuf, lane);  // its loads overlap the block-table loads above
   __syncwarp();
   uint32_t qf[8][2];
   TT::qfrag(qbuf, qf, g, c);
@@ -594,7 +599,7 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
   __syncwarp();  // the ring is reused for stages below
   if (__any_sync(kFull, bits != 0)) {  // a page outside the pool: the item reads nothing
     if (lane == 0) atomicOr(p.err, KVQ_DEVERR_PAGE_INDEX);
-    empty_partial(p, T, b, hk, chunk, lane, track);
+    empty_partial(p, T, b, hk, h0, chunk, lane, track);
     return;
   }
   const uint32_t ring = smem_addr(wsm);
@@ -611,14 +616,14 @@ __device__ __forceinline__ void run_item(const GqaParams& p, const GqaTier& T, i
     __syncwarp();
     const int slot = i % TT::S;
     const int nvalid = min(PS, t1 - (pg0 + i) * PS);
-    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.group);
+    TT::page(wsm + slot * TT::STAGE, nvalid, qf, st, lane, track, p.gate != 0, c < p.igroup);
     __syncwarp();
     if (i + TT::S < npg) TT::issue(T, pl, btab[i + TT::S], hk, p.hkv, ring + slot * TT::STAGE, lane);
     cp_commit();
   }
   cp_wait<0>();
-  const bool live = c < p.group;
-  const size_t part = live ? ((size_t)b * p.hq + hk * p.group + c) * p.total_splits + T.split_begin + chunk : 0;
+  const bool live = c < p.igroup;
+  const size_t part = live ? ((size_t)b * p.hq + hk * p.group + h0 + c) * p.total_splits + T.split_begin + chunk : 0;
   TT::finish(st, p.ws_acc + part * D, p.ws_ml + 2 * part, track ? p.ws_min + part : nullptr, lane, live);
   __syncwarp();
 }
@@ -641,6 +646,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
     int rem = item - T.item_begin;
     const int chunk = rem % T.nchunks;
     rem /= T.nchunks;
+    // a group of 8: every chunk of heads 0-3, then every chunk of heads 4-7, so the second
+    // pass over a chunk comes a few items later and finds its pages in L2
+    const int half = p.halves == 2 ? (rem & 1) : 0;
+    rem = p.halves == 2 ? rem >> 1 : rem;
     const int hk = rem % p.hkv, b = rem / p.hkv;
     int bits = 0;  // a length out of range is cut into it here and reported by the combine pass
     const int len = checked_len(T.seq_lens[b], T.max_pages, PS, &bits);
@@ -648,8 +657,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
     if (t0 < len) {
       const int t1 = min(len, t0 + T.chunk);
       const bool track = p.spike && T.first;
-      if (T.far) run_item<Far>(p, T, b, hk, chunk, t0, t1, wsm, lane, track);
-      else run_item<Near>(p, T, b, hk, chunk, t0, t1, wsm, lane, track);
+      if (T.far) run_item<Far>(p, T, b, hk, 4 * half, chunk, t0, t1, wsm, lane, track);
+      else run_item<Near>(p, T, b, hk, 4 * half, chunk, t0, t1, wsm, lane, track);
     }
     item = __shfl_sync(kFull, next, 0);
   }
@@ -658,7 +667,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_gqa_kernel(const __grid
 }  // namespace
 
 bool gqa_fast_supported(int head_dim, int group, int k_fmt, int v_fmt) {
-  if (head_dim != D || (group != 1 && group != 2 && group != 4)) return false;
+  if (head_dim != D || (group != 1 && group != 2 && group != 4 && group != 8)) return false;
   return (k_fmt == KVQ_FMT_FP16 && v_fmt == KVQ_FMT_FP16) || (k_fmt == KVQ_FMT_FP8_E4M3 && v_fmt == KVQ_FMT_INT4_G32);
 }
 
@@ -697,10 +706,12 @@ cudaError_t launch_decode_gqa(const DecParams& dp, int* counter, cudaStream_t st
     g.nchunks = t.num_splits;
     g.split_begin = t.split_begin;
     g.item_begin = items;
-    items += dp.batch * dp.hkv * t.num_splits;
+    items += dp.batch * dp.hkv * t.num_splits * (dp.hq / dp.hkv == 8 ? 2 : 1);
   }
   p.num_tiers = n;
   p.group = dp.hq / dp.hkv;
+  p.halves = p.group == 8 ? 2 : 1;
+  p.igroup = p.group < 4 ? p.group : 4;
   p.trigger = trigger ? 1 : 0;
   p.q = dp.q;
   p.k_signs = dp.k_signs;

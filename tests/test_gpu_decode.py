@@ -71,6 +71,7 @@ def test_decode_edge_lengths_and_groups(group):
 
 CODE_WIDTHS = [(128, 1, 3, 3), (128, 4, 3, 3), (128, 2, 2, 4), (128, 1, 4, 2), (128, 4, 2, 3),
                (256, 1, 3, 3), (256, 4, 4, 4), (256, 2, 2, 3), (256, 4, 3, 2), (256, 1, 2, 2),
+               (128, 8, 3, 2), (128, 8, 4, 4), (256, 8, 3, 3),  # 8 heads: two 4-head items a chunk
                (64, 1, 4, 4), (64, 2, 3, 3), (64, 4, 3, 2), (64, 8, 2, 4)]  # D = 64: the generic kernel
 
 
@@ -141,10 +142,15 @@ def test_decode_head_dim_64_two_tier(group):
 
 
 @pytest.mark.gpu
-def test_decode_two_tier_edge_lengths():
-    cfg = W.CONFIGS["gqa32k"].scaled(batch=5, num_q_heads=8, num_kv_heads=2)
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+@pytest.mark.parametrize("split", [32, 0])
+def test_decode_two_tier_edge_lengths(group, split):
+    """fp16 near tier + fp8 / INT4 far tier at head_dim 128 on the fused kernel for every
+    group size (a group of 8 runs as two items of four heads per chunk), short and
+    multi-split lengths, small forced splits and the default plan."""
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=5, num_q_heads=2 * group, num_kv_heads=2)
     lens = [1, 9, 10, 11, 1234]  # near tier holds round(0.1 L): 0, 1, 1, 1, 123 tokens
-    got, want, _, _ = run_exact(cfg, lens, split_tokens=32)
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=split)
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
 
 
