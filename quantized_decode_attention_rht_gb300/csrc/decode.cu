@@ -328,7 +328,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 }
 
 // ---------------------------------------------------------------- pass 2
-// One block of kCombineWarps warps per (sequence, query head).  First every thread reads
+// One block of kCombineWarps warps (4, 8 or 16: more where each output has many splits, so
+// every warp's chain of loads stays short) per (sequence, query head).  First every thread reads
 // the (max, sum) pair of one split (all splits of every tier at once), and the block forms
 // the global max and each split's weight exp2(m_s - max); then warp w streams the
 // accumulators of splits w, w + kCombineWarps, ... with no dependence between splits (lane
@@ -336,10 +337,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
 // undoes the V rotation with a Walsh-Hadamard transform (in-register stages for the lane's
 // coordinates, shuffles across lanes).  Launched as a programmatic dependent of the split-K
 // pass: it waits for that grid's completion before touching the partials.
-constexpr int kCombineWarps = 4;
 constexpr int kCombineMaxSplits = KVQ_MAX_SPLITS;  // the plan never makes more splits per output
 
-template <int D>
+template <int D, int kCombineWarps>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecParams p) {
   constexpr int PER = D / 32;
   __shared__ float s_acc[kCombineWarps][D];
@@ -580,14 +580,14 @@ cudaError_t launch_decode(const DecParams& p, int head_dim, int group, cudaStrea
   return cudaErrorNotSupported;
 }
 
-cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
-  const int blocks = p.batch * p.hq;
-  if (blocks == 0) return cudaSuccess;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return cudaErrorNotSupported;
+namespace {
+
+template <int D, int W>
+cudaError_t launch_combine_w(const DecParams& p, cudaStream_t stream) {
   // programmatic dependent launch: the grid may be set up while the split-K pass drains
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.gridDim = dim3(p.batch * p.hq);
+  cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -595,11 +595,29 @@ cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = head_dim == 64    ? cudaLaunchKernelEx(&cfg, combine_kernel<64>, p)
-                        : head_dim == 128 ? cudaLaunchKernelEx(&cfg, combine_kernel<128>, p)
-                                          : cudaLaunchKernelEx(&cfg, combine_kernel<256>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel<D, W>, p);
   if (e == cudaSuccess) note_launch();
   return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
+template <int D>
+cudaError_t launch_combine_d(const DecParams& p, cudaStream_t stream) {
+  // warps per output from the splits one output may have (every tier's); measured on GB300:
+  // 171 splits (the append workload) 851.5 -> 836.2 us per call with 16 warps instead of 4,
+  // 39 (gqa32k) 332.9 -> 335.0 us with 8
+  if (p.total_splits > 128) return launch_combine_w<D, 16>(p, stream);
+  if (p.total_splits > 64) return launch_combine_w<D, 8>(p, stream);
+  return launch_combine_w<D, 4>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const DecParams& p, int head_dim, cudaStream_t stream) {
+  if (p.batch * p.hq == 0) return cudaSuccess;
+  if (head_dim == 64) return launch_combine_d<64>(p, stream);
+  if (head_dim == 128) return launch_combine_d<128>(p, stream);
+  if (head_dim == 256) return launch_combine_d<256>(p, stream);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace kvq
