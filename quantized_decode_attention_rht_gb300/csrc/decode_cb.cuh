@@ -257,7 +257,7 @@ constexpr int block_smem(int qtab, int table, int skt, int warps, int wsm) {
   return blk + warps * wsm + wsm > align + blk ? blk + warps * wsm + wsm : align + blk;
 }
 
-template <int D, int G, int KB, int VB, int WARPS_, int MODE_>
+template <int D, int G, int KB, int VB, int WARPS_, int MODE_, int STAGES_ = 3>
 struct Layout {
   static constexpr bool QJL = MODE_ == kModeSketch, OUT = MODE_ == kModeOutlier;
   static constexpr int KCODE = D * KB / 8;                            // code bytes of a key row
@@ -265,7 +265,7 @@ struct Layout {
   static constexpr int KBLK = PS * KROW, VBLK = PS * VROW;
   static constexpr int KNORM = PS * (QJL ? 4 : (OUT ? 4 + KVQ_OUTLIER_CHANNELS : 2));  // key side data of a page block
   static constexpr int STAGE = KBLK + VBLK + KNORM + 32;  // + 16 fp16 value norms
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = STAGES_;
   static constexpr int WARPS = WARPS_;
   static constexpr int TABLE = (1 << (2 * (KB > VB ? KB : VB))) * 256;
   static constexpr int SKT = QJL ? 4 * 256 : 0;  // 4 entries: pairs of sketch signs
@@ -832,6 +832,186 @@ struct Path1 {
   }
 };
 
+// ================================================================ G = 1, head_dim 256: 8 lanes a token
+// Plain codes at head_dim 256.  The head_dim-128 mapping (4 lanes a token, 64 coordinates a
+// lane at D = 256) needs ~250 registers and leaves 8 warps per SM to hide the table
+// lookups' latency; here lane (t, c) takes coordinates [32c, 32c + 32) of tokens t, t+4,
+// t+8 and t+12 of the page: the query pairs and the value accumulators of a lane halve
+// (168 registers), and 12 warps with two ring stages each fit the shared memory (measured
+// on the append workload: 837 us per decode call with 8 warps and the 4-lane mapping, 771
+// with 11 warps and three stages, 755 with 12 and two).  Same arithmetic as Path1 (exact
+// fp32 pair products).
+template <int KB, int VB>
+struct Path1W {
+  static constexpr int D = 256;
+  using L = Layout<D, 1, KB, VB, 12, kModePlain, 2>;
+  static constexpr int kD = D, kG = 1, kGQ = 1;
+  static constexpr bool kH8 = false;
+  static constexpr int LPT = 8, TS = 32 / LPT, TPL = PS / TS;  // lanes a token, token slots, tokens a lane
+  static constexpr int DL = D / LPT;                          // coordinates per lane and token
+  static constexpr int NP = DL / 2;                           // pair slots per lane and token
+  static constexpr int KBYTES = DL * KB / 8, VBYTES = DL * VB / 8;
+  static constexpr int KW = KBYTES / 4, VW = VBYTES / 4;
+  static constexpr float kInvD = 0.0625f;
+
+  __device__ static void build_tables(const float* kc, const float* vc, uint32_t base) {
+    Path1<D, KB, VB, kModePlain>::build_tables(kc, vc, base);
+  }
+
+  __device__ static void run_item(const CbParams& p, const Item& it, bool has_next, const Item& nx, float* qbuf,
+                                  Ring& rg, uint32_t klane, uint32_t vlane, uint32_t, int lane) {
+    const CbTier& T = p.t;
+    const int b = it.b, hk = it.hk;
+    const int t1 = min(it.len, it.t0 + T.chunk);
+    const int pg0 = it.t0 / PS, npg = item_pages(T, it);
+    const int t = lane / LPT, c = lane % LPT;
+    Feeder<L> fd;
+    fd.init(p, it, nx, npg, has_next ? item_pages(T, nx) : 0, rg, lane);
+#ifdef KVQ_SPIN_TEST
+    if (rg.issued == 0) {  // test build: poll the first slot before its copies exist, then
+      ring_wait<L>(rg, T.err, lane);  // issue them so that the drain has copies to wait for
+      rg.lost = false;
+      fd.top_up(rg);
+      rg.lost = true;
+    }
+#endif
+    fd.top_up(rg);
+    rotate_query<D, 1>(p, b, hk, 0, qbuf, lane);
+    __syncwarp();
+    u64 q2[NP], acc[NP];
+    {
+      const uint32_t base = smem_addr(qbuf + DL * c);
+#pragma unroll
+      for (int j = 0; j < NP; j += 2) {
+        const uint4 v = lds128(base + 8 * j);
+        q2[j] = pk2(__uint_as_float(v.x), __uint_as_float(v.y));
+        q2[j + 1] = pk2(__uint_as_float(v.z), __uint_as_float(v.w));
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NP; ++j) acc[j] = 0ull;
+    float m = -INFINITY, l = 0.f, mn = INFINITY;
+    constexpr float sscale = kInvD / kQScale;
+#pragma unroll 1
+    for (int i = 0; i < npg; ++i) {
+      const uint32_t st = ring_wait<L>(rg, T.err, lane);
+      if (rg.lost) break;  // nothing more is read: the item's partial is written empty below
+      uint32_t k[TPL][KW], v[TPL][VW], nk[TPL], nv[TPL];
+#pragma unroll
+      for (int r = 0; r < TPL; ++r) {
+        const int tok = t + TS * r;
+        lds_run<KBYTES>(st + tok * L::KROW + c * KBYTES, k[r]);
+        lds_run<VBYTES>(st + L::KBLK + tok * L::VROW + c * VBYTES, v[r]);
+        nk[r] = lds_u16(st + L::KBLK + L::VBLK + 2 * tok);
+        nv[r] = lds_u16(st + L::KBLK + L::VBLK + L::KNORM + 2 * tok);
+      }
+      __syncwarp();  // every lane holds its words: the slot may be refilled
+      ++rg.consumed;
+      fd.top_up(rg);
+      const int tok0 = (pg0 + i) * PS;
+      // ---- scores of the lane's four tokens, each part scaled by its own norm, then summed
+      // over the 8 lanes of a token
+      float x[TPL];
+#pragma unroll
+      for (int r = 0; r < TPL; ++r) {
+        u64 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+        for (int j = 0; j < NP; j += 2) {
+          s0 = fma2(q2[j], lut64x(field_addr<2 * KB>(k[r], 2 * KB * j, klane)), s0);
+          s1 = fma2(q2[j + 1], lut64x(field_addr<2 * KB>(k[r], 2 * KB * (j + 1), klane)), s1);
+        }
+        float a0, b0, e0, f0;
+        upk2(s0, a0, b0);
+        upk2(s1, e0, f0);
+        x[r] = ((a0 + b0) + (e0 + f0)) * (__half2float(__ushort_as_half((uint16_t)nk[r])) * sscale);
+      }
+#pragma unroll
+      for (int o = 1; o < LPT; o <<= 1)
+#pragma unroll
+        for (int r = 0; r < TPL; ++r) x[r] += __shfl_xor_sync(kFull, x[r], o);
+      bool val[TPL];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < TPL; ++r) {
+        val[r] = tok0 + t + TS * r < t1;
+        x[r] = val[r] ? x[r] : -INFINITY;
+        mt = fmaxf(mt, x[r]);
+      }
+      // ---- online softmax over the 16 tokens: the page maximum matters only where a score
+      // rises above the running maximum (and for the gate)
+      if (p.gate || __any_sync(kFull, mt > m)) {
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o));
+      }
+      if (mt > m) {
+        const float f = exp2_fast(m - mt);  // m = -inf at first: f = 0
+        l *= f;
+        const u64 f2 = pk2(f, f);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) acc[j] = mul2(acc[j], f2);
+        m = mt;
+      }
+      float pr[TPL];
+#pragma unroll
+      for (int r = 0; r < TPL; ++r) {
+        pr[r] = val[r] ? exp2_fast(x[r] - m) : 0.f;
+        l += pr[r];
+      }
+      if (p.track) {
+        float lo = INFINITY;
+#pragma unroll
+        for (int r = 0; r < TPL; ++r) lo = fminf(lo, val[r] ? x[r] : INFINITY);
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
+        mn = fminf(mn, lo);
+      }
+      if (p.gate && mt - m < -kGateLog2) continue;  // score gate: mt is warp-uniform here
+      // ---- values of the lane's four tokens
+#pragma unroll
+      for (int r = 0; r < TPL; ++r) {
+        const float w = val[r] ? pr[r] * (__half2float(__ushort_as_half((uint16_t)nv[r])) * kInvD) : 0.f;
+        const u64 W = pk2(w, w);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) acc[j] = fma2(W, lut64x(field_addr<2 * VB>(v[r], 2 * VB * j, vlane)), acc[j]);
+      }
+    }
+    if (rg.lost) {  // a wait gave up: the item contributes nothing (its partial says so)
+#pragma unroll
+      for (int j = 0; j < NP; ++j) acc[j] = 0ull;
+      m = -INFINITY;
+      l = 0.f;
+      mn = INFINITY;
+    }
+    // ---- sums over the 4 token slots of a coordinate block: reduce-scatter on lane bits 4, 3
+    float a[DL];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) upk2(acc[j], a[2 * j], a[2 * j + 1]);
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      const int msk = 16 >> s2, n = DL >> s2;
+      const bool up = lane & msk;
+#pragma unroll
+      for (int kk = 0; kk < n / 2; ++kk) {
+        const float send = up ? a[kk] : a[kk + n / 2];
+        const float keep = up ? a[kk + n / 2] : a[kk];
+        a[kk] = keep + __shfl_xor_sync(kFull, send, msk);
+      }
+    }
+#pragma unroll
+    for (int o = LPT; o < 32; o <<= 1) l += __shfl_xor_sync(kFull, l, o);
+    const size_t part = ((size_t)b * p.hq + hk) * p.total_splits + T.split_begin + it.chunk;
+    const int off = DL * c + ((lane >> 4) & 1) * (DL / 2) + ((lane >> 3) & 1) * (DL / 4);
+    float4* dst = reinterpret_cast<float4*>(p.ws_acc + part * D + off);
+#pragma unroll
+    for (int kk = 0; kk < DL / 4; kk += 4) dst[kk / 4] = make_float4(a[kk], a[kk + 1], a[kk + 2], a[kk + 3]);
+    if (lane == 0) {
+      p.ws_ml[2 * part] = m;
+      p.ws_ml[2 * part + 1] = l;
+      if (p.track) p.ws_min[part] = mn;
+    }
+  }
+};
+
 // ================================================================ G = 2, 4: tensor-core path
 // WIDE: 16 warps instead of 12 (register-limited to 128, a few spilled bytes): more warps
 // hide more of the path's latency on large caches, fewer items per warp hurt small ones.
@@ -1269,7 +1449,8 @@ cudaError_t launch_path(const CbParams& p, int sms, cudaStream_t stream) {
 
 template <int D, int G, int KB, int VB, int MODE>
 cudaError_t launch_bits(const CbParams& p, int sms, cudaStream_t s) {
-  if constexpr (G == 1) return launch_path<Path1<D, KB, VB, MODE>>(p, sms, s);
+  if constexpr (G == 1 && D == 256 && MODE == kModePlain) return launch_path<Path1W<KB, VB>>(p, sms, s);
+  else if constexpr (G == 1) return launch_path<Path1<D, KB, VB, MODE>>(p, sms, s);
   else return launch_path<PathM<D, G, KB, VB, MODE>>(p, sms, s);
 }
 
