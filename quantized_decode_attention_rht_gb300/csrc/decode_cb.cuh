@@ -832,19 +832,22 @@ struct Path1 {
   }
 };
 
-// ================================================================ G = 1, head_dim 256: 8 lanes a token
-// Plain codes at head_dim 256.  The head_dim-128 mapping (4 lanes a token, 64 coordinates a
-// lane at D = 256) needs ~250 registers and leaves 8 warps per SM to hide the table
-// lookups' latency; here lane (t, c) takes coordinates [32c, 32c + 32) of tokens t, t+4,
-// t+8 and t+12 of the page: the query pairs and the value accumulators of a lane halve
-// (168 registers), and 12 warps with two ring stages each fit the shared memory (measured
-// on the append workload: 837 us per decode call with 8 warps and the 4-lane mapping, 771
-// with 11 warps and three stages, 755 with 12 and two).  Same arithmetic as Path1 (exact
-// fp32 pair products).
-template <int KB, int VB>
+// ================================================================ G = 1: 8 lanes a token
+// Plain codes, one query head per kv head, at head_dim 256.  The 4-lanes-a-token mapping of
+// Path1 holds
+// D/4 coordinates of the query pairs and of the value accumulators per lane (~250
+// registers at D = 256: 8 warps per SM to hide the table lookups' latency); here lane
+// (t, c) takes coordinates [c D/8, (c + 1) D/8) of tokens t, t+4, t+8 and t+12 of the page,
+// which halves that state, so more warps fit: at D = 256 12 warps with two ring stages (168
+// registers; measured on the append workload: 837 us per decode call with Path1's 8 warps,
+// 771 with 11 warps and three stages, 755 with 12 and two).  Same arithmetic as Path1
+// (exact fp32 pair products).  At head_dim 128 (2- and 4-bit codes, whose runs are whole
+// words) the same mapping measured slower than Path1 on llama7b: 112.6 / 113.6 / 145 us with
+// 16 / 20 / 24 warps against 110.7 us (three shuffle stages per score instead of two, and
+// 8-byte code runs).
+template <int D, int KB, int VB, int WARPS_ = (D == 256 ? 12 : 20), int STAGES_ = (D == 256 ? 2 : 3)>
 struct Path1W {
-  static constexpr int D = 256;
-  using L = Layout<D, 1, KB, VB, 12, kModePlain, 2>;
+  using L = Layout<D, 1, KB, VB, WARPS_, kModePlain, STAGES_>;
   static constexpr int kD = D, kG = 1, kGQ = 1;
   static constexpr bool kH8 = false;
   static constexpr int LPT = 8, TS = 32 / LPT, TPL = PS / TS;  // lanes a token, token slots, tokens a lane
@@ -852,7 +855,8 @@ struct Path1W {
   static constexpr int NP = DL / 2;                           // pair slots per lane and token
   static constexpr int KBYTES = DL * KB / 8, VBYTES = DL * VB / 8;
   static constexpr int KW = KBYTES / 4, VW = VBYTES / 4;
-  static constexpr float kInvD = 0.0625f;
+  static constexpr float kInvD = D == 128 ? 0.08838834764831845f : 0.0625f;
+  static_assert(KBYTES % 4 == 0 && VBYTES % 4 == 0, "whole-word runs");
 
   __device__ static void build_tables(const float* kc, const float* vc, uint32_t base) {
     Path1<D, KB, VB, kModePlain>::build_tables(kc, vc, base);
@@ -1449,7 +1453,7 @@ cudaError_t launch_path(const CbParams& p, int sms, cudaStream_t stream) {
 
 template <int D, int G, int KB, int VB, int MODE>
 cudaError_t launch_bits(const CbParams& p, int sms, cudaStream_t s) {
-  if constexpr (G == 1 && D == 256 && MODE == kModePlain) return launch_path<Path1W<KB, VB>>(p, sms, s);
+  if constexpr (G == 1 && MODE == kModePlain && D == 256) return launch_path<Path1W<D, KB, VB>>(p, sms, s);
   else if constexpr (G == 1) return launch_path<Path1<D, KB, VB, MODE>>(p, sms, s);
   else return launch_path<PathM<D, G, KB, VB, MODE>>(p, sms, s);
 }

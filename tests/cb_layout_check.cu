@@ -42,8 +42,8 @@ void check(const char* name, int d, int g, int kb, int vb, int mode, int wide) {
 
 template <int D, int G, int KB, int VB, int MODE, bool WIDE>
 void one() {
-  if constexpr (G == 1 && D == 256 && MODE == kModePlain)
-    check<typename Path1W<KB, VB>::L>("Path1W", D, G, KB, VB, MODE, 0);
+  if constexpr (G == 1 && MODE == kModePlain && D == 256)
+    check<typename Path1W<D, KB, VB>::L>("Path1W", D, G, KB, VB, MODE, 0);
   else if constexpr (G == 1) check<typename Path1<D, KB, VB, MODE>::L>("Path1", D, G, KB, VB, MODE, 0);
   else check<typename PathM<D, G, KB, VB, MODE, WIDE>::L>("PathM", D, G, KB, VB, MODE, WIDE ? 1 : 0);
 }
