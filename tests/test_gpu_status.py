@@ -22,10 +22,13 @@ from tests import gpu_util as gu
 
 FAMILIES = {
     "fused_fp16_fp8_g4": ((W.Tier("fp16", "fp16"), W.Tier("fp8_e4m3", "int4_g32")), 4, 128),
+    "fused_fp16_fp8_g8": ((W.Tier("fp16", "fp16"), W.Tier("fp8_e4m3", "int4_g32")), 8, 128),
     "codebook_g1": ((W.Tier("codebook", "codebook", 4, 4),), 1, 128),
+    "codebook_g1_d256": ((W.Tier("codebook", "codebook", 4, 4),), 1, 256),
     "codebook_g4": ((W.Tier("codebook", "codebook", 3, 2),), 4, 128),
-    "generic_g8": ((W.Tier("codebook", "codebook", 4, 4),), 8, 128),
+    "codebook_g8": ((W.Tier("codebook", "codebook", 4, 4),), 8, 128),
     "generic_d64": ((W.Tier("fp16", "fp16"), W.Tier("fp8_e4m3", "int4_g32")), 2, 64),
+    "generic_d64_codebook": ((W.Tier("codebook", "codebook", 4, 4),), 8, 64),
 }
 
 
@@ -96,7 +99,7 @@ def _spintest_lib(kvq):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["codebook_g1", "codebook_g4"])
+@pytest.mark.parametrize("name", ["codebook_g1", "codebook_g1_d256", "codebook_g4", "codebook_g8"])
 def test_copy_wait_give_up_is_reported(name):
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
