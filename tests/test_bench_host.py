@@ -1,6 +1,6 @@
 """Host logic of the benchmark that needs no GPU: the clock record kept beside every
 number (samples of nvidia-smi inside the timed region only, median SM clock, the throttle
-reasons that were active)."""
+reasons that were active), the layer reshaping options and the traffic record's guard."""
 import os
 import sys
 import time
@@ -30,3 +30,25 @@ def test_clock_samples_inside_the_timed_region_only():
     every = bench.parse_clock_samples(lines)
     assert every["samples"] == 5 and every["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
     assert bench.parse_clock_samples(lines, t + 5, t + 6)["samples"] == 0
+
+
+def test_layer_reshaping_keeps_the_workload_and_changes_only_its_shape():
+    """--head-dim / --num-kv-heads reshape a workload (to time the shapes the fused kernels
+    leave to the generic one); every other field and the per-rank seeds stay as they were."""
+    base = bench.rank_config("llama7b", 0)
+    d64 = bench.rank_config("llama7b", 0, head_dim=64)
+    g8 = bench.rank_config("llama7b", 0, num_kv_heads=4)
+    assert (d64.head_dim, d64.num_q_heads, d64.num_kv_heads) == (64, base.num_q_heads, base.num_kv_heads)
+    assert (g8.head_dim, g8.num_q_heads, g8.num_kv_heads) == (base.head_dim, 32, 4) and g8.group == 8
+    assert d64.seed == base.seed and d64.tiers == base.tiers and d64.seq_len == base.seq_len
+    assert bench.rank_config("llama7b", 1, num_kv_heads=4).seed == base.seed + 1000
+
+
+def test_kernel_traffic_only_for_the_captured_source_and_batch():
+    """The DRAM traffic of the dominant kernel is reported only for the batch it was captured
+    at (its split-K partial writes do not grow with the batch) and only while the kernel
+    source is the captured one."""
+    t = bench.TRAFFIC["gqa32k"]
+    assert bench.kernel_traffic("gqa32k", t["captured_batch"]) in (None, t["bytes"])
+    assert bench.kernel_traffic("gqa32k", t["captured_batch"] // 2) is None
+    assert bench.kernel_traffic("llama7b", 8) is None
