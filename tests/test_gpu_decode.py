@@ -318,3 +318,26 @@ def test_full_size_sampled_heads(name):
         err = np.abs(got[b, h] - want).max()
         print(f"{name} b={b} h={h}: max-abs {err:.3e} (|out| max {np.abs(want).max():.2f})")
         assert err <= gu.ATOL_OUT
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("group,kb,vb,width", [(8, 4, 4, 65536), (8, 3, 2, 131072), (4, 3, 2, 131072)])
+def test_codebook_large_cache_instances(group, kb, vb, width):
+    """The 16-warp tensor-core codebook instances, which the library picks for caches of 512 MB
+    and more (sized by the block table's width), on short sequences: a block table `width`
+    pages wide whose unused entries name page 0, 4096-token splits.  Eight query heads per kv
+    head run as two 4-head items a chunk there too."""
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_module()
+    hkv = 2
+    cfg = W.CONFIGS["llama7b"].scaled(batch=2, num_q_heads=hkv * group, num_kv_heads=hkv,
+                                      tiers=(W.Tier("codebook", "codebook", kb, vb),))
+    lens = [3000, 1700]
+    _, want, built, q = run_exact(cfg, lens)
+    views = []
+    for v in built.views:
+        bt = torch.zeros((len(lens), width), dtype=torch.int32, device="cuda")
+        bt[:, :v.block_table.shape[1]] = v.block_table
+        views.append(kvq.TierView(v.cache, bt, v.seq_lens))
+    got = gu.gpu_decode(kvq, torch, views, q, split_tokens=4096)
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
