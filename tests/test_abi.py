@@ -291,3 +291,20 @@ def test_make_signs_argument_checks(kvq):
     assert lib.kvq_make_signs(0, 1 << 24, 1, 128, buf.ctypes.data, buf.ctypes.data) == 1
     assert lib.kvq_make_signs(0, 0, 0, 128, buf.ctypes.data, buf.ctypes.data) == 1
     assert lib.kvq_make_signs(0, 0, 1, 96, buf.ctypes.data, buf.ctypes.data) == 2
+
+
+def test_eight_query_heads_per_kv_head(kvq):
+    """Eight query heads per kv head: plain codebook tiers (D 128, 256), fp16 and fp8 / INT4
+    tiers (D 128) and the generic kernel (D 64) accept the call; keys with a residual sketch or
+    an outlier stream, which only the codebook kernel's 1/2/4-head instances read, refuse it
+    before any launch."""
+    hq = 8 * 2  # the fake caches have 2 kv heads
+    assert _ws(kvq, [_fake_cache(kvq)], hq=hq)[0] == 0
+    assert _ws(kvq, [_fake_cache(kvq, head_dim=256)], hq=hq)[0] == 0
+    assert _ws(kvq, [_fake_cache(kvq, head_dim=64)], hq=hq)[0] == 0
+    assert _ws(kvq, [_fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_bits=0, v_bits=0),
+                     _fake_cache(kvq, k_format=kvq.FMT_FP8_E4M3, k_bits=0, v_format=kvq.FMT_INT4_G32, v_bits=0)],
+               hq=hq)[0] == 0
+    assert _ws(kvq, [_qjl_cache(kvq)], hq=hq)[0] == 2
+    assert _ws(kvq, [_outl_cache(kvq)], hq=hq)[0] == 2
+    assert _ws(kvq, [_qjl_cache(kvq)], hq=4 * 2)[0] == 0 and _ws(kvq, [_outl_cache(kvq)], hq=4 * 2)[0] == 0
