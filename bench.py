@@ -320,38 +320,66 @@ def step_bytes(cfg, wl, kvq):
     return dec, quant
 
 
-def output_error_vs_fp16(cfg, wl, q_host, out, k_new, v_new, window, samples=4):
+def quality_pairs(cfg):
+    """The (sequence, query head) pairs the quality record samples: every kv head, the first
+    and last query head of its group, in the first and last sequence -- the same pairs
+    whatever the batch (a random handful can miss the kv heads that carry outlier channels,
+    where the compression loses most)."""
+    seqs = sorted({0, cfg.batch - 1})
+    heads = sorted({h for g in range(cfg.num_kv_heads) for h in (g * cfg.group, (g + 1) * cfg.group - 1)})
+    return [(b, h) for b in seqs for h in heads]
+
+
+def _error_stats(errs, coss):
+    import numpy as np
+    if not errs:
+        return {"pairs": 0}
+    return {"pairs": len(errs), "rel_err_mean": float(np.mean(errs)), "rel_err_max": float(np.max(errs)),
+            "cosine_mean": float(np.mean(coss)), "cosine_min": float(np.min(coss))}
+
+
+def output_error_vs_fp16(cfg, wl, q_host, out, k_new, v_new, window):
     """Relative error of the decode output against exact attention over the UNQUANTISED fp16
-    cache (the quality cost of the compression, not a parity check): for a few (sequence,
-    query head) pairs, softmax(q K^T / sqrt(d)) V in float64 over the fp16 keys and values
+    cache (the quality cost of the compression, not a parity check): for the pairs of
+    `quality_pairs`, softmax(q K^T / sqrt(d)) V in float64 over the fp16 keys and values
     the cache holds -- the seeded inputs, with the token each step overwrote replaced by the
     step's new one.  Plain numpy; returns the mean and max of ||out - exact|| / ||exact||
     and the mean and min of the cosine between out and exact (the measure the FoveatedKV
-    page quotes, "0.995+ cosine fidelity vs exact fp16 attention", and AdapTQ's 0.947)."""
+    page quotes, "0.995+ cosine fidelity vs exact fp16 attention", and AdapTQ's 0.947),
+    over all pairs and apart for the kv heads with and without outlier channels."""
     import numpy as np
     import workloads as W
-    rng = np.random.default_rng(5)
-    picks = sorted({(int(rng.integers(cfg.batch)), int(rng.integers(cfg.num_q_heads))) for _ in range(samples)})
-    errs, coss = [], []
-    for b, h in picks:
+    mult = W.outlier_multipliers(cfg)
+    errs, coss, kind = [], [], []
+    kv = {}
+    for b, h in quality_pairs(cfg):
         g = h // cfg.group
         n = int(wl.lens[b])
-        k = W.kv_head(cfg, 0, b, g, n).astype(np.float64)
-        v = W.kv_head(cfg, 1, b, g, n).astype(np.float64)
-        members = W.tier_members(cfg, b, g, n)[-1]
-        if len(members):
-            i = members[0] if window else members[-1]  # the slot the bench step writes
-            k[i], v[i] = k_new[b, g], v_new[b, g]
+        if (b, g) not in kv:
+            kv.clear()
+            k = W.kv_head(cfg, 0, b, g, n).astype(np.float64)
+            v = W.kv_head(cfg, 1, b, g, n).astype(np.float64)
+            members = W.tier_members(cfg, b, g, n)[-1]
+            if len(members):
+                i = members[0] if window else members[-1]  # the slot the bench step writes
+                k[i], v[i] = k_new[b, g], v_new[b, g]
+            kv[(b, g)] = (k, v)
+        k, v = kv[(b, g)]
         s = k @ q_host[b, h].astype(np.float64) / np.sqrt(cfg.head_dim)
         w = np.exp(s - s.max())
         exact = (w / w.sum()) @ v
         o = out[b, h].astype(np.float64)
         errs.append(float(np.linalg.norm(o - exact) / np.linalg.norm(exact)))
         coss.append(float(o @ exact / (np.linalg.norm(o) * np.linalg.norm(exact))))
+        kind.append(bool((mult[g] != 1.0).any()))
+    pick = lambda flag: ([e for e, f in zip(errs, kind) if f == flag], [c for c, f in zip(coss, kind) if f == flag])
     return {"rel_err_vs_fp16_cache": {"mean": float(np.mean(errs)), "max": float(np.max(errs))},
             "cosine_vs_fp16_cache": {"mean": float(np.mean(coss)), "min": float(np.min(coss))},
-            "sample": f"{len(picks)} (sequence, query head) pairs; exact softmax(qK^T/sqrt(d))V over the "
-                      "unquantised fp16 K/V in float64"}
+            "kv_heads_with_outlier_channels": _error_stats(*pick(True)),
+            "kv_heads_without_outlier_channels": _error_stats(*pick(False)),
+            "sample": f"{len(errs)} (sequence, query head) pairs: the first and last sequence x the first and "
+                      "last query head of every kv head; exact softmax(qK^T/sqrt(d))V over the unquantised "
+                      "fp16 K/V in float64"}
 
 
 def quantize_throughput(kvq, torch, reps=5, tokens=0):

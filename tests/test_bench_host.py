@@ -52,3 +52,52 @@ def test_kernel_traffic_only_for_the_captured_source_and_batch():
     assert bench.kernel_traffic("gqa32k", t["captured_batch"]) in (None, t["bytes"])
     assert bench.kernel_traffic("gqa32k", t["captured_batch"] // 2) is None
     assert bench.kernel_traffic("llama7b", 8) is None
+
+
+def test_quality_sample_covers_every_kv_head_whatever_the_batch():
+    """The quality record samples the first and last query head of every kv head in the first
+    and last sequence, so the kv heads with outlier channels are always in it, and it splits
+    the error between kv heads with and without them."""
+    import types
+    import numpy as np
+    import workloads as W
+    from oracle.attention import attend
+
+    for batch in (1, 4, 32):
+        cfg = W.CONFIGS["gqa32k"].scaled(batch=batch)
+        pairs = bench.quality_pairs(cfg)
+        assert {h // cfg.group for _, h in pairs} == set(range(cfg.num_kv_heads))
+        assert {b for b, _ in pairs} == {0, batch - 1}
+        assert len(pairs) == len(set(pairs)) == len({0, batch - 1}) * cfg.num_kv_heads * 2
+
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=2, seq_len=96)
+    wl = types.SimpleNamespace(lens=W.seq_lens(cfg))
+    q = W.queries(cfg)
+    k_new = np.stack([[W.kv_head(cfg, 0, b, g, 1, stream=7)[0] for g in range(cfg.num_kv_heads)]
+                      for b in range(cfg.batch)])
+    v_new = np.stack([[W.kv_head(cfg, 1, b, g, 1, stream=7)[0] for g in range(cfg.num_kv_heads)]
+                      for b in range(cfg.batch)])
+    out = np.zeros((cfg.batch, cfg.num_q_heads, cfg.head_dim))
+    for b in range(cfg.batch):  # exact attention over the fp16 cache with the step's token in place
+        for g in range(cfg.num_kv_heads):
+            n = int(wl.lens[b])
+            k = W.kv_head(cfg, 0, b, g, n).astype(np.float64)
+            v = W.kv_head(cfg, 1, b, g, n).astype(np.float64)
+            i = W.tier_members(cfg, b, g, n)[-1][-1]
+            k[i], v[i] = k_new[b, g], v_new[b, g]
+            for h in range(g * cfg.group, (g + 1) * cfg.group):
+                out[b, h] = attend(q[b, h].astype(np.float64), k, v)
+    got = bench.output_error_vs_fp16(cfg, wl, q, out, k_new, v_new, window=False)
+    assert got["rel_err_vs_fp16_cache"]["max"] < 1e-12 and got["cosine_vs_fp16_cache"]["min"] > 1 - 1e-12
+    with_out = {g for g in range(cfg.num_kv_heads) if (W.outlier_multipliers(cfg)[g] != 1).any()}
+    assert 0 < len(with_out) < cfg.num_kv_heads
+    assert got["kv_heads_with_outlier_channels"]["pairs"] == 2 * 2 * len(with_out)
+    assert got["kv_heads_without_outlier_channels"]["pairs"] == 2 * 2 * (cfg.num_kv_heads - len(with_out))
+
+    # a wrong output on one kv head with outlier channels shows in that bucket only
+    g = min(with_out)
+    bad = out.copy()
+    bad[0, g * cfg.group] *= -1.0
+    got = bench.output_error_vs_fp16(cfg, wl, q, bad, k_new, v_new, window=False)
+    assert abs(got["kv_heads_with_outlier_channels"]["cosine_min"] + 1.0) < 1e-9
+    assert got["kv_heads_without_outlier_channels"]["cosine_min"] > 1 - 1e-12
