@@ -123,7 +123,10 @@ typedef struct kvq_cache {
                            with a sketch are appended at 128 or 256 and decoded at 128;
                            anything else returns KVQ_ERR_UNSUPPORTED */
   int32_t num_kv_heads; /* Hkv >= 1 */
-  int32_t page_size;    /* tokens per page, 16 */
+  int32_t page_size;    /* tokens per page, >= 1; 16 is the size the fused decode kernels
+                           take, any other decodes on the generic kernel (a decode of keys
+                           with a sketch or an outlier stream needs 16, else
+                           KVQ_ERR_UNSUPPORTED; appends take any size) */
   int32_t num_pages;    /* pages in the pool */
   int32_t k_format;     /* kvq_format of keys   */
   int32_t v_format;     /* kvq_format of values */

@@ -91,6 +91,32 @@ def test_decode_code_widths(d, group, kb, vb):
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
 
 
+# (head_dim, query heads per kv head, page size, tiers): pools whose pages are not 16 tokens
+# run on the generic kernel, whose warps step through a page TPS tokens at a time (16 at
+# D = 64 with one head per kv head, 8 at D = 128, 4 at D = 128 with two heads or D = 256
+# with one, 2 at D = 128 with four, 1 with eight); sizes that are no multiple of TPS leave
+# the last step of a page part empty, a one-token page is all tail
+_CB44 = (W.Tier("codebook", "codebook", 4, 4),)
+_TWO_TIER = W.CONFIGS["gqa32k"].tiers
+PAGE_SIZES = [(64, 1, 24, _CB44), (64, 1, 5, _CB44), (128, 1, 12, _CB44), (128, 2, 6, _CB44),
+              (256, 1, 10, _CB44), (128, 4, 1, _CB44), (128, 8, 3, _CB44), (128, 4, 32, _CB44),
+              (128, 4, 24, _TWO_TIER), (128, 1, 7, _TWO_TIER)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d,group,ps,tiers", PAGE_SIZES)
+def test_decode_page_sizes(d, group, ps, tiers):
+    """Pages of other sizes than 16 tokens (the generic kernel): lengths of one token, one
+    page, a page and a token, and a ragged several-split one, on shuffled pages."""
+    hkv = 2
+    cfg = W.CONFIGS["llama7b"].scaled(batch=4, num_q_heads=hkv * group, num_kv_heads=hkv, head_dim=d,
+                                      page_size=ps, tiers=tiers)
+    lens = [1, ps, ps + 1, 333]
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=4 * ps, shuffle=5)
+    assert np.all(np.isfinite(got))
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
 QJL_WIDTHS = [(1, 3, 4), (1, 2, 2), (2, 2, 3), (2, 4, 4), (4, 4, 4), (4, 3, 2)]
 
 

@@ -59,9 +59,23 @@ SIZES = [203, 5600]
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("fmt,bits", FORMATS)
 def test_quantize_matches_oracle(fmt, bits, d, n):
+    check_append(fmt, bits, d, n, 16)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("fmt,bits,d,ps", [("codebook", 4, 128, 1), ("codebook", 3, 256, 12), ("int4_g32", 0, 128, 24),
+                                           ("codebook", 2, 64, 32), ("fp8_e4m3", 0, 128, 7)])
+def test_quantize_page_sizes(fmt, bits, d, ps, n):
+    """Pools with pages of other sizes than 16 tokens: powers of two (the kernels shift the
+    slot) and others (they divide it), on both append kernels."""
+    check_append(fmt, bits, d, n, ps)
+
+
+def check_append(fmt, bits, d, n, ps):
     torch = gu.torch_cuda()
     kvq = gu.kvq_module()
-    k, v, ks, vs, slots, cache = run_append(kvq, torch, fmt, bits, d, n=n, seed=d + bits)
+    k, v, ks, vs, slots, cache = run_append(kvq, torch, fmt, bits, d, n=n, ps=ps, seed=d + bits)
     keep = np.flatnonzero((slots >= 0) & (slots < cache.num_pages * cache.page_size))
     assert np.all(keep[:DEGENERATE] == np.arange(DEGENERATE))
     stats = []
