@@ -213,10 +213,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_tier_kernel(const DecParam
     const size_t row_base = ((size_t)phys * p.hkv + hk) * p.page_size;
     for (int s0 = 0; s0 < p.page_size; s0 += TPS) {
       const int off = s0 + gi;
-      const int t = lp * p.page_size + off;
-      // a page size that is not a multiple of TPS leaves the last step's upper lanes past
-      // the page: their slots belong to the next (page, kv head) block
-      const bool valid = off < p.page_size && t < t_end;
+      const bool valid = slot_holds_token(lp, off, p.page_size, t_end);
       const size_t rowid = row_base + off;
       float x[DPL], ks = 0.f;
       if (valid) Row<KF, D, DPL>::load(T.k_rows, T.k_aux, rowid, T.k_row_bytes, e0, lut_k, x, ks);

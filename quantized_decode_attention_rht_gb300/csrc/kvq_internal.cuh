@@ -89,6 +89,13 @@ __host__ __device__ __forceinline__ int splits_holding_tokens(int len, int chunk
   const int n = (len + chunk - 1) / chunk;
   return n < num_splits ? n : num_splits;
 }
+// Whether slot `off` of logical page `lp` holds one of a chunk's tokens (those before
+// t_end): it must lie inside the page -- a page size that is no multiple of the tokens a
+// warp step covers leaves the last step's upper lanes past the page, on the next (page,
+// kv head) block's rows -- and before the chunk's end.
+__host__ __device__ __forceinline__ bool slot_holds_token(int lp, int off, int page_size, int t_end) {
+  return off < page_size && (long long)lp * page_size + off < t_end;
+}
 
 struct DecTier {
   const uint8_t* k_rows;
