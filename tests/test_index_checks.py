@@ -2,7 +2,9 @@
 csrc/kvq_internal.cuh that every decode kernel applies to the lengths and block-table
 entries it reads (clamp a length into [0, max_pages * page_size], skip a page outside the
 pool, never read more splits than the plan made), each raising its KVQ_DEVERR_* bit, are
-compiled for the CPU with nvcc and fed out-of-range values -- on the CPU only."""
+compiled for the CPU with nvcc and fed out-of-range values -- on the CPU only.  The same
+program walks the generic decode kernel's page loop with its slot test for every page size
+up to 40 and every warp step width: each token of a chunk once, no lane past its page."""
 import os
 import shutil
 import subprocess
