@@ -117,6 +117,27 @@ def test_decode_page_sizes(d, group, ps, tiers):
     assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
 
 
+# the most tiers one call attends (KVQ_MAX_TIERS): fp16 near and fp8 / INT4 far tiers (one
+# launch of the fused fp16 / fp8 kernel, with the window below), a 4-bit codebook tier (the
+# codebook kernel) and an fp16 recent-token window
+FOUR_TIERS = (W.Tier("fp16", "fp16", fraction=0.1), W.Tier("fp8_e4m3", "int4_g32", fraction=0.4),
+              W.Tier("codebook", "codebook", 4, 4), W.Tier("fp16", "fp16", window=64))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("split", [0, 64])
+@pytest.mark.parametrize("group", [1, 4, 8])
+def test_decode_four_tiers(group, split):
+    """One softmax over four tiers of three kernel families, lengths from one token (the
+    window alone) to several splits of every tier."""
+    hkv = 2
+    cfg = W.CONFIGS["gqa32k"].scaled(batch=4, num_q_heads=hkv * group, num_kv_heads=hkv, tiers=FOUR_TIERS)
+    lens = [1, 63, 700, 2111]
+    got, want, _, _ = run_exact(cfg, lens, split_tokens=split, shuffle=3)
+    assert np.all(np.isfinite(got))
+    assert np.abs(got - want).max() <= 1e-4 * max(1.0, np.abs(want).max())
+
+
 QJL_WIDTHS = [(1, 3, 4), (1, 2, 2), (2, 2, 3), (2, 4, 4), (4, 4, 4), (4, 3, 2)]
 
 
