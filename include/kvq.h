@@ -256,7 +256,11 @@ KVQ_API kvq_status kvq_outlier_calibrate(const uint16_t* k, int32_t num_tokens, 
  * split_tokens: tokens per split-K chunk (a multiple of page_size), or 0 to let the
  * library choose; pass the same value to kvq_decode_attention.  The chunks of the longest
  * possible sequence (max_pages * page_size tokens per tier), summed over the tiers, may not
- * exceed KVQ_MAX_SPLITS: a smaller split_tokens returns KVQ_ERR_UNSUPPORTED. */
+ * exceed KVQ_MAX_SPLITS: a smaller split_tokens returns KVQ_ERR_UNSUPPORTED.  With 0 the
+ * library sizes chunks for the GPU's item count and lengthens them where a long block table
+ * would need more splits (few sequences at long context); chunks of the fused fp16 / fp8
+ * kernel stop at 2048 tokens, so its tiers take block tables of at most KVQ_MAX_SPLITS x
+ * 2048 tokens in total, other tiers 2^20 tokens a chunk. */
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t num_tiers,
                                              int32_t batch, int32_t num_q_heads,
                                              int32_t split_tokens, size_t* bytes);

@@ -179,6 +179,27 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
     plan->splits[i] = max_len == 0 ? 0 : (int)((max_len + chunk - 1) / chunk);
     plan->total += plan->splits[i];
   }
+  // Chunks sized for the item count are short where few (sequence, kv head) pairs share a
+  // long block table (batch 1 at long context): one sequence would then need more splits
+  // than the combine pass holds.  The chunks the library chose double, each within its
+  // kernel's longest, until the splits fit; a plan that already fits stays as it is.
+  while (split_tokens == 0 && plan->total > KVQ_MAX_SPLITS) {
+    bool grew = false;
+    plan->total = 0;
+    for (int i = 0; i < n; ++i) {
+      const long long cap = plan->kind[i] == TIER_GQA ? gqa_max_chunk_tokens()
+                                                      : std::max<long long>(ps, (1LL << 20) / ps * ps);
+      const long long next = std::min<long long>(cap, 2LL * plan->chunk[i]);
+      if (next > plan->chunk[i]) {
+        plan->chunk[i] = (int)next;
+        grew = true;
+      }
+      const long long max_len = (long long)usable_pages(tiers[i]) * ps;
+      plan->splits[i] = max_len == 0 ? 0 : (int)((max_len + plan->chunk[i] - 1) / plan->chunk[i]);
+      plan->total += plan->splits[i];
+    }
+    if (!grew) break;
+  }
   // the combine pass keeps the per-split weights of one output in shared memory
   if (plan->total > KVQ_MAX_SPLITS) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;

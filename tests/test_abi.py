@@ -308,3 +308,25 @@ def test_eight_query_heads_per_kv_head(kvq):
     assert _ws(kvq, [_qjl_cache(kvq)], hq=hq)[0] == 2
     assert _ws(kvq, [_outl_cache(kvq)], hq=hq)[0] == 2
     assert _ws(kvq, [_qjl_cache(kvq)], hq=4 * 2)[0] == 0 and _ws(kvq, [_outl_cache(kvq)], hq=4 * 2)[0] == 0
+
+
+def test_library_chosen_chunks_fit_long_block_tables(kvq):
+    """With split_tokens = 0 the chunks sized for the GPU's item count lengthen where one
+    long sequence would need more splits than KVQ_MAX_SPLITS (few sequences at long
+    context); the fused fp16 / fp8 kernel's chunks stop at 2048 tokens, so its tiers refuse
+    block tables of more than KVQ_MAX_SPLITS x 2048 tokens in total.  An explicit split size
+    is taken as given."""
+    def fp16(**kw):
+        return _fake_cache(kvq, k_format=kvq.FMT_FP16, v_format=kvq.FMT_FP16, k_bits=0, v_bits=0,
+                           num_pages=1 << 20, **kw)
+
+    for hkv, hq in ((2, 4), (8, 32)):
+        for c in (fp16(num_kv_heads=hkv), _fake_cache(kvq, num_kv_heads=hkv, num_pages=1 << 20),
+                  _fake_cache(kvq, num_kv_heads=hkv, num_pages=1 << 20, page_size=8)):
+            for mp in (4096, 65536, 131072):  # up to 2,097,152 tokens (1,048,576 at page size 8)
+                assert _ws(kvq, [c], batch=1, hq=hq, max_pages=mp)[0] == 0, (hkv, c.k_format, c.page_size, mp)
+    assert _ws(kvq, [fp16()], batch=1, hq=4, max_pages=1024 * 128)[0] == 0
+    assert _ws(kvq, [fp16()], batch=1, hq=4, max_pages=1024 * 128 + 1)[0] == 2
+    assert _ws(kvq, [fp16(), fp16()], batch=1, hq=4, max_pages=512 * 128)[0] == 0
+    assert _ws(kvq, [fp16(), fp16()], batch=1, hq=4, max_pages=512 * 128 + 1)[0] == 2
+    assert _ws(kvq, [fp16()], batch=1, hq=4, split=16, max_pages=1025)[0] == 2
