@@ -260,7 +260,9 @@ KVQ_API kvq_status kvq_outlier_calibrate(const uint16_t* k, int32_t num_tokens, 
  * library sizes chunks for the GPU's item count and lengthens them where a long block table
  * would need more splits (few sequences at long context); chunks of the fused fp16 / fp8
  * kernel stop at 2048 tokens, so its tiers take block tables of at most KVQ_MAX_SPLITS x
- * 2048 tokens in total, other tiers 2^20 tokens a chunk. */
+ * 2048 tokens in total, other tiers 2^20 tokens a chunk.  A tier on the generic kernel
+ * (page sizes other than 16, D = 64, format pairs the fused kernels do not take) takes at
+ * most 65535 sequences a call (KVQ_ERR_UNSUPPORTED beyond). */
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_tier_view* tiers, int32_t num_tiers,
                                              int32_t batch, int32_t num_q_heads,
                                              int32_t split_tokens, size_t* bytes);

@@ -139,6 +139,8 @@ kvq_status make_plan(const kvq_tier_view* tiers, int n, int batch, int hq, int s
   size_t family_bytes[3] = {0, 0, 0};
   for (int i = 0; i < n; ++i) {
     plan->kind[i] = tier_kind(tiers[i].cache, group, split_tokens, q16);
+    // the generic kernel's grid has the sequences in its z and the kv heads in its y extent
+    if (plan->kind[i] == TIER_GENERIC && (batch > 65535 || hkv > 65535)) return KVQ_ERR_UNSUPPORTED;
     family_bytes[plan->kind[i]] += (size_t)batch * hkv * usable_pages(tiers[i]) * ps * token_bytes(tiers[i].cache);
   }
   plan->total = 0;

@@ -330,3 +330,13 @@ def test_library_chosen_chunks_fit_long_block_tables(kvq):
     assert _ws(kvq, [fp16(), fp16()], batch=1, hq=4, max_pages=512 * 128)[0] == 0
     assert _ws(kvq, [fp16(), fp16()], batch=1, hq=4, max_pages=512 * 128 + 1)[0] == 2
     assert _ws(kvq, [fp16()], batch=1, hq=4, split=16, max_pages=1025)[0] == 2
+
+
+def test_generic_kernel_batch_limit(kvq):
+    """The generic kernel's grid holds the sequences in its z extent: a tier on it takes at
+    most 65535 sequences a call, refused before any launch beyond; the fused kernels, which
+    are persistent, take any batch."""
+    generic = _fake_cache(kvq, page_size=8)
+    assert _ws(kvq, [generic], batch=65535, hq=4, max_pages=2)[0] == 0
+    assert _ws(kvq, [generic], batch=65536, hq=4, max_pages=2)[0] == 2
+    assert _ws(kvq, [_fake_cache(kvq)], batch=65536, hq=4, max_pages=2)[0] == 0
