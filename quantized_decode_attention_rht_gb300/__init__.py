@@ -130,6 +130,23 @@ def _dense(*tensors) -> None:
             raise ValueError("tensors passed to libkvq must be contiguous")
 
 
+def _arg(t, name: str, dtype: str, shape=None, min_numel: int = 0) -> None:
+    """The C ABI takes device pointers of fixed element types: refuse a host tensor, another
+    dtype, a shape that disagrees with the call (None entries in `shape` are free) or fewer
+    elements than the call reads, before the library is called."""
+    if t is None:
+        return
+    import torch
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != getattr(torch, dtype):
+        raise TypeError(f"{name} must be torch.{dtype}, got {t.dtype}")
+    if shape is not None and (t.dim() != len(shape) or any(w is not None and w != n for w, n in zip(shape, t.shape))):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)} (None: any)")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, the call reads {min_numel}")
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -200,7 +217,12 @@ def kvq_make_signs(seed: int, layer: int, num_kv_heads: int, head_dim: int):
 def kvq_quantize_append(cache: KvqCache, k, v, slot_mapping, stream=None) -> None:
     """k, v: fp16 CUDA tensors [T, Hkv, D] (either may be None); slot_mapping: int32 [T]."""
     _dense(k, v, slot_mapping)
+    if k is None and v is None:
+        raise ValueError("kvq_quantize_append needs k or v")
     t = (k if k is not None else v).shape[0]
+    for x, name in ((k, "k"), (v, "v")):
+        _arg(x, name, "float16", (t, cache.num_kv_heads, cache.head_dim))
+    _arg(slot_mapping, "slot_mapping", "int32", (None,), min_numel=t)
     _check(lib().kvq_quantize_append(ctypes.byref(cache), _ptr(k), _ptr(v), t, _ptr(slot_mapping),
                                      _stream(stream)), "kvq_quantize_append")
 
@@ -209,7 +231,9 @@ def kvq_outlier_calibrate(k, out_idx, stream=None) -> None:
     """k: fp16 CUDA tensor [N, Hkv, D] (the calibration tokens' keys); out_idx: int32 CUDA
     tensor [Hkv, OUTLIER_CHANNELS], written with each head's largest-variance channels."""
     _dense(k, out_idx)
+    _arg(k, "k", "float16", (None, None, None))
     n, hkv, d = k.shape
+    _arg(out_idx, "out_idx", "int32", (hkv, OUTLIER_CHANNELS))
     _check(lib().kvq_outlier_calibrate(_ptr(k), n, hkv, d, _ptr(out_idx), _stream(stream)), "kvq_outlier_calibrate")
 
 
@@ -217,14 +241,22 @@ def kvq_requantize(src: KvqCache, src_slots, dst: KvqCache, dst_slots, stream=No
     """Move tokens from an fp16 tier (a recent-token window) into another tier, re-encoding
     their rows; src_slots / dst_slots: int32 CUDA tensors [T]."""
     _dense(src_slots, dst_slots)
+    _arg(src_slots, "src_slots", "int32", (None,))
+    _arg(dst_slots, "dst_slots", "int32", (None,), min_numel=int(src_slots.shape[0]))
     _check(lib().kvq_requantize(ctypes.byref(src), _ptr(src_slots), ctypes.byref(dst), _ptr(dst_slots),
                                 int(src_slots.shape[0]), _stream(stream)), "kvq_requantize")
 
 
-def _views(tiers: Sequence["TierView"]):
+def _views(tiers: Sequence["TierView"], batch: int = 0):
+    """The tiers as the C ABI's array; `batch` > 0: the call reads that many rows of every
+    block table and entries of every length array."""
     arr = (KvqTierView * len(tiers))()
     for i, t in enumerate(tiers):
         _dense(t.block_table, t.seq_lens)
+        _arg(t.block_table, "block_table", "int32", (None, None))
+        _arg(t.seq_lens, "seq_lens", "int32", (None,), min_numel=batch)
+        if batch and t.block_table is not None and t.block_table.shape[0] < batch:
+            raise ValueError(f"block_table has {t.block_table.shape[0]} rows for {batch} sequences")
         arr[i].cache = ctypes.pointer(t.cache.struct)
         arr[i].block_table = _ptr(t.block_table)
         arr[i].seq_lens = _ptr(t.seq_lens)
@@ -240,6 +272,15 @@ def kvq_decode_workspace_size(tiers, batch: int, num_q_heads: int, split_tokens:
     return n.value
 
 
+def _decode_args(tiers, q, out):
+    """q: fp16 [B, Hq, D] with D the tiers' head_dim; out: fp32 of q's shape.  Returns (B, Hq)."""
+    if not tiers:
+        raise ValueError("decode attention needs at least one tier")
+    _arg(q, "q", "float16", (None, None, tiers[0].cache.struct.head_dim))
+    _arg(out, "out", "float32", tuple(q.shape))
+    return int(q.shape[0]), int(q.shape[1])
+
+
 def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream=None, score_gate: bool = False,
                          spike_flags=None, status=None) -> None:
     """q: fp16 [B, Hq, D]; out: fp32 [B, Hq, D]; workspace: uint8 CUDA tensor.
@@ -247,8 +288,12 @@ def kvq_decode_attention(tiers, q, out, workspace, split_tokens: int = 0, stream
     element, receives the call's DEVERR_* bits): the options of kvq_decode_attention_ex
     (FoveatedKV score-gated value loading and spike detection, the device error report)."""
     _dense(q, out, workspace, spike_flags, status)
-    arr = _views(tiers)
-    b, hq, _ = q.shape
+    b, hq = _decode_args(tiers, q, out)
+    _arg(spike_flags, "spike_flags", "int32", (b, hq))
+    _arg(status, "status", "int32", None, min_numel=1)
+    if workspace is not None and not getattr(workspace, "is_cuda", False):
+        raise ValueError("workspace must be a CUDA tensor")
+    arr = _views(tiers, b)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if not score_gate and spike_flags is None and status is None:
         _check(lib().kvq_decode_attention(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out),
@@ -267,8 +312,8 @@ def kvq_decode_attention_noalloc(tiers, q, out, split_tokens: int = 0, stream=No
     for callers that may not allocate device memory.  Calls that overlap on the GPU race on
     the shared scratch."""
     _dense(q, out)
-    arr = _views(tiers)
-    b, hq, _ = q.shape
+    b, hq = _decode_args(tiers, q, out)
+    arr = _views(tiers, b)
     _check(lib().kvq_decode_attention_noalloc(arr, len(tiers), _ptr(q), b, hq, split_tokens, _ptr(out),
                                               _stream(stream)), "kvq_decode_attention_noalloc")
 
